@@ -1,0 +1,191 @@
+/*
+ * lmkv.h -- C ABI of liblmkv.so: batched paged-KV chunk gather / scatter on
+ * GB300 (sm_103a).
+ *
+ * What the calls compute.  An inference engine keeps each layer's KV cache
+ * in small fixed-size pages ("blocks") of block_size tokens, addressed per
+ * request through a block table.  LMCache moves KV cache in large chunks
+ * instead of pages: a GPU kernel copies the scattered pages of many layers
+ * into a contiguous streaming buffer of 256-token chunks, which is then moved
+ * as a whole; on load the chunks are split back into pages by a kernel
+ * ("LMCache: An Efficient KV Cache Layer for Enterprise-Scale LLM Inference",
+ * section on the configurable chunk size).  The layer-wise pipeline moves one
+ * layer at a time so that transfer overlaps compute (same paper, section on
+ * the layer-wise pipeline).  The store entry point of the engine cuts tokens
+ * into chunk_size chunks, keeps a tail shorter than a chunk only when
+ * save_unfull_chunk is set, and requires the already-cached prefix to be a
+ * multiple of chunk_size ("LMCache 源码解析", cache_engine.py walk-through,
+ * section "store()").
+ *
+ * Notation: L = num_layers, HD = num_kv_heads * head_dim, e = elem_bytes,
+ * B = block_size, C = chunk_size, row = HD * e bytes (one token of K or V of
+ * one layer).
+ *
+ * Layouts (all row-major, contiguous):
+ *   pool layer l  : [2][num_blocks][B][HD]   (index 0 = K, 1 = V)
+ *   block table   : int32 [num_req][max_blocks]; entry [r][t / B] is the
+ *                   block that holds token t of request r
+ *   chunk g       : [2][L][n_g][HD]           (n_g = tokens in chunk g)
+ *   fp8 codes g   : uint8 [2][L][n_g][HD]     (float8 e4m3fn bit patterns)
+ *   fp8 scales    : float32 [num_chunks][2][L]
+ *
+ * Chunk enumeration.  Request r covers tokens [start[r], end[r]) with
+ * start[r] % C == 0.  Its chunk j covers [start + j*C, min(start+(j+1)*C, end));
+ * a chunk shorter than C exists only as the request's last chunk and only
+ * when save_unfull_chunk != 0.  Chunks are numbered request by request; that
+ * number g indexes chunk_ptrs / code_ptrs / scales.
+ *
+ * Ownership and synchronisation.  The caller owns every buffer.  The library
+ * allocates nothing, never synchronises, and returns right after enqueueing
+ * its kernels on `stream` (a cudaStream_t passed as void*; NULL = the legacy
+ * default stream).  Pointers marked DEVICE must be device memory of the
+ * current device; HOST arrays are read before the call returns.
+ *
+ * Errors.  Every call returns an lmkv_status value.  Argument errors are
+ * detected on the host before anything is launched (nothing is written).
+ * Errors found by the kernels (a block id outside [0, num_blocks), a null or
+ * misaligned device pointer inside the pointer arrays) skip the affected
+ * rows, move everything else, and store the code into *d_status (a DEVICE
+ * int32 the caller zeroes beforehand; may be NULL) -- readable after the
+ * stream has been synchronised.  Kernels never trap and never wait on a flag.
+ *
+ * Preconditions the library cannot check cheaply: block ids written by a
+ * scatter must be distinct across the batch (otherwise the result depends on
+ * write order); chunk buffers must not overlap the pool.
+ */
+#ifndef LMKV_H
+#define LMKV_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LMKV_ABI_VERSION 1
+
+typedef enum lmkv_status {
+    LMKV_OK = 0,
+    LMKV_ERR_INVALID_ARG = 1,   /* host: bad size, null pointer, unaligned start, short table */
+    LMKV_ERR_MISALIGNED = 2,    /* host: row bytes or a host-visible pointer not 16-byte aligned */
+    LMKV_ERR_CUDA = 3,          /* host: a CUDA launch or attribute call failed */
+    LMKV_ERR_UNSUPPORTED = 4,   /* host: e.g. the fp8 variant on a pool that is not bf16 */
+    LMKV_ERR_BAD_BLOCK = 5,     /* device: a block id outside [0, num_blocks); token skipped */
+    LMKV_ERR_BAD_POINTER = 6,   /* device: null or misaligned entry in a pointer array; skipped */
+    LMKV_ERR_TIMEOUT = 7        /* device: a bounded wait on an asynchronous copy gave up */
+} lmkv_status;
+
+/* The paged KV pool.  layer_base is a DEVICE array of num_layers DEVICE
+ * pointers, each to one layer's [2][num_blocks][B][HD] pool (16-byte
+ * aligned).  The struct itself is read on the host during the call. */
+typedef struct lmkv_pool {
+    void* const* layer_base;
+    int64_t num_blocks;
+    int32_t num_layers;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t block_size;
+    int32_t elem_bytes;     /* 2 for bf16 / fp16; 1 and 4 also accepted by the copies */
+} lmkv_pool_t;
+
+/* Number of chunks of a batch (host only, no CUDA).  Returns
+ * LMKV_ERR_INVALID_ARG for num_req < 0, chunk_size <= 0, start < 0,
+ * end < start, or start % chunk_size != 0. */
+int lmkv_count_chunks(const int64_t* start, const int64_t* end, int32_t num_req,
+                      int32_t chunk_size, int32_t save_unfull_chunk,
+                      int32_t* out_num_chunks);
+
+/* The chunk list itself (host only): for chunk g, its request, first token
+ * and token count n_g.  `capacity` is the length of the three HOST output
+ * arrays; LMKV_ERR_INVALID_ARG if it is smaller than the chunk count. */
+int lmkv_enumerate_chunks(const int64_t* start, const int64_t* end, int32_t num_req,
+                          int32_t chunk_size, int32_t save_unfull_chunk,
+                          int32_t* out_req, int64_t* out_tok0, int32_t* out_ntok,
+                          int32_t capacity);
+
+/* Store path: X_g[kv][l][t][:] = P_l[kv][BT[r][tok/B]][tok % B][:] for every
+ * chunk g (request r, tok = first token of g + t), kv, layer l, t < n_g.
+ * Configurable chunk size section of the LMCache paper (pages -> contiguous
+ * chunk buffer).
+ *   pool        : the paged pool (see lmkv_pool_t)
+ *   block_table : DEVICE int32 [num_req][max_blocks]
+ *   start, end  : HOST int64 [num_req]
+ *   chunk_ptrs  : DEVICE array [num_chunks] of DEVICE pointers, chunk g's
+ *                 buffer [2][L][n_g][HD], 16-byte aligned
+ *   d_status    : DEVICE int32 or NULL
+ * Host errors: INVALID_ARG (null pool/arrays, sizes <= 0, chunk_size not a
+ * multiple of block_size, unaligned start, end needing a column >= max_blocks),
+ * MISALIGNED (row bytes not a multiple of 16), CUDA. */
+int lmkv_gather_chunks(const lmkv_pool_t* pool, const int32_t* block_table, int32_t max_blocks,
+                       const int64_t* start, const int64_t* end, int32_t num_req,
+                       int32_t chunk_size, int32_t save_unfull_chunk,
+                       void* const* chunk_ptrs, int32_t* d_status, void* stream);
+
+/* Retrieve path: the inverse copy, P_l[kv][BT[r][tok/B]][tok % B][:] =
+ * X_g[kv][l][t][:], writing exactly the enumerated tokens (other slots of a
+ * partially covered block keep their contents).  Same arguments; chunk
+ * buffers are read.  Same section of the LMCache paper (chunks -> pages). */
+int lmkv_scatter_chunks(const lmkv_pool_t* pool, const int32_t* block_table, int32_t max_blocks,
+                        const int64_t* start, const int64_t* end, int32_t num_req,
+                        int32_t chunk_size, int32_t save_unfull_chunk,
+                        void* const* chunk_ptrs, int32_t* d_status, void* stream);
+
+/* Layer-wise store: lmkv_gather_chunks restricted to one layer `layer`
+ * (0 <= layer < L); only the X_g[kv][layer] slices of every chunk are
+ * written.  Calls for layer = 0..L-1 together equal one lmkv_gather_chunks.
+ * LMCache paper, layer-wise pipeline section (one layer's KV per transfer).
+ * INVALID_ARG if layer is out of range; otherwise as lmkv_gather_chunks. */
+int lmkv_gather_layer(const lmkv_pool_t* pool, const int32_t* block_table, int32_t max_blocks,
+                      const int64_t* start, const int64_t* end, int32_t num_req,
+                      int32_t chunk_size, int32_t save_unfull_chunk,
+                      void* const* chunk_ptrs, int32_t layer, int32_t* d_status, void* stream);
+
+/* Layer-wise retrieve: lmkv_scatter_chunks restricted to one layer. */
+int lmkv_scatter_layer(const lmkv_pool_t* pool, const int32_t* block_table, int32_t max_blocks,
+                       const int64_t* start, const int64_t* end, int32_t num_req,
+                       int32_t chunk_size, int32_t save_unfull_chunk,
+                       void* const* chunk_ptrs, int32_t layer, int32_t* d_status, void* stream);
+
+/* Quantising store (bf16 pool only, elem_bytes == 2).  For every tile
+ * (chunk g, kv, layer l):
+ *   amax  = max |x| over the tile's n_g x HD values
+ *   scale = amax / 448.0f                      (IEEE fp32 division)
+ *   code  = e4m3fn_round_nearest_even_saturating(x / scale)   (IEEE fp32 division)
+ *   amax == 0 gives scale 0 and all codes 0.
+ * scales[(g*2 + kv)*L + l] = scale.  The LMCache fp8 serde casts every element
+ * to float8_e4m3fn at one byte per element (LMCache serde guide, section 7.1);
+ * this variant adds the per-tile scale and fuses the cast into the gather.
+ *   code_ptrs : DEVICE array [num_chunks] of DEVICE pointers, chunk g's
+ *               codes [2][L][n_g][HD] uint8, 16-byte aligned
+ *   scales    : DEVICE float32 [num_chunks][2][L]
+ * Rows with a bad block id are skipped (not part of amax, codes not written).
+ * UNSUPPORTED if elem_bytes != 2 or HD is not a multiple of 16. */
+int lmkv_gather_chunks_fp8e4m3(const lmkv_pool_t* pool, const int32_t* block_table,
+                               int32_t max_blocks, const int64_t* start, const int64_t* end,
+                               int32_t num_req, int32_t chunk_size, int32_t save_unfull_chunk,
+                               void* const* code_ptrs, float* scales, int32_t* d_status,
+                               void* stream);
+
+/* Dequantising retrieve: P[...] = bf16_round_nearest_even(float(e4m3(code)) * scale),
+ * one fp32 multiply per element, into the enumerated tokens' rows. */
+int lmkv_scatter_chunks_fp8e4m3(const lmkv_pool_t* pool, const int32_t* block_table,
+                                int32_t max_blocks, const int64_t* start, const int64_t* end,
+                                int32_t num_req, int32_t chunk_size, int32_t save_unfull_chunk,
+                                void* const* code_ptrs, const float* scales, int32_t* d_status,
+                                void* stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* lmkv_status_string(int status);
+
+/* LMKV_ABI_VERSION of the loaded library. */
+int lmkv_abi_version(void);
+
+/* Number of kernel launches the library has enqueued since load (all entry
+ * points, all streams); a host-side counter for accounting, not a sync. */
+int64_t lmkv_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LMKV_H */

@@ -1,0 +1,527 @@
+// lmkv_kernels.cuh -- sm_103a kernels for the paged-KV chunk gather / scatter.
+//
+// The movement (LMCache paper notes, configurable chunk size section): a
+// kernel copies the scattered pages of many layers into a contiguous chunk
+// buffer on store and splits chunk buffers back into pages on load.  With
+// chunk_size a multiple of block_size, every (chunk, K/V, layer, block)
+// pair is one contiguous run of rows on BOTH sides: block_size rows of the
+// pool page and the matching rows of the chunk tile X_g[kv][l].  The unit of
+// work ("item") is such a run, optionally split into equal parts.
+//
+// Item numbering is chunk-major so that consecutive items touch consecutive
+// bytes of the chunk buffers:
+//   item = (((g * 2 + kv) * layer_n + ll) * blocks_per_chunk + j) * parts + q
+//
+// Two copy engines are provided for the same item stream:
+//  * move_lsu_kernel : CTA-wide 16-byte vector loads into registers, then
+//                      stores; one CTA per item (or grid-stride).
+//  * move_bulk_kernel: one thread per CTA drives the TMA bulk-copy engine
+//                      (cp.async.bulk global->shared->global) through a ring
+//                      of shared-memory stages with mbarrier completion.
+// The fp8 variant quantises one (chunk, K/V, layer) tile per thread-block
+// cluster, keeping the tile in registers and reducing the absmax across the
+// cluster through distributed shared memory, so HBM is read once.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_fp16.h>
+#include <cooperative_groups.h>
+
+namespace lmkv {
+
+constexpr int kMaxReqPerLaunch = 256;
+constexpr int kStatusBadBlock = 5;    // LMKV_ERR_BAD_BLOCK
+constexpr int kStatusBadPointer = 6;  // LMKV_ERR_BAD_POINTER
+constexpr int kStatusTimeout = 7;     // LMKV_ERR_TIMEOUT (bounded waits gave up)
+
+// By-value launch parameters (kept in the constant bank via __grid_constant__).
+struct Batch {
+    const uint8_t* const* layer_base;   // DEVICE [num_layers] pool layer bases
+    uint8_t* const* chunk_ptrs;         // DEVICE [total chunks] chunk (or code) buffers
+    const int32_t* block_table;         // DEVICE [num_req_total][bt_stride]
+    int32_t* status;                    // DEVICE int32 or null
+    float* scales;                      // DEVICE [total chunks][2][L] (fp8 only)
+    int64_t num_blocks;
+    int64_t bt_stride;
+    int32_t num_layers;
+    int32_t row_bytes;                  // pool row bytes (HD * elem_bytes)
+    int32_t block_size;
+    int32_t chunk_size;
+    int32_t blocks_per_chunk;           // chunk_size / block_size
+    int32_t parts;                      // items per (chunk, kv, layer, block); divides block_size
+    int32_t layer_lo;                   // first layer moved
+    int32_t layer_n;                    // number of layers moved
+    int32_t num_req;                    // requests packed in this launch (all with >= 1 chunk)
+    int32_t chunk_base;                 // global index of this launch's chunk 0
+    int32_t num_chunks;                 // chunks in this launch
+    int32_t pad_;
+    int32_t req_row[kMaxReqPerLaunch];              // block-table row of packed request i
+    int32_t req_chunk_begin[kMaxReqPerLaunch + 1];  // local chunk index of its first chunk
+    int64_t req_tok0[kMaxReqPerLaunch];             // its first enumerated token
+    int64_t req_tok_end[kMaxReqPerLaunch];          // end (exclusive) of its enumerated tokens
+};
+
+__host__ __device__ inline int64_t batch_items(const Batch& p) {
+    return (int64_t)p.num_chunks * 2 * p.layer_n * p.blocks_per_chunk * p.parts;
+}
+
+struct ChunkRef {
+    int32_t req_row;
+    int32_t ntok;
+    int64_t tok0;
+};
+
+// Chunk gl (local) -> its request: the last packed request whose first chunk <= gl.
+__device__ __forceinline__ ChunkRef resolve_chunk(const Batch& p, int32_t gl) {
+    int lo = 0, hi = p.num_req - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (p.req_chunk_begin[mid] <= gl) lo = mid; else hi = mid - 1;
+    }
+    ChunkRef c;
+    c.req_row = p.req_row[lo];
+    c.tok0 = p.req_tok0[lo] + (int64_t)(gl - p.req_chunk_begin[lo]) * p.chunk_size;
+    int64_t left = p.req_tok_end[lo] - c.tok0;
+    c.ntok = (int32_t)(left < p.chunk_size ? left : p.chunk_size);
+    return c;
+}
+
+__device__ __forceinline__ void report(const Batch& p, int code) {
+    if (p.status != nullptr) atomicCAS(p.status, 0, code);
+}
+
+// One item's two runs.  Returns false (after reporting, if it is an error)
+// when the item has nothing to move.
+struct Run {
+    uint8_t* pool;
+    uint8_t* chunk;
+    uint32_t bytes;
+};
+
+__device__ __forceinline__ bool item_run(const Batch& p, int64_t item, Run& run) {
+    const int q = (int)(item % p.parts);
+    int64_t t = item / p.parts;
+    const int j = (int)(t % p.blocks_per_chunk);
+    t /= p.blocks_per_chunk;
+    const int ll = (int)(t % p.layer_n);
+    t /= p.layer_n;
+    const int kv = (int)(t & 1);
+    const int gl = (int)(t >> 1);
+    const ChunkRef c = resolve_chunk(p, gl);
+    const int part_rows = p.block_size / p.parts;
+    const int row0 = j * p.block_size + q * part_rows;     // first row inside the chunk
+    if (row0 >= c.ntok) return false;                       // past a partial chunk's end
+    const int rows = min(part_rows, c.ntok - row0);
+    const int l = p.layer_lo + ll;
+    const int64_t col = c.tok0 / p.block_size + j;
+    const int64_t blk = p.block_table[(int64_t)c.req_row * p.bt_stride + col];
+    if (blk < 0 || blk >= p.num_blocks) { report(p, kStatusBadBlock); return false; }
+    uint8_t* lb = const_cast<uint8_t*>(p.layer_base[l]);
+    uint8_t* cb = p.chunk_ptrs[p.chunk_base + gl];
+    if (lb == nullptr || cb == nullptr || ((reinterpret_cast<uintptr_t>(lb) |
+                                            reinterpret_cast<uintptr_t>(cb)) & 15)) {
+        report(p, kStatusBadPointer);
+        return false;
+    }
+    const int64_t rb = p.row_bytes;
+    run.pool = lb + ((kv * p.num_blocks + blk) * p.block_size + q * part_rows) * rb;
+    run.chunk = cb + (((int64_t)kv * p.num_layers + l) * c.ntok + row0) * rb;
+    run.bytes = (uint32_t)(rows * rb);
+    return true;
+}
+
+// ---------------------------------------------------------------------------
+// 16-byte global accesses with streaming cache hints.
+__device__ __forceinline__ int4 ld_stream(const int4* ptr) {
+    int4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.s32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(ptr));
+    return r;
+}
+
+__device__ __forceinline__ void st_stream(int4* ptr, const int4& v) {
+    asm volatile("st.global.cs.v4.s32 [%0], {%1, %2, %3, %4};"
+                 :: "l"(ptr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+// CTA-wide copy of `bytes` (a multiple of 16) from src to dst.
+template <int kThreads, int kUnroll>
+__device__ __forceinline__ void cta_copy(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
+                                         uint32_t bytes) {
+    const int nvec = (int)(bytes >> 4);
+    const int4* s = reinterpret_cast<const int4*>(src);
+    int4* d = reinterpret_cast<int4*>(dst);
+    for (int base = threadIdx.x; base < nvec; base += kThreads * kUnroll) {
+        int4 r[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int v = base + u * kThreads;
+            if (v < nvec) r[u] = ld_stream(s + v);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int v = base + u * kThreads;
+            if (v < nvec) st_stream(d + v, r[u]);
+        }
+    }
+}
+
+// LSU engine.  kGather: pool -> chunk, else chunk -> pool.  Grid-stride over
+// items, so the grid may be the item count (one CTA per item) or smaller.
+template <bool kGather, int kThreads, int kUnroll>
+__global__ void __launch_bounds__(kThreads)
+move_lsu_kernel(const __grid_constant__ Batch p, int64_t num_items) {
+    for (int64_t item = blockIdx.x; item < num_items; item += gridDim.x) {
+        Run run;
+        if (!item_run(p, item, run)) continue;
+        if (kGather) cta_copy<kThreads, kUnroll>(run.pool, run.chunk, run.bytes);
+        else cta_copy<kThreads, kUnroll>(run.chunk, run.pool, run.bytes);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// TMA bulk-copy engine primitives (inline PTX).
+__device__ __forceinline__ uint32_t smem_addr(const void* ptr) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(done) : "r"(smem_addr(bar)), "r"(parity) : "memory");
+    return done != 0;
+}
+
+// Bounded wait on an mbarrier phase: false if it did not complete in time.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+    for (uint32_t i = 0; i < (1u << 20); ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+__device__ __forceinline__ void bulk_g2s(void* sdst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(smem_addr(sdst)), "l"(gsrc), "r"(bytes), "r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void bulk_s2g(void* gdst, const void* ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 :: "l"(gdst), "r"(smem_addr(ssrc)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_read_1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// A piece is at most one stage of an item's run.
+struct Piece {
+    const uint8_t* src;
+    uint8_t* dst;
+    uint32_t bytes;
+};
+
+// Sequential cursor over the pieces of the items this CTA owns.
+template <bool kGather, int kStageBytes>
+struct PieceCursor {
+    int64_t item;
+    int64_t num_items;
+    int64_t stride;
+    Run run;
+    uint32_t off;
+    bool have_run;
+
+    __device__ __forceinline__ void init(const Batch& p, int64_t first, int64_t n, int64_t s) {
+        item = first;
+        num_items = n;
+        stride = s;
+        have_run = false;
+        off = 0;
+        advance_item(p);
+    }
+    __device__ __forceinline__ void advance_item(const Batch& p) {
+        have_run = false;
+        while (item < num_items) {
+            const bool ok = item_run(p, item, run);
+            item += stride;
+            if (ok && run.bytes > 0) { have_run = true; off = 0; return; }
+        }
+    }
+    __device__ __forceinline__ bool next(const Batch& p, Piece& pc) {
+        if (!have_run) return false;
+        const uint32_t left = run.bytes - off;
+        const uint32_t n = left < (uint32_t)kStageBytes ? left : (uint32_t)kStageBytes;
+        if (kGather) { pc.src = run.pool + off; pc.dst = run.chunk + off; }
+        else { pc.src = run.chunk + off; pc.dst = run.pool + off; }
+        pc.bytes = n;
+        off += n;
+        if (off >= run.bytes) advance_item(p);
+        return true;
+    }
+};
+
+// TMA engine: lane 0 of a single warp streams pieces through kStages shared
+// stages.  Loads run kStages-1 ahead of stores; a stage is refilled once the
+// bulk store that read it has finished reading (wait_group.read with one
+// group of slack).
+template <bool kGather, int kStages, int kStageBytes>
+__global__ void __launch_bounds__(32)
+move_bulk_kernel(const __grid_constant__ Batch p, int64_t num_items) {
+    extern __shared__ __align__(128) uint8_t stage_mem[];
+    __shared__ __align__(8) uint64_t bar[kStages];
+    if (threadIdx.x != 0) return;
+    for (int s = 0; s < kStages; ++s) mbar_init(&bar[s], 1);
+    fence_barrier_init();
+
+    PieceCursor<kGather, kStageBytes> cur;
+    cur.init(p, blockIdx.x, num_items, gridDim.x);
+    Piece ring[kStages];
+    uint32_t k_load = 0, k_store = 0;
+    Piece pc;
+    while (k_load < (uint32_t)kStages && cur.next(p, pc)) {
+        const int s = (int)(k_load % kStages);
+        ring[s] = pc;
+        mbar_arrive_expect_tx(&bar[s], pc.bytes);
+        bulk_g2s(stage_mem + (size_t)s * kStageBytes, pc.src, pc.bytes, &bar[s]);
+        ++k_load;
+    }
+    bool timed_out = false;
+    while (k_store < k_load) {
+        const int s = (int)(k_store % kStages);
+        if (!mbar_wait_bounded(&bar[s], (k_store / kStages) & 1)) { timed_out = true; break; }
+        bulk_s2g(ring[s].dst, stage_mem + (size_t)s * kStageBytes, ring[s].bytes);
+        bulk_commit();
+        ++k_store;
+        if (k_store >= 2 && cur.next(p, pc)) {
+            // stage of piece k_store-2 is free once its store has read shared memory
+            bulk_wait_read_1();
+            const int sf = (int)(k_load % kStages);
+            ring[sf] = pc;
+            mbar_arrive_expect_tx(&bar[sf], pc.bytes);
+            bulk_g2s(stage_mem + (size_t)sf * kStageBytes, pc.src, pc.bytes, &bar[sf]);
+            ++k_load;
+        }
+    }
+    if (timed_out) {
+        report(p, kStatusTimeout);
+        // let the loads already in flight land before shared memory is released
+        for (uint32_t k = k_store; k < k_load; ++k)
+            (void)mbar_wait_bounded(&bar[k % kStages], (k / kStages) & 1);
+    }
+    bulk_wait_all();
+}
+
+// ---------------------------------------------------------------------------
+// fp8 e4m3 quantising gather.  One thread-block cluster of kCluster CTAs per
+// tile (chunk g, kv, layer l); CTA `rank` owns rows [rank*R, rank*R + R) of the
+// tile (R = ceil(n_g / kCluster)).  Values stay in registers between the
+// absmax pass and the quantising pass when the slice fits in
+// kThreads * kVPT vectors of 16 bytes; otherwise the rest is re-read.
+constexpr int kQuantMaxRows = 256;   // rows per CTA slice (chunk_size <= kCluster * 256)
+
+__device__ __forceinline__ uint32_t absmax_bf16x8(const uint4& v) {
+    const uint32_t m = 0x7FFF7FFFu;
+    uint32_t a = __vmaxu2(v.x & m, v.y & m);
+    uint32_t b = __vmaxu2(v.z & m, v.w & m);
+    a = __vmaxu2(a, b);
+    return max(a & 0xFFFFu, a >> 16);
+}
+
+__device__ __forceinline__ uint2 quant_bf16x8(const uint4& v, float scale) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t out[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t packed = 0;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const uint32_t word = w[h * 2 + k];
+            float2 f;
+            f.x = __fdiv_rn(__uint_as_float(word << 16), scale);
+            f.y = __fdiv_rn(__uint_as_float(word & 0xFFFF0000u), scale);
+            const __nv_fp8x2_storage_t q = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
+            packed |= (uint32_t)q << (16 * k);
+        }
+        out[h] = packed;
+    }
+    return make_uint2(out[0], out[1]);
+}
+
+template <int kThreads, int kVPT, int kCluster>
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
+quant_gather_kernel(const __grid_constant__ Batch p) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    __shared__ const uint8_t* row_src[kQuantMaxRows];
+    __shared__ uint32_t warp_max[kThreads / 32];
+    __shared__ uint32_t cta_max;
+    __shared__ uint32_t tile_max;
+
+    const int rank = (int)cluster.block_rank();
+    const int64_t tile = blockIdx.x / kCluster;
+    const int ll = (int)(tile % p.layer_n);
+    const int kv = (int)((tile / p.layer_n) & 1);
+    const int gl = (int)(tile / p.layer_n / 2);
+    const int l = p.layer_lo + ll;
+    const ChunkRef c = resolve_chunk(p, gl);
+    const int rows_per = (c.ntok + kCluster - 1) / kCluster;
+    const int r0 = rank * rows_per;
+    const int nrows = max(0, min(c.ntok, r0 + rows_per) - r0);
+    const int vpr = p.row_bytes >> 4;             // 16-byte vectors per row
+    const int row_elems = p.row_bytes >> 1;
+    const int nvec = nrows * vpr;
+
+    uint8_t* codes = p.chunk_ptrs[p.chunk_base + gl];
+    const uint8_t* lb = p.layer_base[l];
+    const bool ptr_ok = codes != nullptr && lb != nullptr &&
+                        ((reinterpret_cast<uintptr_t>(codes) | reinterpret_cast<uintptr_t>(lb)) & 15) == 0;
+    if (!ptr_ok && threadIdx.x == 0 && rank == 0) report(p, kStatusBadPointer);
+    for (int i = threadIdx.x; i < nrows; i += kThreads) {
+        const int row = r0 + i;
+        const int64_t tok = c.tok0 + row;
+        const int64_t blk = p.block_table[(int64_t)c.req_row * p.bt_stride + tok / p.block_size];
+        const uint8_t* src = nullptr;
+        if (blk < 0 || blk >= p.num_blocks) report(p, kStatusBadBlock);
+        else if (ptr_ok)
+            src = lb + ((kv * p.num_blocks + blk) * p.block_size + tok % p.block_size) * (int64_t)p.row_bytes;
+        row_src[i] = src;
+    }
+    __syncthreads();
+
+    uint4 regs[kVPT];
+    uint32_t m = 0;
+#pragma unroll
+    for (int u = 0; u < kVPT; ++u) {
+        const int v = threadIdx.x + u * kThreads;
+        regs[u] = make_uint4(0, 0, 0, 0);
+        if (v < nvec) {
+            const uint8_t* src = row_src[v / vpr];
+            if (src != nullptr) {
+                const int4 x = ld_stream(reinterpret_cast<const int4*>(src) + (v % vpr));
+                regs[u] = make_uint4((uint32_t)x.x, (uint32_t)x.y, (uint32_t)x.z, (uint32_t)x.w);
+                m = max(m, absmax_bf16x8(regs[u]));
+            }
+        }
+    }
+    for (int v = threadIdx.x + kVPT * kThreads; v < nvec; v += kThreads) {
+        const uint8_t* src = row_src[v / vpr];
+        if (src == nullptr) continue;
+        const int4 x = ld_stream(reinterpret_cast<const int4*>(src) + (v % vpr));
+        m = max(m, absmax_bf16x8(make_uint4((uint32_t)x.x, (uint32_t)x.y, (uint32_t)x.z, (uint32_t)x.w)));
+    }
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        uint32_t w = threadIdx.x < kThreads / 32 ? warp_max[threadIdx.x] : 0u;
+        w = __reduce_max_sync(0xFFFFFFFFu, w);
+        if (threadIdx.x == 0) cta_max = w;
+    }
+    cluster.sync();                               // every CTA's cta_max is visible
+    if (threadIdx.x < 32) {
+        uint32_t w = 0;
+        if (threadIdx.x < kCluster) w = *cluster.map_shared_rank(&cta_max, (unsigned)threadIdx.x);
+        w = __reduce_max_sync(0xFFFFFFFFu, w);
+        if (threadIdx.x == 0) tile_max = w;
+    }
+    cluster.sync();                               // remote reads done before any CTA may exit
+    const float amax = __uint_as_float(tile_max << 16);
+    const float scale = __fdiv_rn(amax, 448.0f);
+    if (rank == 0 && threadIdx.x == 0 && p.scales != nullptr)
+        p.scales[((int64_t)(p.chunk_base + gl) * 2 + kv) * p.num_layers + l] = scale;
+    if (!ptr_ok) return;
+
+    uint8_t* tile_codes = codes + (((int64_t)kv * p.num_layers + l) * c.ntok + r0) * row_elems;
+#pragma unroll
+    for (int u = 0; u < kVPT; ++u) {
+        const int v = threadIdx.x + u * kThreads;
+        if (v < nvec && row_src[v / vpr] != nullptr) {
+            const uint2 q = scale == 0.0f ? make_uint2(0, 0) : quant_bf16x8(regs[u], scale);
+            *reinterpret_cast<uint2*>(tile_codes + (int64_t)v * 8) = q;
+        }
+    }
+    for (int v = threadIdx.x + kVPT * kThreads; v < nvec; v += kThreads) {
+        const uint8_t* src = row_src[v / vpr];
+        if (src == nullptr) continue;
+        const int4 x = ld_stream(reinterpret_cast<const int4*>(src) + (v % vpr));
+        const uint4 xv = make_uint4((uint32_t)x.x, (uint32_t)x.y, (uint32_t)x.z, (uint32_t)x.w);
+        const uint2 q = scale == 0.0f ? make_uint2(0, 0) : quant_bf16x8(xv, scale);
+        *reinterpret_cast<uint2*>(tile_codes + (int64_t)v * 8) = q;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// fp8 e4m3 dequantising scatter: per item (chunk, kv, layer, block part),
+// 16 codes (16 bytes) in, 16 bf16 (32 bytes) out per thread step.
+__device__ __forceinline__ uint32_t dequant_pair(uint16_t two_codes, float scale) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two_codes, __NV_E4M3);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+    const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * scale, f.y * scale);
+    return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+template <int kThreads>
+__global__ void __launch_bounds__(kThreads)
+dequant_scatter_kernel(const __grid_constant__ Batch p, int64_t num_items) {
+    for (int64_t item = blockIdx.x; item < num_items; item += gridDim.x) {
+        // Decode the item against a bf16 pool, then derive the code run from it.
+        Run run;
+        if (!item_run(p, item, run)) continue;
+        int64_t t = item / p.parts / p.blocks_per_chunk;
+        const int ll = (int)(t % p.layer_n);
+        t /= p.layer_n;
+        const int kv = (int)(t & 1);
+        const int gl = (int)(t >> 1);
+        const int l = p.layer_lo + ll;
+        const float scale = p.scales[((int64_t)(p.chunk_base + gl) * 2 + kv) * p.num_layers + l];
+        // chunk-side offset of the run in bf16 bytes -> the same rows in code bytes
+        const uint8_t* cb = p.chunk_ptrs[p.chunk_base + gl];
+        const int64_t code_off = (run.chunk - cb) >> 1;
+        const uint4* src = reinterpret_cast<const uint4*>(cb + code_off);
+        uint4* dst = reinterpret_cast<uint4*>(run.pool);
+        const int n16 = (int)(run.bytes >> 5);     // 16 codes per step
+        for (int v = threadIdx.x; v < n16; v += kThreads) {
+            const int4 ci = ld_stream(reinterpret_cast<const int4*>(src) + v);
+            const uint32_t cw[4] = {(uint32_t)ci.x, (uint32_t)ci.y, (uint32_t)ci.z, (uint32_t)ci.w};
+            uint32_t o[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                o[2 * k] = dequant_pair((uint16_t)(cw[k] & 0xFFFFu), scale);
+                o[2 * k + 1] = dequant_pair((uint16_t)(cw[k] >> 16), scale);
+            }
+            st_stream(reinterpret_cast<int4*>(dst + 2 * v),
+                      make_int4((int)o[0], (int)o[1], (int)o[2], (int)o[3]));
+            st_stream(reinterpret_cast<int4*>(dst + 2 * v + 1),
+                      make_int4((int)o[4], (int)o[5], (int)o[6], (int)o[7]));
+        }
+    }
+}
+
+}  // namespace lmkv

@@ -1,0 +1,237 @@
+"""Python binding of liblmkv.so (argument marshalling only).
+
+Every function here maps one-to-one onto an ``extern "C"`` entry point of
+``include/lmkv.h``; all data movement runs in the library's CUDA kernels.
+PyTorch tensors are used only as carriers of device memory and streams.  If
+the library has not been built, the first call raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Sequence
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "liblmkv.so")
+
+OK = 0
+ERR_INVALID_ARG = 1
+ERR_MISALIGNED = 2
+ERR_CUDA = 3
+ERR_UNSUPPORTED = 4
+ERR_BAD_BLOCK = 5
+ERR_BAD_POINTER = 6
+ERR_TIMEOUT = 7
+
+ENTRY_POINTS = (
+    "lmkv_count_chunks", "lmkv_enumerate_chunks", "lmkv_gather_chunks", "lmkv_scatter_chunks",
+    "lmkv_gather_layer", "lmkv_scatter_layer", "lmkv_gather_chunks_fp8e4m3",
+    "lmkv_scatter_chunks_fp8e4m3", "lmkv_status_string", "lmkv_abi_version",
+    "lmkv_launch_count",
+)
+
+
+class LmkvError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        super().__init__(f"{what}: lmkv status {code} ({status_string(code)})")
+
+
+class _PoolT(ctypes.Structure):
+    _fields_ = [
+        ("layer_base", ctypes.c_void_p),
+        ("num_blocks", ctypes.c_int64),
+        ("num_layers", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("block_size", ctypes.c_int32),
+        ("elem_bytes", ctypes.c_int32),
+    ]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load() -> ctypes.CDLL:
+    """Load liblmkv.so (raises if it is missing: build it with build.build())."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: the CUDA library must be built "
+                               "(paged_kv_cache_lmkv_gb300.build.build()); there is no fallback")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        pool_p = ctypes.POINTER(_PoolT)
+        lib.lmkv_count_chunks.argtypes = [P, P, i32, i32, i32, P]
+        lib.lmkv_enumerate_chunks.argtypes = [P, P, i32, i32, i32, P, P, P, i32]
+        move = [pool_p, P, i32, P, P, i32, i32, i32, P, P, P]
+        lib.lmkv_gather_chunks.argtypes = move
+        lib.lmkv_scatter_chunks.argtypes = move
+        layer = [pool_p, P, i32, P, P, i32, i32, i32, P, i32, P, P]
+        lib.lmkv_gather_layer.argtypes = layer
+        lib.lmkv_scatter_layer.argtypes = layer
+        fp8 = [pool_p, P, i32, P, P, i32, i32, i32, P, P, P, P]
+        lib.lmkv_gather_chunks_fp8e4m3.argtypes = fp8
+        lib.lmkv_scatter_chunks_fp8e4m3.argtypes = fp8
+        for name in ("lmkv_count_chunks", "lmkv_enumerate_chunks", "lmkv_gather_chunks",
+                     "lmkv_scatter_chunks", "lmkv_gather_layer", "lmkv_scatter_layer",
+                     "lmkv_gather_chunks_fp8e4m3", "lmkv_scatter_chunks_fp8e4m3",
+                     "lmkv_abi_version"):
+            getattr(lib, name).restype = ctypes.c_int
+        lib.lmkv_status_string.argtypes = [ctypes.c_int]
+        lib.lmkv_status_string.restype = ctypes.c_char_p
+        lib.lmkv_launch_count.argtypes = []
+        lib.lmkv_launch_count.restype = ctypes.c_int64
+        _lib = lib
+        return lib
+
+
+def status_string(code: int) -> str:
+    return load().lmkv_status_string(int(code)).decode()
+
+
+def launch_count() -> int:
+    return int(load().lmkv_launch_count())
+
+
+def _i64_array(values):
+    arr = (ctypes.c_int64 * max(len(values), 1))()
+    for i, v in enumerate(values):
+        arr[i] = int(v)
+    return arr
+
+
+def _stream_handle(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+class Pool:
+    """A paged KV pool: per-layer device tensors [2][num_blocks][block_size][heads*head_dim].
+
+    Holds the DEVICE array of layer base pointers the ABI takes.
+    """
+
+    def __init__(self, layers: Sequence[torch.Tensor], num_kv_heads: int, head_dim: int):
+        t0 = layers[0]
+        if t0.dim() != 4 or t0.shape[0] != 2 or t0.shape[3] != num_kv_heads * head_dim:
+            raise ValueError("pool layers must be [2][num_blocks][block_size][heads*head_dim]")
+        for t in layers:
+            if t.shape != t0.shape or t.dtype != t0.dtype or not t.is_contiguous() or not t.is_cuda:
+                raise ValueError("pool layers must be contiguous CUDA tensors of one shape/dtype")
+        self.layers = list(layers)
+        self.num_kv_heads = num_kv_heads
+        self.head_dim = head_dim
+        self.block_size = t0.shape[2]
+        self.num_blocks = t0.shape[1]
+        self.elem_bytes = t0.element_size()
+        self.ptrs = torch.tensor([t.data_ptr() for t in layers], dtype=torch.int64,
+                                 device=t0.device)
+        self._struct = _PoolT(self.ptrs.data_ptr(), self.num_blocks, len(layers), num_kv_heads,
+                              head_dim, self.block_size, self.elem_bytes)
+
+    @property
+    def num_layers(self) -> int:
+        return len(self.layers)
+
+    @property
+    def struct(self):
+        return ctypes.byref(self._struct)
+
+
+def pointer_array(tensors: Sequence[torch.Tensor], device) -> torch.Tensor:
+    """DEVICE int64 array of the tensors' data pointers (chunk_ptrs / code_ptrs)."""
+    return torch.tensor([t.data_ptr() for t in tensors], dtype=torch.int64, device=device)
+
+
+def count_chunks(start, end, chunk_size: int, save_unfull: bool) -> int:
+    lib = load()
+    s, e = _i64_array(start), _i64_array(end)
+    out = ctypes.c_int32(0)
+    rc = lib.lmkv_count_chunks(s, e, len(start), chunk_size, int(save_unfull), ctypes.byref(out))
+    if rc != OK:
+        raise LmkvError(rc, "lmkv_count_chunks")
+    return out.value
+
+
+def enumerate_chunks(start, end, chunk_size: int, save_unfull: bool):
+    """[(request, first token, n tokens)] in chunk order."""
+    lib = load()
+    n = count_chunks(start, end, chunk_size, save_unfull)
+    s, e = _i64_array(start), _i64_array(end)
+    req = (ctypes.c_int32 * max(n, 1))()
+    tok0 = (ctypes.c_int64 * max(n, 1))()
+    ntok = (ctypes.c_int32 * max(n, 1))()
+    rc = lib.lmkv_enumerate_chunks(s, e, len(start), chunk_size, int(save_unfull), req, tok0,
+                                   ntok, n)
+    if rc != OK:
+        raise LmkvError(rc, "lmkv_enumerate_chunks")
+    return [(req[i], tok0[i], ntok[i]) for i in range(n)]
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _common(pool: Pool, block_table: torch.Tensor, start, end):
+    if block_table.dtype != torch.int32:
+        raise ValueError("block_table must be int32")
+    return (pool.struct, _ptr(block_table), block_table.shape[-1], _i64_array(start),
+            _i64_array(end), len(start))
+
+
+def gather_chunks(pool, block_table, start, end, chunk_size, save_unfull, chunk_ptrs,
+                  status=None, stream=None) -> int:
+    """lmkv_gather_chunks; returns the status code (0 = launched)."""
+    a = _common(pool, block_table, start, end)
+    return load().lmkv_gather_chunks(*a, chunk_size, int(save_unfull), _ptr(chunk_ptrs),
+                                     _ptr(status), _stream_handle(stream))
+
+
+def scatter_chunks(pool, block_table, start, end, chunk_size, save_unfull, chunk_ptrs,
+                   status=None, stream=None) -> int:
+    a = _common(pool, block_table, start, end)
+    return load().lmkv_scatter_chunks(*a, chunk_size, int(save_unfull), _ptr(chunk_ptrs),
+                                      _ptr(status), _stream_handle(stream))
+
+
+def gather_layer(pool, block_table, start, end, chunk_size, save_unfull, chunk_ptrs, layer,
+                 status=None, stream=None) -> int:
+    a = _common(pool, block_table, start, end)
+    return load().lmkv_gather_layer(*a, chunk_size, int(save_unfull), _ptr(chunk_ptrs),
+                                    int(layer), _ptr(status), _stream_handle(stream))
+
+
+def scatter_layer(pool, block_table, start, end, chunk_size, save_unfull, chunk_ptrs, layer,
+                  status=None, stream=None) -> int:
+    a = _common(pool, block_table, start, end)
+    return load().lmkv_scatter_layer(*a, chunk_size, int(save_unfull), _ptr(chunk_ptrs),
+                                     int(layer), _ptr(status), _stream_handle(stream))
+
+
+def gather_chunks_fp8e4m3(pool, block_table, start, end, chunk_size, save_unfull, code_ptrs,
+                          scales, status=None, stream=None) -> int:
+    a = _common(pool, block_table, start, end)
+    return load().lmkv_gather_chunks_fp8e4m3(*a, chunk_size, int(save_unfull), _ptr(code_ptrs),
+                                             _ptr(scales), _ptr(status), _stream_handle(stream))
+
+
+def scatter_chunks_fp8e4m3(pool, block_table, start, end, chunk_size, save_unfull, code_ptrs,
+                           scales, status=None, stream=None) -> int:
+    a = _common(pool, block_table, start, end)
+    return load().lmkv_scatter_chunks_fp8e4m3(*a, chunk_size, int(save_unfull), _ptr(code_ptrs),
+                                              _ptr(scales), _ptr(status), _stream_handle(stream))
+
+
+def check(rc: int, what: str = "lmkv") -> None:
+    if rc != OK:
+        raise LmkvError(rc, what)

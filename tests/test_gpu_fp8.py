@@ -1,0 +1,171 @@
+"""GPU parity of the fp8-e4m3 quantising gather and dequantising scatter.
+
+Codes and scales must equal the oracle's bit for bit: the quantised code is
+an integer decided by fp32 arithmetic, and both sides take that decision in
+fp32 (absmax/448 by IEEE division, x/scale by IEEE division, round to nearest
+even with saturation).  The LMCache fp8 serde casts to float8_e4m3fn at one
+byte per element (serde guide, section 7.1); the per-(K/V, layer, chunk)
+scale is the fused variant's definition.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_lmkv_gb300 as pkg
+from paged_kv_cache_lmkv_gb300 import workloads as wl
+from gpu_util import (DEV, alloc_chunks, compact_subbatch, device_pool, host_bytes, host_u16,
+                      new_status, require_gpu)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _gpu():
+    require_gpu()
+    yield
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def gpu_quant(pool, w, table, flag):
+    chunks = pkg.enumerate_chunks(w.starts, w.ends, w.chunk_size, flag)
+    codes, cptrs = alloc_chunks(chunks, w, dtype=torch.uint8, fill=0xEE)
+    scales = torch.full((len(chunks), 2, w.num_layers), -1.0, dtype=torch.float32, device=DEV)
+    st = new_status()
+    bt = torch.from_numpy(table).to(DEV)
+    pkg.check(pkg.gather_chunks_fp8e4m3(pool, bt, w.starts, w.ends, w.chunk_size, flag, cptrs,
+                                        scales, st))
+    torch.cuda.synchronize()
+    return chunks, codes, cptrs, scales, st
+
+
+SMALL = [
+    # L, H, D, B, nb, ends, starts, C, flag
+    (3, 2, 64, 16, 64, (512,), (0,), 256, True),
+    (2, 2, 64, 16, 96, (300, 1000, 17), (0, 256, 0), 256, True),
+    (2, 2, 64, 16, 96, (300, 1000, 17), (0, 256, 0), 256, False),
+    (2, 1, 16, 4, 300, (333, 64), (64, 0), 64, True),
+    (2, 8, 128, 32, 64, (900,), (0,), 256, True),
+    (2, 8, 128, 64, 32, (1100,), (256,), 256, True),
+    (1, 1, 32, 8, 600, (2000,), (0,), 1024, True),     # chunk larger than the cluster's registers
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=[str(i) for i in range(len(SMALL))])
+def test_small_quant_dequant_vs_oracle(shape):
+    L, H, D, B, nb, ends, starts, C, flag = shape
+    w = wl.Workload("f", L, H, D, B, nb, ends, req_start=starts, chunk_size=C, outliers=True,
+                    save_unfull=flag)
+    table, table2 = wl.block_table(w, 1), wl.block_table(w, 2)
+    pool = device_pool(w, 0)
+    chunks, codes, cptrs, scales, st = gpu_quant(pool, w, table, flag)
+    assert st.item() == 0
+    host = [host_u16(t) for t in pool.layers]
+    rc = [np.full((2, L, n, w.row_elems), 0xEE, np.uint8) for _, _, n in chunks]
+    rs = np.full((len(chunks), 2, L), -1.0, np.float32)
+    assert oracle.gather_fp8(oracle.HostPool(host, B), table, w.starts, w.ends, C, flag, rc, rs) == 0
+    np.testing.assert_array_equal(scales.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+    for g, (a, b) in enumerate(zip(codes, rc)):
+        np.testing.assert_array_equal(a.cpu().numpy(), b, err_msg=f"codes chunk {g}")
+    # dequantising scatter into a sentinel pool
+    pool2 = device_pool(w, None, fill="sentinel")
+    st.zero_()
+    pkg.check(pkg.scatter_chunks_fp8e4m3(pool2, torch.from_numpy(table2).to(DEV), w.starts,
+                                         w.ends, C, flag, cptrs, scales, st))
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    h2 = [np.full_like(a, wl.SENTINEL_BF16) for a in host]
+    assert oracle.scatter_fp8(oracle.HostPool(h2, B), table2, w.starts, w.ends, C, flag, rc, rs) == 0
+    for l, (t, h) in enumerate(zip(pool2.layers, h2)):
+        np.testing.assert_array_equal(host_u16(t), h, err_msg=f"dequant layer {l}")
+
+
+def test_exhaustive_bf16_against_many_scales():
+    """Tile i holds every finite bf16 value whose magnitude is at most A_i
+    (repeated to fill 256 x 1024 elements), so its scale is A_i / 448; 48
+    tiles with A_i spread over the bf16 range cover all bf16 inputs under 48
+    different scales."""
+    all_bits = np.arange(1 << 16, dtype=np.uint32)
+    vals = (all_bits << 16).view(np.float32)
+    finite = np.isfinite(vals)
+    rng = np.random.default_rng(0)
+    amaxes = np.concatenate([[448.0, 1.0, 2.0 ** -120, 3.0e38, 1.5e-5],
+                             np.exp2(rng.uniform(-100, 100, 43))]).astype(np.float32)
+    amax_bf16 = (amaxes.view(np.uint32) >> 16).astype(np.uint32)   # truncate to bf16
+    L = len(amax_bf16)
+    w = wl.Workload("x", L, 8, 128, 16, 16, (256,), chunk_size=256)
+    layers = []
+    for l, ab in enumerate(amax_bf16):
+        a = (ab << 16).view(np.float32) if np.ndim(ab) else np.uint32(ab << 16).view(np.float32)
+        pick = all_bits[finite & (np.abs(vals) <= a)].astype(np.uint16)
+        tile = np.resize(rng.permutation(pick), 256 * 1024).reshape(16, 16, 1024)
+        tile[0, 0, 0] = np.uint16(ab)                       # make sure +A_i is present
+        lay = np.empty((2, 16, 16, 1024), np.uint16)
+        lay[0] = tile
+        lay[1] = tile[:, :, ::-1]
+        layers.append(torch.from_numpy(lay.view(np.int16)).view(torch.bfloat16).to(DEV))
+    pool = pkg.Pool(layers, 8, 128)
+    table = np.arange(16, dtype=np.int32)[None, :]
+    chunks, codes, cptrs, scales, st = gpu_quant(pool, w, table, True)
+    assert st.item() == 0
+    host = [host_u16(t) for t in layers]
+    rc = [np.zeros((2, L, 256, 1024), np.uint8)]
+    rs = np.zeros((1, 2, L), np.float32)
+    assert oracle.gather_fp8(oracle.HostPool(host, 16), table, [0], [256], 256, True, rc, rs) == 0
+    np.testing.assert_array_equal(scales.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+    np.testing.assert_array_equal(codes[0].cpu().numpy(), rc[0])
+
+
+@pytest.mark.parametrize("block_size", [16, 32, 64])
+def test_qwen32b_full_size_sampled(block_size):
+    """Qwen2.5-32B shape, 16384 tokens, outlier channels; GPU run at full size,
+    oracle on two sampled chunks (all layers, K and V)."""
+    w = wl.qwen_with_block_size(block_size)
+    table = wl.block_table(w, 1)
+    table2 = wl.block_table(w, 2)
+    pool = device_pool(w, 0)
+    chunks, codes, cptrs, scales, st = gpu_quant(pool, w, table, True)
+    assert st.item() == 0 and len(chunks) == 64
+    sample = [0, 45]
+    hp, tab, s, e, _ = compact_subbatch(pool.layers, table, chunks, sample)
+    hp16 = oracle.HostPool([a.view(np.uint16) for a in hp.layers], block_size)
+    rc = [np.zeros((2, 64, 256, 1024), np.uint8) for _ in sample]
+    rs = np.zeros((len(sample), 2, 64), np.float32)
+    assert oracle.gather_fp8(hp16, tab, s, e, 256, True, rc, rs) == 0
+    for i, g in enumerate(sample):
+        np.testing.assert_array_equal(scales[g].cpu().numpy().view(np.uint32), rs[i].view(np.uint32))
+        np.testing.assert_array_equal(codes[g].cpu().numpy(), rc[i], err_msg=f"chunk {g}")
+    pool2 = device_pool(w, None, fill="sentinel")
+    pkg.check(pkg.scatter_chunks_fp8e4m3(pool2, torch.from_numpy(table2).to(DEV), w.starts,
+                                         w.ends, 256, True, cptrs, scales, st))
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    hq, tab2, s2, e2, _ = compact_subbatch(pool2.layers, table2, chunks, sample)
+    h2 = [np.full(a.shape[:3] + (a.shape[3] // 2,), wl.SENTINEL_BF16, np.uint16) for a in hq.layers]
+    assert oracle.scatter_fp8(oracle.HostPool(h2, block_size), tab2, s2, e2, 256, True, rc, rs) == 0
+    for a, b in zip(hq.layers, h2):
+        np.testing.assert_array_equal(a.view(np.uint16), b)
+
+
+def test_quant_error_bound_full_8b_shape():
+    """Closed-form bound on the round trip at the Llama-3.1-8B shape (a property
+    that holds at any size): |deq - x| <= half an e4m3 step at the tile's scale
+    plus one bf16 rounding."""
+    w = wl.LLAMA8B.with_(outliers=True)
+    pool = device_pool(w, 0)
+    table = wl.block_table(w, 1)
+    chunks, codes, cptrs, scales, st = gpu_quant(pool, w, table, True)
+    pool2 = device_pool(w, None, fill="sentinel")
+    pkg.check(pkg.scatter_chunks_fp8e4m3(pool2, torch.from_numpy(table).to(DEV), w.starts,
+                                         w.ends, 256, True, cptrs, scales, st))
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    ids = torch.as_tensor(table[0], dtype=torch.long, device=DEV)
+    for l in range(0, w.num_layers, 7):
+        x = pool.layers[l].index_select(1, ids).float().view(2, 40, 256, -1)
+        y = pool2.layers[l].index_select(1, ids).float().view(2, 40, 256, -1)
+        s = scales[:, :, l].t().reshape(2, 40, 1, 1)
+        bound = torch.maximum(x.abs() * 2.0 ** -4, s * 2.0 ** -10) * (1 + 2.0 ** -8) + \
+            x.abs() * 2.0 ** -8
+        assert bool(((y - x).abs() <= bound).all())
