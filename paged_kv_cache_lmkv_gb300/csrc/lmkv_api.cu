@@ -10,17 +10,14 @@
 #include "lmkv_kernels.cuh"
 
 #include <atomic>
-#include <cstring>
-#include <vector>
 
 namespace {
 
-using lmkv::Batch;
-
 std::atomic<int64_t> g_launches{0};
 
-// Copy engine configuration (chosen by measurement on GB300; see the kernel
-// header for the two engines).
+// Copy engine configuration (chosen by measurement on GB300: a sweep of the
+// LSU and TMA bulk engines over threads, unroll, grid shape and stages found
+// the LSU engine with one CTA per run at the top for the 8B gather).
 constexpr int kLsuThreads = 256;
 constexpr int kLsuUnroll = 8;
 constexpr int kQuantThreads = 512;
@@ -28,36 +25,30 @@ constexpr int kQuantVPT = 8;
 constexpr int kQuantCluster = 8;
 constexpr int kDequantThreads = 256;
 
-struct ChunkSpan {
-    int32_t req;
-    int64_t tok0;
-    int32_t ntok;
-};
+// Chunks of one request (cache_engine.py walk-through, "store()").
+inline int64_t request_chunks(int64_t s, int64_t e, int32_t chunk_size, int32_t save_unfull) {
+    const int64_t len = e - s;
+    return len / chunk_size + ((save_unfull && len % chunk_size) ? 1 : 0);
+}
 
-// Host-side chunk enumeration; returns LMKV_OK and fills `out` (if given).
-int enumerate(const int64_t* start, const int64_t* end, int32_t num_req, int32_t chunk_size,
-              int32_t save_unfull, std::vector<ChunkSpan>* out, int64_t* count) {
+// Validate the request list; returns the chunk count and the number of
+// requests that have at least one chunk.
+int check_requests(const int64_t* start, const int64_t* end, int32_t num_req, int32_t chunk_size,
+                   int32_t save_unfull, int64_t* num_chunks, int32_t* nonempty) {
     if (num_req < 0 || chunk_size <= 0) return LMKV_ERR_INVALID_ARG;
     if (num_req > 0 && (start == nullptr || end == nullptr)) return LMKV_ERR_INVALID_ARG;
     int64_t n = 0;
+    int32_t ne = 0;
     for (int32_t r = 0; r < num_req; ++r) {
         const int64_t s = start[r], e = end[r];
         if (s < 0 || e < s || s % chunk_size != 0) return LMKV_ERR_INVALID_ARG;
-        const int64_t len = e - s;
-        int64_t full = len / chunk_size;
-        const int64_t tail = len % chunk_size;
-        const int64_t nch = full + ((save_unfull && tail) ? 1 : 0);
-        if (out != nullptr) {
-            for (int64_t j = 0; j < nch; ++j) {
-                const int64_t t0 = s + j * chunk_size;
-                const int64_t t1 = (t0 + chunk_size < e) ? t0 + chunk_size : e;
-                out->push_back({r, t0, (int32_t)(t1 - t0)});
-            }
-        }
-        n += nch;
+        const int64_t c = request_chunks(s, e, chunk_size, save_unfull);
+        n += c;
+        ne += c > 0;
     }
     if (n > INT32_MAX) return LMKV_ERR_INVALID_ARG;
-    *count = n;
+    *num_chunks = n;
+    if (nonempty) *nonempty = ne;
     return LMKV_OK;
 }
 
@@ -75,98 +66,129 @@ int check_pool(const lmkv_pool_t* pool) {
     return LMKV_OK;
 }
 
-// Validate a call and build its launch parameter blocks.
-int prepare(const lmkv_pool_t* pool, const int32_t* block_table, int32_t max_blocks,
-            const int64_t* start, const int64_t* end, int32_t num_req, int32_t chunk_size,
-            int32_t save_unfull, void* const* chunk_ptrs, int32_t* d_status, int32_t layer_lo,
-            int32_t layer_n, int32_t parts, std::vector<Batch>* launches) {
-    int rc = check_pool(pool);
+// Everything a call needs besides the kernel choice.
+struct Call {
+    const lmkv_pool_t* pool;
+    const int32_t* block_table;
+    int32_t max_blocks;
+    const int64_t* start;
+    const int64_t* end;
+    int32_t num_req;
+    int32_t chunk_size;
+    int32_t save_unfull;
+    void* const* chunk_ptrs;
+    int32_t* d_status;
+    int32_t layer_lo;
+    int32_t layer_n;
+    int32_t parts;
+    int64_t num_chunks;
+    int32_t nonempty;
+};
+
+int validate(Call& c) {
+    int rc = check_pool(c.pool);
     if (rc != LMKV_OK) return rc;
-    if (chunk_size <= 0 || chunk_size % pool->block_size != 0) return LMKV_ERR_INVALID_ARG;
-    if (max_blocks < 0 || num_req < 0) return LMKV_ERR_INVALID_ARG;
-    if (layer_lo < 0 || layer_n <= 0 || layer_lo + layer_n > pool->num_layers)
+    if (c.chunk_size <= 0 || c.chunk_size % c.pool->block_size != 0) return LMKV_ERR_INVALID_ARG;
+    if (c.max_blocks < 0 || c.num_req < 0) return LMKV_ERR_INVALID_ARG;
+    if (c.layer_lo < 0 || c.layer_n <= 0 || c.layer_lo + c.layer_n > c.pool->num_layers)
         return LMKV_ERR_INVALID_ARG;
-    if (pool->block_size % parts != 0) parts = 1;
-    std::vector<ChunkSpan> chunks;
-    int64_t nch = 0;
-    rc = enumerate(start, end, num_req, chunk_size, save_unfull, &chunks, &nch);
+    if (c.pool->block_size % c.parts != 0) c.parts = 1;
+    rc = check_requests(c.start, c.end, c.num_req, c.chunk_size, c.save_unfull, &c.num_chunks,
+                        &c.nonempty);
     if (rc != LMKV_OK) return rc;
-    for (int32_t r = 0; r < num_req; ++r) {
-        if (end[r] > start[r] && (end[r] - 1) / pool->block_size >= max_blocks)
+    for (int32_t r = 0; r < c.num_req; ++r) {
+        if (c.end[r] > c.start[r] && (c.end[r] - 1) / c.pool->block_size >= c.max_blocks)
             return LMKV_ERR_INVALID_ARG;
     }
-    if (nch == 0) return LMKV_OK;
-    if (block_table == nullptr || chunk_ptrs == nullptr) return LMKV_ERR_INVALID_ARG;
-
-    Batch base;
-    std::memset(&base, 0, sizeof(base));
-    base.layer_base = reinterpret_cast<const uint8_t* const*>(pool->layer_base);
-    base.chunk_ptrs = reinterpret_cast<uint8_t* const*>(chunk_ptrs);
-    base.block_table = block_table;
-    base.status = d_status;
-    base.num_blocks = pool->num_blocks;
-    base.bt_stride = max_blocks;
-    base.num_layers = pool->num_layers;
-    base.row_bytes = pool->num_kv_heads * pool->head_dim * pool->elem_bytes;
-    base.block_size = pool->block_size;
-    base.chunk_size = chunk_size;
-    base.blocks_per_chunk = chunk_size / pool->block_size;
-    base.parts = parts;
-    base.layer_lo = layer_lo;
-    base.layer_n = layer_n;
-
-    // Pack requests with at least one chunk, kMaxReqPerLaunch per launch.
-    Batch cur = base;
-    int32_t g = 0;
-    size_t ci = 0;
-    while (ci < chunks.size()) {
-        const int32_t r = chunks[ci].req;
-        size_t cj = ci;
-        while (cj < chunks.size() && chunks[cj].req == r) ++cj;
-        if (cur.num_req == lmkv::kMaxReqPerLaunch) {
-            launches->push_back(cur);
-            const int32_t next_base = cur.chunk_base + cur.num_chunks;
-            cur = base;
-            cur.chunk_base = next_base;
-        }
-        const int i = cur.num_req++;
-        cur.req_row[i] = r;
-        cur.req_chunk_begin[i] = cur.num_chunks;
-        cur.req_tok0[i] = chunks[ci].tok0;
-        cur.req_tok_end[i] = chunks[cj - 1].tok0 + chunks[cj - 1].ntok;
-        cur.num_chunks += (int32_t)(cj - ci);
-        cur.req_chunk_begin[i + 1] = cur.num_chunks;
-        g += (int32_t)(cj - ci);
-        ci = cj;
-    }
-    if (cur.num_req > 0) launches->push_back(cur);
-    (void)g;
+    if (c.num_chunks > 0 && (c.block_table == nullptr || c.chunk_ptrs == nullptr))
+        return LMKV_ERR_INVALID_ARG;
     return LMKV_OK;
 }
 
-int finish_launch() {
-    const cudaError_t err = cudaGetLastError();
+// Pack the call's non-empty requests into parameter blocks of capacity
+// B::kCapacity and hand each block to `launch`.
+template <class B, class LaunchFn>
+int for_each_block(const Call& c, float* scales, LaunchFn&& launch) {
+    B b;
+    b.layer_base = reinterpret_cast<const uint8_t* const*>(c.pool->layer_base);
+    b.chunk_ptrs = reinterpret_cast<uint8_t* const*>(c.chunk_ptrs);
+    b.block_table = c.block_table;
+    b.status = c.d_status;
+    b.scales = scales;
+    b.num_blocks = c.pool->num_blocks;
+    b.bt_stride = c.max_blocks;
+    b.num_layers = c.pool->num_layers;
+    b.row_bytes = c.pool->num_kv_heads * c.pool->head_dim * c.pool->elem_bytes;
+    b.block_size = c.pool->block_size;
+    b.chunk_size = c.chunk_size;
+    b.blocks_per_chunk = c.chunk_size / c.pool->block_size;
+    b.parts = c.parts;
+    b.layer_lo = c.layer_lo;
+    b.layer_n = c.layer_n;
+    b.num_req = 0;
+    b.chunk_base = 0;
+    b.num_chunks = 0;
+    b.pad_ = 0;
+    b.req_chunk_begin[0] = 0;
+    for (int32_t r = 0; r < c.num_req; ++r) {
+        const int64_t nch = request_chunks(c.start[r], c.end[r], c.chunk_size, c.save_unfull);
+        if (nch == 0) continue;
+        if (b.num_req == B::kCapacity) {
+            const int rc = launch(b);
+            if (rc != LMKV_OK) return rc;
+            b.chunk_base += b.num_chunks;
+            b.num_chunks = 0;
+            b.num_req = 0;
+            b.req_chunk_begin[0] = 0;
+        }
+        const int i = b.num_req++;
+        b.req_row[i] = r;
+        b.req_chunk_begin[i] = b.num_chunks;
+        b.req_tok0[i] = c.start[r];
+        b.req_col0[i] = (int32_t)(c.start[r] / c.pool->block_size);
+        b.req_tok_end[i] = c.save_unfull ? c.end[r]
+                                          : c.start[r] + (c.end[r] - c.start[r]) / c.chunk_size * c.chunk_size;
+        b.num_chunks += (int32_t)nch;
+        b.req_chunk_begin[i + 1] = b.num_chunks;
+    }
+    if (b.num_req > 0) return launch(b);
+    return LMKV_OK;
+}
+
+// Launch with programmatic stream serialization (the kernels wait for their
+// predecessors with griddepcontrol.wait before touching memory).
+template <class Kernel, class... Args>
+int launch_pdl(Kernel kernel, int64_t grid, int threads, cudaStream_t stream, Args... args) {
+    if (grid <= 0) return LMKV_OK;
+    if (grid > INT32_MAX) return LMKV_ERR_INVALID_ARG;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, args...);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
     return err == cudaSuccess ? LMKV_OK : LMKV_ERR_CUDA;
 }
 
-// Number of CTAs the LSU engine launches for `items` items.
+// Number of CTAs the LSU engine launches for `items` items (one per item).
 int64_t lsu_grid(int64_t items) {
     const int64_t cap = (int64_t)1 << 30;
     return items < cap ? items : cap;
 }
 
-template <bool kGather>
-int launch_move(const std::vector<Batch>& launches, cudaStream_t stream) {
-    for (const Batch& b : launches) {
+template <class B, bool kGather>
+int launch_move(const Call& c, cudaStream_t stream) {
+    return for_each_block<B>(c, nullptr, [&](const B& b) {
         const int64_t items = lmkv::batch_items(b);
-        if (items == 0) continue;
-        lmkv::move_lsu_kernel<kGather, kLsuThreads, kLsuUnroll>
-            <<<(unsigned)lsu_grid(items), kLsuThreads, 0, stream>>>(b, items);
-        g_launches.fetch_add(1, std::memory_order_relaxed);
-        const int rc = finish_launch();
-        if (rc != LMKV_OK) return rc;
-    }
-    return LMKV_OK;
+        return launch_pdl(lmkv::move_lsu_kernel<B, kGather, kLsuThreads, kLsuUnroll>,
+                          lsu_grid(items), kLsuThreads, stream, b, items);
+    });
 }
 
 // Parts per block: split runs when the call has too few items to fill the GPU.
@@ -180,19 +202,21 @@ int move_entry(bool gather, const lmkv_pool_t* pool, const int32_t* block_table,
                int32_t layer, int32_t* d_status, void* stream) {
     const int rc0 = check_pool(pool);
     if (rc0 != LMKV_OK) return rc0;
-    int32_t lo = 0, n = pool->num_layers;
+    Call c{pool, block_table, max_blocks, start, end, num_req, chunk_size, save_unfull,
+           chunk_ptrs, d_status, 0, pool->num_layers, 1, 0, 0};
     if (layer >= 0) {
         if (layer >= pool->num_layers) return LMKV_ERR_INVALID_ARG;
-        lo = layer;
-        n = 1;
+        c.layer_lo = layer;
+        c.layer_n = 1;
     }
-    std::vector<Batch> launches;
-    const int rc = prepare(pool, block_table, max_blocks, start, end, num_req, chunk_size,
-                           save_unfull, chunk_ptrs, d_status, lo, n, choose_parts(pool, n),
-                           &launches);
-    if (rc != LMKV_OK) return rc;
+    c.parts = choose_parts(pool, c.layer_n);
+    const int rc = validate(c);
+    if (rc != LMKV_OK || c.num_chunks == 0) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    return gather ? launch_move<true>(launches, s) : launch_move<false>(launches, s);
+    if (c.nonempty <= lmkv::kSmallBatch)
+        return gather ? launch_move<lmkv::BatchSmall, true>(c, s)
+                      : launch_move<lmkv::BatchSmall, false>(c, s);
+    return gather ? launch_move<lmkv::Batch, true>(c, s) : launch_move<lmkv::Batch, false>(c, s);
 }
 
 int check_fp8_pool(const lmkv_pool_t* pool, int32_t chunk_size) {
@@ -204,6 +228,42 @@ int check_fp8_pool(const lmkv_pool_t* pool, int32_t chunk_size) {
     return LMKV_OK;
 }
 
+template <class B>
+int launch_quant(const Call& c, float* scales, cudaStream_t stream) {
+    return for_each_block<B>(c, scales, [&](const B& b) {
+        const int64_t tiles = (int64_t)b.num_chunks * 2 * b.layer_n;
+        return launch_pdl(lmkv::quant_gather_kernel<B, kQuantThreads, kQuantVPT, kQuantCluster>,
+                          tiles * kQuantCluster, kQuantThreads, stream, b);
+    });
+}
+
+template <class B>
+int launch_dequant(const Call& c, float* scales, cudaStream_t stream) {
+    return for_each_block<B>(c, scales, [&](const B& b) {
+        const int64_t items = lmkv::batch_items(b);
+        return launch_pdl(lmkv::dequant_scatter_kernel<B, kDequantThreads>, lsu_grid(items),
+                          kDequantThreads, stream, b, items);
+    });
+}
+
+int fp8_entry(bool gather, const lmkv_pool_t* pool, const int32_t* block_table, int32_t max_blocks,
+              const int64_t* start, const int64_t* end, int32_t num_req, int32_t chunk_size,
+              int32_t save_unfull, void* const* code_ptrs, float* scales, int32_t* d_status,
+              void* stream) {
+    int rc = check_fp8_pool(pool, chunk_size);
+    if (rc != LMKV_OK) return rc;
+    Call c{pool, block_table, max_blocks, start, end, num_req, chunk_size, save_unfull,
+           code_ptrs, d_status, 0, pool->num_layers, 1, 0, 0};
+    rc = validate(c);
+    if (rc != LMKV_OK || c.num_chunks == 0) return rc;
+    if (scales == nullptr) return LMKV_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (c.nonempty <= lmkv::kSmallBatch)
+        return gather ? launch_quant<lmkv::BatchSmall>(c, scales, s)
+                      : launch_dequant<lmkv::BatchSmall>(c, scales, s);
+    return gather ? launch_quant<lmkv::Batch>(c, scales, s) : launch_dequant<lmkv::Batch>(c, scales, s);
+}
+
 }  // namespace
 
 extern "C" {
@@ -212,7 +272,7 @@ int lmkv_count_chunks(const int64_t* start, const int64_t* end, int32_t num_req,
                       int32_t chunk_size, int32_t save_unfull_chunk, int32_t* out_num_chunks) {
     if (out_num_chunks == nullptr) return LMKV_ERR_INVALID_ARG;
     int64_t n = 0;
-    const int rc = enumerate(start, end, num_req, chunk_size, save_unfull_chunk, nullptr, &n);
+    const int rc = check_requests(start, end, num_req, chunk_size, save_unfull_chunk, &n, nullptr);
     if (rc != LMKV_OK) return rc;
     *out_num_chunks = (int32_t)n;
     return LMKV_OK;
@@ -221,17 +281,22 @@ int lmkv_count_chunks(const int64_t* start, const int64_t* end, int32_t num_req,
 int lmkv_enumerate_chunks(const int64_t* start, const int64_t* end, int32_t num_req,
                           int32_t chunk_size, int32_t save_unfull_chunk, int32_t* out_req,
                           int64_t* out_tok0, int32_t* out_ntok, int32_t capacity) {
-    std::vector<ChunkSpan> chunks;
     int64_t n = 0;
-    const int rc = enumerate(start, end, num_req, chunk_size, save_unfull_chunk, &chunks, &n);
+    const int rc = check_requests(start, end, num_req, chunk_size, save_unfull_chunk, &n, nullptr);
     if (rc != LMKV_OK) return rc;
     if (n > capacity) return LMKV_ERR_INVALID_ARG;
     if (n > 0 && (out_req == nullptr || out_tok0 == nullptr || out_ntok == nullptr))
         return LMKV_ERR_INVALID_ARG;
-    for (int64_t g = 0; g < n; ++g) {
-        out_req[g] = chunks[g].req;
-        out_tok0[g] = chunks[g].tok0;
-        out_ntok[g] = chunks[g].ntok;
+    int64_t g = 0;
+    for (int32_t r = 0; r < num_req; ++r) {
+        const int64_t nch = request_chunks(start[r], end[r], chunk_size, save_unfull_chunk);
+        for (int64_t j = 0; j < nch; ++j, ++g) {
+            const int64_t t0 = start[r] + j * chunk_size;
+            const int64_t t1 = t0 + chunk_size < end[r] ? t0 + chunk_size : end[r];
+            out_req[g] = r;
+            out_tok0[g] = t0;
+            out_ntok[g] = (int32_t)(t1 - t0);
+        }
     }
     return LMKV_OK;
 }
@@ -275,26 +340,8 @@ int lmkv_gather_chunks_fp8e4m3(const lmkv_pool_t* pool, const int32_t* block_tab
                                int32_t num_req, int32_t chunk_size, int32_t save_unfull_chunk,
                                void* const* code_ptrs, float* scales, int32_t* d_status,
                                void* stream) {
-    int rc = check_fp8_pool(pool, chunk_size);
-    if (rc != LMKV_OK) return rc;
-    std::vector<Batch> launches;
-    rc = prepare(pool, block_table, max_blocks, start, end, num_req, chunk_size,
-                 save_unfull_chunk, code_ptrs, d_status, 0, pool->num_layers, 1, &launches);
-    if (rc != LMKV_OK) return rc;
-    if (!launches.empty() && scales == nullptr) return LMKV_ERR_INVALID_ARG;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    for (Batch& b : launches) {
-        b.scales = scales;
-        const int64_t tiles = (int64_t)b.num_chunks * 2 * b.layer_n;
-        const int64_t ctas = tiles * kQuantCluster;
-        if (ctas > INT32_MAX) return LMKV_ERR_INVALID_ARG;
-        lmkv::quant_gather_kernel<kQuantThreads, kQuantVPT, kQuantCluster>
-            <<<(unsigned)ctas, kQuantThreads, 0, s>>>(b);
-        g_launches.fetch_add(1, std::memory_order_relaxed);
-        rc = finish_launch();
-        if (rc != LMKV_OK) return rc;
-    }
-    return LMKV_OK;
+    return fp8_entry(true, pool, block_table, max_blocks, start, end, num_req, chunk_size,
+                     save_unfull_chunk, code_ptrs, scales, d_status, stream);
 }
 
 int lmkv_scatter_chunks_fp8e4m3(const lmkv_pool_t* pool, const int32_t* block_table,
@@ -302,24 +349,8 @@ int lmkv_scatter_chunks_fp8e4m3(const lmkv_pool_t* pool, const int32_t* block_ta
                                 int32_t num_req, int32_t chunk_size, int32_t save_unfull_chunk,
                                 void* const* code_ptrs, const float* scales, int32_t* d_status,
                                 void* stream) {
-    int rc = check_fp8_pool(pool, chunk_size);
-    if (rc != LMKV_OK) return rc;
-    std::vector<Batch> launches;
-    rc = prepare(pool, block_table, max_blocks, start, end, num_req, chunk_size,
-                 save_unfull_chunk, code_ptrs, d_status, 0, pool->num_layers, 1, &launches);
-    if (rc != LMKV_OK) return rc;
-    if (!launches.empty() && scales == nullptr) return LMKV_ERR_INVALID_ARG;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    for (Batch& b : launches) {
-        b.scales = const_cast<float*>(scales);
-        const int64_t items = lmkv::batch_items(b);
-        lmkv::dequant_scatter_kernel<kDequantThreads>
-            <<<(unsigned)lsu_grid(items), kDequantThreads, 0, s>>>(b, items);
-        g_launches.fetch_add(1, std::memory_order_relaxed);
-        rc = finish_launch();
-        if (rc != LMKV_OK) return rc;
-    }
-    return LMKV_OK;
+    return fp8_entry(false, pool, block_table, max_blocks, start, end, num_req, chunk_size,
+                     save_unfull_chunk, code_ptrs, const_cast<float*>(scales), d_status, stream);
 }
 
 const char* lmkv_status_string(int status) {

@@ -32,13 +32,16 @@
 
 namespace lmkv {
 
-constexpr int kMaxReqPerLaunch = 256;
 constexpr int kStatusBadBlock = 5;    // LMKV_ERR_BAD_BLOCK
 constexpr int kStatusBadPointer = 6;  // LMKV_ERR_BAD_POINTER
 constexpr int kStatusTimeout = 7;     // LMKV_ERR_TIMEOUT (bounded waits gave up)
 
 // By-value launch parameters (kept in the constant bank via __grid_constant__).
-struct Batch {
+// kCap = requests one launch can carry; calls with few requests use a small
+// block so the launch copies a few hundred bytes of parameters, not kilobytes.
+template <int kCap>
+struct BatchT {
+    static constexpr int kCapacity = kCap;
     const uint8_t* const* layer_base;   // DEVICE [num_layers] pool layer bases
     uint8_t* const* chunk_ptrs;         // DEVICE [total chunks] chunk (or code) buffers
     const int32_t* block_table;         // DEVICE [num_req_total][bt_stride]
@@ -58,24 +61,43 @@ struct Batch {
     int32_t chunk_base;                 // global index of this launch's chunk 0
     int32_t num_chunks;                 // chunks in this launch
     int32_t pad_;
-    int32_t req_row[kMaxReqPerLaunch];              // block-table row of packed request i
-    int32_t req_chunk_begin[kMaxReqPerLaunch + 1];  // local chunk index of its first chunk
-    int64_t req_tok0[kMaxReqPerLaunch];             // its first enumerated token
-    int64_t req_tok_end[kMaxReqPerLaunch];          // end (exclusive) of its enumerated tokens
+    int64_t req_tok0[kCap];             // first enumerated token of packed request i
+    int64_t req_tok_end[kCap];          // end (exclusive) of its enumerated tokens
+    int32_t req_row[kCap];              // its block-table row
+    int32_t req_col0[kCap];             // block-table column of its first token (tok0 / B)
+    int32_t req_chunk_begin[kCap + 1];  // local chunk index of its first chunk
 };
 
-__host__ __device__ inline int64_t batch_items(const Batch& p) {
+constexpr int kSmallBatch = 8;
+constexpr int kMaxReqPerLaunch = 256;
+using BatchSmall = BatchT<kSmallBatch>;
+using Batch = BatchT<kMaxReqPerLaunch>;
+
+template <class B>
+__host__ __device__ inline int64_t batch_items(const B& p) {
     return (int64_t)p.num_chunks * 2 * p.layer_n * p.blocks_per_chunk * p.parts;
+}
+
+// Programmatic dependent launch: let the next kernel on the stream be
+// scheduled during this one's tail, and wait for every prerequisite grid
+// (complete, memory visible) before touching global memory.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 struct ChunkRef {
     int32_t req_row;
     int32_t ntok;
+    int32_t col0;       // block-table column of the chunk's first token
     int64_t tok0;
 };
 
 // Chunk gl (local) -> its request: the last packed request whose first chunk <= gl.
-__device__ __forceinline__ ChunkRef resolve_chunk(const Batch& p, int32_t gl) {
+template <class B>
+__device__ __forceinline__ ChunkRef resolve_chunk(const B& p, int32_t gl) {
     int lo = 0, hi = p.num_req - 1;
     while (lo < hi) {
         int mid = (lo + hi + 1) >> 1;
@@ -84,12 +106,14 @@ __device__ __forceinline__ ChunkRef resolve_chunk(const Batch& p, int32_t gl) {
     ChunkRef c;
     c.req_row = p.req_row[lo];
     c.tok0 = p.req_tok0[lo] + (int64_t)(gl - p.req_chunk_begin[lo]) * p.chunk_size;
+    c.col0 = p.req_col0[lo] + (gl - p.req_chunk_begin[lo]) * p.blocks_per_chunk;
     int64_t left = p.req_tok_end[lo] - c.tok0;
     c.ntok = (int32_t)(left < p.chunk_size ? left : p.chunk_size);
     return c;
 }
 
-__device__ __forceinline__ void report(const Batch& p, int code) {
+template <class B>
+__device__ __forceinline__ void report(const B& p, int code) {
     if (p.status != nullptr) atomicCAS(p.status, 0, code);
 }
 
@@ -101,7 +125,8 @@ struct Run {
     uint32_t bytes;
 };
 
-__device__ __forceinline__ bool item_run(const Batch& p, int64_t item, Run& run) {
+template <class B>
+__device__ __forceinline__ bool item_run(const B& p, int64_t item, Run& run) {
     const int q = (int)(item % p.parts);
     int64_t t = item / p.parts;
     const int j = (int)(t % p.blocks_per_chunk);
@@ -116,7 +141,7 @@ __device__ __forceinline__ bool item_run(const Batch& p, int64_t item, Run& run)
     if (row0 >= c.ntok) return false;                       // past a partial chunk's end
     const int rows = min(part_rows, c.ntok - row0);
     const int l = p.layer_lo + ll;
-    const int64_t col = c.tok0 / p.block_size + j;
+    const int64_t col = c.col0 + j;
     const int64_t blk = p.block_table[(int64_t)c.req_row * p.bt_stride + col];
     if (blk < 0 || blk >= p.num_blocks) { report(p, kStatusBadBlock); return false; }
     uint8_t* lb = const_cast<uint8_t*>(p.layer_base[l]);
@@ -171,9 +196,11 @@ __device__ __forceinline__ void cta_copy(const uint8_t* __restrict__ src, uint8_
 
 // LSU engine.  kGather: pool -> chunk, else chunk -> pool.  Grid-stride over
 // items, so the grid may be the item count (one CTA per item) or smaller.
-template <bool kGather, int kThreads, int kUnroll>
+template <class B, bool kGather, int kThreads, int kUnroll>
 __global__ void __launch_bounds__(kThreads)
-move_lsu_kernel(const __grid_constant__ Batch p, int64_t num_items) {
+move_lsu_kernel(const __grid_constant__ B p, int64_t num_items) {
+    pdl_launch_dependents();
+    pdl_wait();
     for (int64_t item = blockIdx.x; item < num_items; item += gridDim.x) {
         Run run;
         if (!item_run(p, item, run)) continue;
@@ -249,7 +276,7 @@ struct Piece {
 };
 
 // Sequential cursor over the pieces of the items this CTA owns.
-template <bool kGather, int kStageBytes>
+template <class B, bool kGather, int kStageBytes>
 struct PieceCursor {
     int64_t item;
     int64_t num_items;
@@ -258,7 +285,7 @@ struct PieceCursor {
     uint32_t off;
     bool have_run;
 
-    __device__ __forceinline__ void init(const Batch& p, int64_t first, int64_t n, int64_t s) {
+    __device__ __forceinline__ void init(const B& p, int64_t first, int64_t n, int64_t s) {
         item = first;
         num_items = n;
         stride = s;
@@ -266,7 +293,7 @@ struct PieceCursor {
         off = 0;
         advance_item(p);
     }
-    __device__ __forceinline__ void advance_item(const Batch& p) {
+    __device__ __forceinline__ void advance_item(const B& p) {
         have_run = false;
         while (item < num_items) {
             const bool ok = item_run(p, item, run);
@@ -274,7 +301,7 @@ struct PieceCursor {
             if (ok && run.bytes > 0) { have_run = true; off = 0; return; }
         }
     }
-    __device__ __forceinline__ bool next(const Batch& p, Piece& pc) {
+    __device__ __forceinline__ bool next(const B& p, Piece& pc) {
         if (!have_run) return false;
         const uint32_t left = run.bytes - off;
         const uint32_t n = left < (uint32_t)kStageBytes ? left : (uint32_t)kStageBytes;
@@ -291,16 +318,18 @@ struct PieceCursor {
 // stages.  Loads run kStages-1 ahead of stores; a stage is refilled once the
 // bulk store that read it has finished reading (wait_group.read with one
 // group of slack).
-template <bool kGather, int kStages, int kStageBytes>
+template <class B, bool kGather, int kStages, int kStageBytes>
 __global__ void __launch_bounds__(32)
-move_bulk_kernel(const __grid_constant__ Batch p, int64_t num_items) {
+move_bulk_kernel(const __grid_constant__ B p, int64_t num_items) {
     extern __shared__ __align__(128) uint8_t stage_mem[];
     __shared__ __align__(8) uint64_t bar[kStages];
+    pdl_launch_dependents();
+    pdl_wait();
     if (threadIdx.x != 0) return;
     for (int s = 0; s < kStages; ++s) mbar_init(&bar[s], 1);
     fence_barrier_init();
 
-    PieceCursor<kGather, kStageBytes> cur;
+    PieceCursor<B, kGather, kStageBytes> cur;
     cur.init(p, blockIdx.x, num_items, gridDim.x);
     Piece ring[kStages];
     uint32_t k_load = 0, k_store = 0;
@@ -344,137 +373,288 @@ move_bulk_kernel(const __grid_constant__ Batch p, int64_t num_items) {
 // tile (R = ceil(n_g / kCluster)).  Values stay in registers between the
 // absmax pass and the quantising pass when the slice fits in
 // kThreads * kVPT vectors of 16 bytes; otherwise the rest is re-read.
+// The absmax is exchanged through distributed shared memory with one split
+// cluster barrier; there is no CTA-wide barrier.
 constexpr int kQuantMaxRows = 256;   // rows per CTA slice (chunk_size <= kCluster * 256)
 
-__device__ __forceinline__ uint32_t absmax_bf16x8(const uint4& v) {
+// Running max of |x| over 8 bf16 values, as bf16x2 bit patterns (the sign bit
+// cleared, so max.bf16x2 of the magnitudes is exact).
+__device__ __forceinline__ uint32_t absmax_bf16x8(uint32_t acc, const uint4& v) {
     const uint32_t m = 0x7FFF7FFFu;
-    uint32_t a = __vmaxu2(v.x & m, v.y & m);
-    uint32_t b = __vmaxu2(v.z & m, v.w & m);
-    a = __vmaxu2(a, b);
-    return max(a & 0xFFFFu, a >> 16);
+    auto as_bf2 = [](uint32_t w) { return *reinterpret_cast<const __nv_bfloat162*>(&w); };
+    __nv_bfloat162 a = __hmax2(as_bf2(v.x & m), as_bf2(v.y & m));
+    __nv_bfloat162 b = __hmax2(as_bf2(v.z & m), as_bf2(v.w & m));
+    a = __hmax2(__hmax2(a, b), as_bf2(acc));
+    return *reinterpret_cast<const uint32_t*>(&a);
 }
 
-__device__ __forceinline__ uint2 quant_bf16x8(const uint4& v, float scale) {
+// x / d for a runtime divisor that is usually a power of two.
+struct UDiv {
+    uint32_t d;
+    int32_t shift;      // log2(d) when d is a power of two, else -1
+    __device__ __forceinline__ explicit UDiv(uint32_t dv) : d(dv), shift(-1) {
+#ifdef __CUDA_ARCH__
+        if (__popc(dv) == 1) shift = __ffs(dv) - 1;
+#endif
+    }
+    __device__ __forceinline__ uint32_t div(uint32_t x) const { return shift >= 0 ? x >> shift : x / d; }
+};
+
+// Correctly rounded x / s for a per-tile constant s, from the correctly
+// rounded reciprocal r = RN(1/s): q0 = RN(x*r) is within an ulp of x/s, the
+// remainder q0*s - x is exact in one FMA, and one correction step
+// RN(q0 - rem*r) yields RN(x/s) (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1),
+// 1990).  The remainder is exact only while it stays out of the fp32
+// subnormal range: it is a multiple of ulp(q0) * ulp(s), which needs
+// exponent(q0) + exponent(s) >= -103.  With s >= 2^-90 that holds for every
+// |q| >= 2^-13, and quotients below 2^-11 round to a signed e4m3 zero however
+// their last bits come out; smaller scales take the IEEE division instead
+// (kFastDivMinScale).
+//
+// The kernel evaluates the steps on y = -x, whose remainder q0*s - y is
+// q0*s + x, so the unpacked x is used as it is, and under round-to-nearest
+// every zero quotient keeps the sign of y.  e4m3 is sign-magnitude and its
+// rounding and saturation are symmetric, so the codes of x / s are those of
+// y / s with the sign bit flipped.  Two lanes at a time use the packed fp32
+// pipe (mul/fma .f32x2).  The tests compare the codes exhaustively with IEEE
+// division over every bf16 input and every scale a bf16 absmax can produce.
+constexpr float kFastDivMinScale = 0x1p-90f;
+
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+// Four fp32 values -> four e4m3 codes (round to nearest even, saturating),
+// byte i of the result from value i.
+__device__ __forceinline__ uint32_t e4m3x4(float v0, float v1, float v2, float v3) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+        "mov.b32 %0, {lo, hi};\n\t}"
+        : "=r"(r) : "f"(v0), "f"(v1), "f"(v2), "f"(v3));
+    return r;
+}
+__device__ __forceinline__ uint32_t e4m3x4(uint64_t a, uint64_t b) {
+    float a0, a1, b0, b1;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(a));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(b0), "=f"(b1) : "l"(b));
+    return e4m3x4(a0, a1, b0, b1);
+}
+
+// Per-tile constants of the quantiser.
+struct QuantK {
+    float scale;
+    uint64_t s2;     // {s, s}
+    uint64_t nr2;    // {-RN(1/s), -RN(1/s)}
+};
+
+__device__ __forceinline__ QuantK make_quant(float scale, bool fast) {
+    QuantK k;
+    k.scale = scale;
+    const float nr = fast ? -__frcp_rn(scale) : 0.0f;
+    k.s2 = f2_pack(scale, scale);
+    k.nr2 = f2_pack(nr, nr);
+    return k;
+}
+
+// 8 bf16 values (one 16-byte vector) -> 8 e4m3 codes.
+template <bool kFastDiv>
+__device__ __forceinline__ uint2 quant_bf16x8(const uint4& v, const QuantK& k) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t out[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-        uint32_t packed = 0;
+        if (kFastDiv) {
+            uint64_t q[2];
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const uint32_t word = w[h * 2 + k];
-            float2 f;
-            f.x = __fdiv_rn(__uint_as_float(word << 16), scale);
-            f.y = __fdiv_rn(__uint_as_float(word & 0xFFFF0000u), scale);
-            const __nv_fp8x2_storage_t q = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
-            packed |= (uint32_t)q << (16 * k);
+            for (int i = 0; i < 2; ++i) {
+                const uint32_t word = w[2 * h + i];
+                const uint64_t x2 = f2_pack(__uint_as_float(word << 16),
+                                            __uint_as_float(word & 0xFFFF0000u));
+                const uint64_t q0 = f2_mul(x2, k.nr2);           // RN(y * r), y = -x
+                const uint64_t rem = f2_fma(q0, k.s2, x2);       // q0 * s - y, exact
+                q[i] = f2_fma(rem, k.nr2, q0);                   // RN(y / s)
+            }
+            out[h] = e4m3x4(q[0], q[1]) ^ 0x80808080u;           // codes of x / s
+        } else {
+            const uint32_t w0 = w[2 * h], w1 = w[2 * h + 1];
+            out[h] = e4m3x4(__fdiv_rn(__uint_as_float(w0 << 16), k.scale),
+                            __fdiv_rn(__uint_as_float(w0 & 0xFFFF0000u), k.scale),
+                            __fdiv_rn(__uint_as_float(w1 << 16), k.scale),
+                            __fdiv_rn(__uint_as_float(w1 & 0xFFFF0000u), k.scale));
         }
-        out[h] = packed;
     }
     return make_uint2(out[0], out[1]);
 }
 
-template <int kThreads, int kVPT, int kCluster>
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Where the CTA's vectors come from: vector v of the slice is row v / vpr,
+// 16-byte column v % vpr.  With kThreads a multiple of vpr each thread keeps
+// one column and steps rows by kThreads / vpr.
+struct SliceMap {
+    const uint8_t* kv_base;     // pool layer l, K or V half
+    const int32_t* bt;          // block-table entries of the chunk (column tok0 / B)
+    uint32_t r0, vpr, row_bytes, block_size, num_blocks;
+    UDiv bdiv, vdiv;
+    __device__ __forceinline__ SliceMap(const uint8_t* kvb, const int32_t* btc, uint32_t r0_,
+                                        uint32_t vpr_, uint32_t rb, uint32_t bs, uint32_t nb)
+        : kv_base(kvb), bt(btc), r0(r0_), vpr(vpr_), row_bytes(rb), block_size(bs), num_blocks(nb),
+          bdiv(bs), vdiv(vpr_) {}
+    // Source of slice vector v (row-major over the slice), or null for a bad block.
+    __device__ __forceinline__ const uint8_t* src(uint32_t row_local, uint32_t col) const {
+        const uint32_t row = r0 + row_local;
+        const uint32_t jb = bdiv.div(row);
+        const int32_t blk = bt[jb];
+        if ((uint32_t)blk >= num_blocks) return nullptr;
+        const uint32_t slot = row - jb * block_size;
+        return kv_base + ((int64_t)blk * block_size + slot) * row_bytes + col * 16u;
+    }
+};
+
+// Quantise the CTA's slice from registers (and re-read the part that did not
+// fit), writing 8 codes per 16-byte source vector.
+template <bool kFastDiv, int kThreads, int kVPT>
+__device__ __forceinline__ void quant_slice(const uint4 (&regs)[kVPT], uint32_t valid, uint32_t nvec,
+                                            const SliceMap& sm, uint8_t* tile_codes, const QuantK& k) {
+#pragma unroll
+    for (int u = 0; u < kVPT; ++u) {
+        const uint32_t v = threadIdx.x + u * kThreads;
+        if (v < nvec && (valid >> u) & 1u) {
+            const uint2 q = k.scale == 0.0f ? make_uint2(0, 0) : quant_bf16x8<kFastDiv>(regs[u], k);
+            *reinterpret_cast<uint2*>(tile_codes + (int64_t)v * 8) = q;
+        }
+    }
+    for (uint32_t v = threadIdx.x + kVPT * kThreads; v < nvec; v += kThreads) {
+        const uint32_t row = sm.vdiv.div(v);
+        const uint8_t* src = sm.src(row, v - row * sm.vpr);
+        if (src == nullptr) continue;
+        const int4 x = ld_stream(reinterpret_cast<const int4*>(src));
+        const uint4 xv = make_uint4((uint32_t)x.x, (uint32_t)x.y, (uint32_t)x.z, (uint32_t)x.w);
+        const uint2 q = k.scale == 0.0f ? make_uint2(0, 0) : quant_bf16x8<kFastDiv>(xv, k);
+        *reinterpret_cast<uint2*>(tile_codes + (int64_t)v * 8) = q;
+    }
+}
+
+template <class B, int kThreads, int kVPT, int kCluster>
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
-quant_gather_kernel(const __grid_constant__ Batch p) {
+quant_gather_kernel(const __grid_constant__ B p) {
     namespace cg = cooperative_groups;
     cg::cluster_group cluster = cg::this_cluster();
-    __shared__ const uint8_t* row_src[kQuantMaxRows];
     __shared__ uint32_t warp_max[kThreads / 32];
-    __shared__ uint32_t cta_max;
-    __shared__ uint32_t tile_max;
+    static_assert(kThreads / 32 <= 32, "one lane per warp slot");
+    pdl_launch_dependents();
+    pdl_wait();
 
     const int rank = (int)cluster.block_rank();
-    const int64_t tile = blockIdx.x / kCluster;
-    const int ll = (int)(tile % p.layer_n);
-    const int kv = (int)((tile / p.layer_n) & 1);
-    const int gl = (int)(tile / p.layer_n / 2);
-    const int l = p.layer_lo + ll;
+    const uint32_t tile = blockIdx.x / kCluster;
+    const uint32_t ll = tile % (uint32_t)p.layer_n;
+    const uint32_t kv = (tile / (uint32_t)p.layer_n) & 1u;
+    const int gl = (int)(tile / (uint32_t)p.layer_n / 2u);
+    const int l = p.layer_lo + (int)ll;
     const ChunkRef c = resolve_chunk(p, gl);
-    const int rows_per = (c.ntok + kCluster - 1) / kCluster;
-    const int r0 = rank * rows_per;
-    const int nrows = max(0, min(c.ntok, r0 + rows_per) - r0);
-    const int vpr = p.row_bytes >> 4;             // 16-byte vectors per row
-    const int row_elems = p.row_bytes >> 1;
-    const int nvec = nrows * vpr;
+    const uint32_t rows_per = (uint32_t)(c.ntok + kCluster - 1) / kCluster;
+    const uint32_t r0 = rank * rows_per;
+    const uint32_t nrows = (uint32_t)max(0, min(c.ntok, (int)(r0 + rows_per)) - (int)r0);
+    const uint32_t vpr = (uint32_t)p.row_bytes >> 4;      // 16-byte vectors per row
+    const uint32_t row_elems = (uint32_t)p.row_bytes >> 1;
+    const uint32_t nvec = nrows * vpr;
+    const int lane = threadIdx.x & 31;
 
     uint8_t* codes = p.chunk_ptrs[p.chunk_base + gl];
     const uint8_t* lb = p.layer_base[l];
     const bool ptr_ok = codes != nullptr && lb != nullptr &&
                         ((reinterpret_cast<uintptr_t>(codes) | reinterpret_cast<uintptr_t>(lb)) & 15) == 0;
     if (!ptr_ok && threadIdx.x == 0 && rank == 0) report(p, kStatusBadPointer);
-    for (int i = threadIdx.x; i < nrows; i += kThreads) {
-        const int row = r0 + i;
-        const int64_t tok = c.tok0 + row;
-        const int64_t blk = p.block_table[(int64_t)c.req_row * p.bt_stride + tok / p.block_size];
-        const uint8_t* src = nullptr;
-        if (blk < 0 || blk >= p.num_blocks) report(p, kStatusBadBlock);
-        else if (ptr_ok)
-            src = lb + ((kv * p.num_blocks + blk) * p.block_size + tok % p.block_size) * (int64_t)p.row_bytes;
-        row_src[i] = src;
-    }
-    __syncthreads();
+    const SliceMap sm(lb + (int64_t)kv * p.num_blocks * p.block_size * p.row_bytes,
+                      p.block_table + (int64_t)c.req_row * p.bt_stride + c.col0,
+                      r0, vpr, (uint32_t)p.row_bytes, (uint32_t)p.block_size, (uint32_t)p.num_blocks);
 
+    // Pass 1: load the slice and take the running max of |x| on bf16 bits.
+    const bool col_fixed = (kThreads % vpr) == 0;
+    const uint32_t t_row = threadIdx.x / vpr, t_col = threadIdx.x - t_row * vpr;
+    const uint32_t rstep = kThreads / vpr;
     uint4 regs[kVPT];
-    uint32_t m = 0;
+    uint32_t valid = 0;
+    uint32_t acc = 0;
+    bool bad = false;
 #pragma unroll
     for (int u = 0; u < kVPT; ++u) {
-        const int v = threadIdx.x + u * kThreads;
+        const uint32_t v = threadIdx.x + u * kThreads;
         regs[u] = make_uint4(0, 0, 0, 0);
-        if (v < nvec) {
-            const uint8_t* src = row_src[v / vpr];
-            if (src != nullptr) {
-                const int4 x = ld_stream(reinterpret_cast<const int4*>(src) + (v % vpr));
+        if (ptr_ok && v < nvec) {
+            uint32_t row, col;
+            if (col_fixed) { row = t_row + u * rstep; col = t_col; }
+            else { row = sm.vdiv.div(v); col = v - row * vpr; }
+            const uint8_t* src = sm.src(row, col);
+            if (src == nullptr) {
+                bad = true;
+            } else {
+                const int4 x = ld_stream(reinterpret_cast<const int4*>(src));
                 regs[u] = make_uint4((uint32_t)x.x, (uint32_t)x.y, (uint32_t)x.z, (uint32_t)x.w);
-                m = max(m, absmax_bf16x8(regs[u]));
+                valid |= 1u << u;
             }
         }
     }
-    for (int v = threadIdx.x + kVPT * kThreads; v < nvec; v += kThreads) {
-        const uint8_t* src = row_src[v / vpr];
-        if (src == nullptr) continue;
-        const int4 x = ld_stream(reinterpret_cast<const int4*>(src) + (v % vpr));
-        m = max(m, absmax_bf16x8(make_uint4((uint32_t)x.x, (uint32_t)x.y, (uint32_t)x.z, (uint32_t)x.w)));
+#pragma unroll
+    for (int u = 0; u < kVPT; ++u) acc = absmax_bf16x8(acc, regs[u]);
+    for (uint32_t v = threadIdx.x + kVPT * kThreads; ptr_ok && v < nvec; v += kThreads) {
+        const uint32_t row = sm.vdiv.div(v);
+        const uint8_t* src = sm.src(row, v - row * vpr);
+        if (src == nullptr) { bad = true; continue; }
+        const int4 x = ld_stream(reinterpret_cast<const int4*>(src));
+        acc = absmax_bf16x8(acc, make_uint4((uint32_t)x.x, (uint32_t)x.y, (uint32_t)x.z, (uint32_t)x.w));
     }
+    if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) report(p, kStatusBadBlock);
+    uint32_t m = max(acc & 0xFFFFu, acc >> 16);
     m = __reduce_max_sync(0xFFFFFFFFu, m);
-    if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = m;
-    __syncthreads();
-    if (threadIdx.x < 32) {
-        uint32_t w = threadIdx.x < kThreads / 32 ? warp_max[threadIdx.x] : 0u;
-        w = __reduce_max_sync(0xFFFFFFFFu, w);
-        if (threadIdx.x == 0) cta_max = w;
-    }
-    cluster.sync();                               // every CTA's cta_max is visible
-    if (threadIdx.x < 32) {
-        uint32_t w = 0;
-        if (threadIdx.x < kCluster) w = *cluster.map_shared_rank(&cta_max, (unsigned)threadIdx.x);
-        w = __reduce_max_sync(0xFFFFFFFFu, w);
-        if (threadIdx.x == 0) tile_max = w;
-    }
-    cluster.sync();                               // remote reads done before any CTA may exit
-    const float amax = __uint_as_float(tile_max << 16);
+    if (lane == 0) warp_max[threadIdx.x >> 5] = m;
+
+    // Exchange: every warp reads all warp maxima of all CTAs of the cluster.
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    uint32_t w = 0;
+    constexpr int kSlots = kCluster * (kThreads / 32);
+    for (int i = lane; i < kSlots; i += 32)
+        w = max(w, *cluster.map_shared_rank(&warp_max[i % (kThreads / 32)], (unsigned)(i / (kThreads / 32))));
+    w = __reduce_max_sync(0xFFFFFFFFu, w);
+    cluster_arrive_relaxed();          // this CTA's shared memory may be released after everyone arrives
+
+    const float amax = __uint_as_float(w << 16);
     const float scale = __fdiv_rn(amax, 448.0f);
     if (rank == 0 && threadIdx.x == 0 && p.scales != nullptr)
         p.scales[((int64_t)(p.chunk_base + gl) * 2 + kv) * p.num_layers + l] = scale;
-    if (!ptr_ok) return;
-
-    uint8_t* tile_codes = codes + (((int64_t)kv * p.num_layers + l) * c.ntok + r0) * row_elems;
-#pragma unroll
-    for (int u = 0; u < kVPT; ++u) {
-        const int v = threadIdx.x + u * kThreads;
-        if (v < nvec && row_src[v / vpr] != nullptr) {
-            const uint2 q = scale == 0.0f ? make_uint2(0, 0) : quant_bf16x8(regs[u], scale);
-            *reinterpret_cast<uint2*>(tile_codes + (int64_t)v * 8) = q;
+    if (ptr_ok) {
+        uint8_t* tile_codes = codes + (((int64_t)kv * p.num_layers + l) * c.ntok + r0) * row_elems;
+        if (scale >= kFastDivMinScale) {          // reciprocal + correction
+            quant_slice<true, kThreads, kVPT>(regs, valid, nvec, sm, tile_codes, make_quant(scale, true));
+        } else {                                  // zero or tiny scale: IEEE division
+            quant_slice<false, kThreads, kVPT>(regs, valid, nvec, sm, tile_codes, make_quant(scale, false));
         }
     }
-    for (int v = threadIdx.x + kVPT * kThreads; v < nvec; v += kThreads) {
-        const uint8_t* src = row_src[v / vpr];
-        if (src == nullptr) continue;
-        const int4 x = ld_stream(reinterpret_cast<const int4*>(src) + (v % vpr));
-        const uint4 xv = make_uint4((uint32_t)x.x, (uint32_t)x.y, (uint32_t)x.z, (uint32_t)x.w);
-        const uint2 q = scale == 0.0f ? make_uint2(0, 0) : quant_bf16x8(xv, scale);
-        *reinterpret_cast<uint2*>(tile_codes + (int64_t)v * 8) = q;
-    }
+    cluster_wait_acquire();
 }
 
 // ---------------------------------------------------------------------------
@@ -487,9 +667,11 @@ __device__ __forceinline__ uint32_t dequant_pair(uint16_t two_codes, float scale
     return *reinterpret_cast<const uint32_t*>(&b);
 }
 
-template <int kThreads>
+template <class B, int kThreads>
 __global__ void __launch_bounds__(kThreads)
-dequant_scatter_kernel(const __grid_constant__ Batch p, int64_t num_items) {
+dequant_scatter_kernel(const __grid_constant__ B p, int64_t num_items) {
+    pdl_launch_dependents();
+    pdl_wait();
     for (int64_t item = blockIdx.x; item < num_items; item += gridDim.x) {
         // Decode the item against a bf16 pool, then derive the code run from it.
         Run run;

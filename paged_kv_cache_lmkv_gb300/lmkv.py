@@ -12,6 +12,7 @@ import os
 import threading
 from typing import Sequence
 
+import numpy as np
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -100,11 +101,11 @@ def launch_count() -> int:
     return int(load().lmkv_launch_count())
 
 
-def _i64_array(values):
-    arr = (ctypes.c_int64 * max(len(values), 1))()
-    for i, v in enumerate(values):
-        arr[i] = int(v)
-    return arr
+def _i64_array(values) -> np.ndarray:
+    """Contiguous int64 host array (no copy when it already is one)."""
+    if isinstance(values, np.ndarray) and values.dtype == np.int64 and values.flags.c_contiguous:
+        return values
+    return np.ascontiguousarray(values, dtype=np.int64)
 
 
 def _stream_handle(stream) -> int | None:
@@ -157,7 +158,8 @@ def count_chunks(start, end, chunk_size: int, save_unfull: bool) -> int:
     lib = load()
     s, e = _i64_array(start), _i64_array(end)
     out = ctypes.c_int32(0)
-    rc = lib.lmkv_count_chunks(s, e, len(start), chunk_size, int(save_unfull), ctypes.byref(out))
+    rc = lib.lmkv_count_chunks(s.ctypes.data, e.ctypes.data, len(s), chunk_size, int(save_unfull),
+                               ctypes.byref(out))
     if rc != OK:
         raise LmkvError(rc, "lmkv_count_chunks")
     return out.value
@@ -171,8 +173,8 @@ def enumerate_chunks(start, end, chunk_size: int, save_unfull: bool):
     req = (ctypes.c_int32 * max(n, 1))()
     tok0 = (ctypes.c_int64 * max(n, 1))()
     ntok = (ctypes.c_int32 * max(n, 1))()
-    rc = lib.lmkv_enumerate_chunks(s, e, len(start), chunk_size, int(save_unfull), req, tok0,
-                                   ntok, n)
+    rc = lib.lmkv_enumerate_chunks(s.ctypes.data, e.ctypes.data, len(s), chunk_size,
+                                   int(save_unfull), req, tok0, ntok, n)
     if rc != OK:
         raise LmkvError(rc, "lmkv_enumerate_chunks")
     return [(req[i], tok0[i], ntok[i]) for i in range(n)]
@@ -183,51 +185,55 @@ def _ptr(t):
 
 
 def _common(pool: Pool, block_table: torch.Tensor, start, end):
+    """(pool, table, max_blocks, start, end, num_req) plus the host arrays to keep alive."""
     if block_table.dtype != torch.int32:
         raise ValueError("block_table must be int32")
-    return (pool.struct, _ptr(block_table), block_table.shape[-1], _i64_array(start),
-            _i64_array(end), len(start))
+    s, e = _i64_array(start), _i64_array(end)
+    if s.shape != e.shape:
+        raise ValueError("start and end must have one entry per request")
+    return (pool.struct, block_table.data_ptr(), block_table.shape[-1], s.ctypes.data,
+            e.ctypes.data, len(s)), (s, e)
 
 
 def gather_chunks(pool, block_table, start, end, chunk_size, save_unfull, chunk_ptrs,
                   status=None, stream=None) -> int:
     """lmkv_gather_chunks; returns the status code (0 = launched)."""
-    a = _common(pool, block_table, start, end)
+    a, _keep = _common(pool, block_table, start, end)
     return load().lmkv_gather_chunks(*a, chunk_size, int(save_unfull), _ptr(chunk_ptrs),
                                      _ptr(status), _stream_handle(stream))
 
 
 def scatter_chunks(pool, block_table, start, end, chunk_size, save_unfull, chunk_ptrs,
                    status=None, stream=None) -> int:
-    a = _common(pool, block_table, start, end)
+    a, _keep = _common(pool, block_table, start, end)
     return load().lmkv_scatter_chunks(*a, chunk_size, int(save_unfull), _ptr(chunk_ptrs),
                                       _ptr(status), _stream_handle(stream))
 
 
 def gather_layer(pool, block_table, start, end, chunk_size, save_unfull, chunk_ptrs, layer,
                  status=None, stream=None) -> int:
-    a = _common(pool, block_table, start, end)
+    a, _keep = _common(pool, block_table, start, end)
     return load().lmkv_gather_layer(*a, chunk_size, int(save_unfull), _ptr(chunk_ptrs),
                                     int(layer), _ptr(status), _stream_handle(stream))
 
 
 def scatter_layer(pool, block_table, start, end, chunk_size, save_unfull, chunk_ptrs, layer,
                   status=None, stream=None) -> int:
-    a = _common(pool, block_table, start, end)
+    a, _keep = _common(pool, block_table, start, end)
     return load().lmkv_scatter_layer(*a, chunk_size, int(save_unfull), _ptr(chunk_ptrs),
                                      int(layer), _ptr(status), _stream_handle(stream))
 
 
 def gather_chunks_fp8e4m3(pool, block_table, start, end, chunk_size, save_unfull, code_ptrs,
                           scales, status=None, stream=None) -> int:
-    a = _common(pool, block_table, start, end)
+    a, _keep = _common(pool, block_table, start, end)
     return load().lmkv_gather_chunks_fp8e4m3(*a, chunk_size, int(save_unfull), _ptr(code_ptrs),
                                              _ptr(scales), _ptr(status), _stream_handle(stream))
 
 
 def scatter_chunks_fp8e4m3(pool, block_table, start, end, chunk_size, save_unfull, code_ptrs,
                            scales, status=None, stream=None) -> int:
-    a = _common(pool, block_table, start, end)
+    a, _keep = _common(pool, block_table, start, end)
     return load().lmkv_scatter_chunks_fp8e4m3(*a, chunk_size, int(save_unfull), _ptr(code_ptrs),
                                               _ptr(scales), _ptr(status), _stream_handle(stream))
 
