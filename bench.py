@@ -280,28 +280,28 @@ def bench_device(c: Ctx, args, stream, rank, world, gpu_index):
 
 
 def bench_e2e(c: Ctx, args, stream):
-    """Store + retrieve through host memory with the public API: H2D of the
-    step's block tables, gather, D2H of every chunk into pinned host memory,
-    H2D of the chunks back into device staging buffers, scatter, D2H of the
-    status word.  Timed with events on the stream, copies included."""
+    """Store + retrieve through host memory with the public API.  The chunk
+    buffers live in pinned host memory: the gather kernel writes each chunk
+    straight into it over the GPU-host link, and the scatter kernel reads it
+    back from there (the store / retrieve round trip of KV offloading to CPU
+    memory).  Per step: H2D of the block tables, gather to host, scatter from
+    host, D2H of the status word; timed with events on the stream."""
     w = c.w
     host_bt = torch.from_numpy(c.table).pin_memory()
     host_bt2 = torch.from_numpy(c.table2).pin_memory()
     host_chunks = [torch.empty(b.shape, dtype=b.dtype, pin_memory=True) for b in c.bufs]
+    host_ptrs = pkg.pointer_array(host_chunks, c.dev)
     host_status = torch.zeros(1, dtype=torch.int32, pin_memory=True)
     a = (w.starts, w.ends, w.chunk_size, w.save_unfull)
-    h2d = host_bt.numel() * 4 + host_bt2.numel() * 4 + sum(h.numel() * 2 for h in host_chunks)
-    d2h = sum(h.numel() * 2 for h in host_chunks) + 4
+    chunk_bytes = sum(h.numel() * h.element_size() for h in host_chunks)
+    h2d = host_bt.numel() * 4 + host_bt2.numel() * 4 + chunk_bytes
+    d2h = chunk_bytes + 4
 
     def one():
         c.bt.copy_(host_bt, non_blocking=True)
         c.bt2.copy_(host_bt2, non_blocking=True)
-        pkg.check(pkg.gather_chunks(c.pool, c.bt, *a, c.ptrs, c.status, stream))
-        for d, h in zip(c.bufs, host_chunks):
-            h.copy_(d, non_blocking=True)
-        for d, h in zip(c.lbufs, host_chunks):
-            d.copy_(h, non_blocking=True)
-        pkg.check(pkg.scatter_chunks(c.pool2, c.bt2, *a, c.lptrs, c.status, stream))
+        pkg.check(pkg.gather_chunks(c.pool, c.bt, *a, host_ptrs, c.status, stream))
+        pkg.check(pkg.scatter_chunks(c.pool2, c.bt2, *a, host_ptrs, c.status, stream))
         host_status.copy_(c.status, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -320,8 +320,9 @@ def bench_e2e(c: Ctx, args, stream):
     return {"value": round(bytes_step / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "ms_per_step": round(ms, 4),
-            "what": "store+retrieve via pinned host memory: H2D tables, gather, D2H chunks, "
-                    "H2D chunks, scatter, D2H status; bytes counted as the two kernels'"}
+            "what": "store + retrieve round trip through pinned host memory: H2D block tables, "
+                    "gather kernel writing the chunks into host memory, scatter kernel reading "
+                    "them back, D2H status; bytes counted as the two kernels' (read + write)"}
 
 
 # ---------------------------------------------------------------------------

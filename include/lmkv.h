@@ -153,7 +153,8 @@ int lmkv_scatter_layer(const lmkv_pool_t* pool, const int32_t* block_table, int3
  *   code  = e4m3fn_round_nearest_even_saturating(x / scale)   (IEEE fp32 division)
  *   amax == 0 gives scale 0 and all codes 0.
  * scales[(g*2 + kv)*L + l] = scale.  The LMCache fp8 serde casts every element
- * to float8_e4m3fn at one byte per element (LMCache serde guide, section 7.1);
+ * to float8_e4m3fn at one byte per element ("LMCache 分布式 KV Cache 序列化框架：
+ * Serde 双层接口设计与自定义扩展实战", section 7.1);
  * this variant adds the per-tile scale and fuses the cast into the gather.
  *   code_ptrs : DEVICE array [num_chunks] of DEVICE pointers, chunk g's
  *               codes [2][L][n_g][HD] uint8, 16-byte aligned

@@ -15,7 +15,8 @@ The functions follow:
   the layer-wise pipeline (one layer per call);
 * "LMCache 源码解析" (cache_engine.py walk-through), section "store()"
   (chunk_size, save_unfull_chunk, chunk-aligned prefix);
-* the LMCache serde guide, section 7.1 (fp8 e4m3 cast, one byte per element).
+* "LMCache 分布式 KV Cache 序列化框架：Serde 双层接口设计与自定义扩展实战",
+  section 7.1 (fp8 e4m3 cast, one byte per element).
 
 Parity status: every function here is pinned by the tests in
 ``tests/test_oracle_*.py`` (a per-token dictionary model, closed forms,

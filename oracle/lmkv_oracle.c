@@ -20,7 +20,8 @@
  *    (default 256) chunks, the tail shorter than a chunk is kept only when
  *    save_unfull_chunk is set, and the already-computed prefix given to the
  *    store must be a multiple of chunk_size (else ValueError).
- *  - "LMCache 分布式 serde" guide, section 7.1 (fp8 serde): elements are cast
+ *  - "LMCache 分布式 KV Cache 序列化框架：Serde 双层接口设计与自定义扩展实战",
+ *    section 7.1 (fp8 serde): elements are cast
  *    to float8_e4m3fn, one byte per element.  The scaled form used here (one
  *    fp32 absmax/448 scale per (K/V, layer, chunk), round-to-nearest-even,
  *    saturating) is the workload definition of the fused variant.

@@ -20,7 +20,8 @@ std::atomic<int64_t> g_launches{0};
 // the LSU engine with one CTA per run at the top for the 8B gather).
 constexpr int kLsuThreads = 256;
 constexpr int kLsuUnroll = 8;
-constexpr int kQuantThreads = 512;
+constexpr int kQuantThreads = 256;        // TMA-staged quantiser
+constexpr int kQuantRegThreads = 512;     // register-staged fallback (slices beyond shared memory)
 constexpr int kQuantVPT = 8;
 constexpr int kQuantCluster = 8;
 constexpr int kDequantThreads = 256;
@@ -176,6 +177,26 @@ int launch_pdl(Kernel kernel, int64_t grid, int threads, cudaStream_t stream, Ar
     return err == cudaSuccess ? LMKV_OK : LMKV_ERR_CUDA;
 }
 
+template <class Kernel, class... Args>
+int launch_pdl_smem(Kernel kernel, int64_t grid, int threads, int64_t smem, cudaStream_t stream,
+                    Args... args) {
+    if (grid <= 0) return LMKV_OK;
+    if (grid > INT32_MAX) return LMKV_ERR_INVALID_ARG;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, args...);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return err == cudaSuccess ? LMKV_OK : LMKV_ERR_CUDA;
+}
+
 // Number of CTAs the LSU engine launches for `items` items (one per item).
 int64_t lsu_grid(int64_t items) {
     const int64_t cap = (int64_t)1 << 30;
@@ -192,8 +213,12 @@ int launch_move(const Call& c, cudaStream_t stream) {
 }
 
 // Parts per block: split runs when the call has too few items to fill the GPU.
+// (Measured on the 8B layer-wise calls: splitting 32 KiB runs into 2, 4 or 8
+// parts was 2-120% slower than one CTA per run.)
 int32_t choose_parts(const lmkv_pool_t* pool, int32_t layer_n) {
-    return layer_n == 1 && pool->block_size % 2 == 0 ? 2 : 1;
+    (void)pool;
+    (void)layer_n;
+    return 1;
 }
 
 int move_entry(bool gather, const lmkv_pool_t* pool, const int32_t* block_table,
@@ -228,12 +253,46 @@ int check_fp8_pool(const lmkv_pool_t* pool, int32_t chunk_size) {
     return LMKV_OK;
 }
 
+// Shared-memory bytes the TMA-staged quantiser needs per CTA: one cluster
+// slice of a full chunk.
+int64_t quant_slice_bytes(const Call& c) {
+    const int64_t rows = (c.chunk_size + kQuantCluster - 1) / kQuantCluster;
+    return rows * c.pool->num_kv_heads * c.pool->head_dim * c.pool->elem_bytes;
+}
+
+// Opt a kernel into `bytes` of dynamic shared memory (once per device).
+template <class Kernel>
+bool ensure_smem(Kernel kernel, int64_t bytes, std::atomic<int>* cache) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    if (cache[dev].load(std::memory_order_relaxed) >= bytes) return true;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+        cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    if (kQuantCluster > 8 &&
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    cache[dev].store((int)bytes, std::memory_order_relaxed);
+    return true;
+}
+
+constexpr int64_t kQuantSmemMax = 200 * 1024;
+
 template <class B>
 int launch_quant(const Call& c, float* scales, cudaStream_t stream) {
+    const int64_t smem = quant_slice_bytes(c);
+    auto tma = lmkv::quant_gather_tma_kernel<B, kQuantThreads, kQuantCluster>;
+    static std::atomic<int> smem_cache[64];
+    const bool use_tma = smem <= kQuantSmemMax && ensure_smem(tma, smem, smem_cache);
     return for_each_block<B>(c, scales, [&](const B& b) {
-        const int64_t tiles = (int64_t)b.num_chunks * 2 * b.layer_n;
-        return launch_pdl(lmkv::quant_gather_kernel<B, kQuantThreads, kQuantVPT, kQuantCluster>,
-                          tiles * kQuantCluster, kQuantThreads, stream, b);
+        const int64_t ctas = (int64_t)b.num_chunks * 2 * b.layer_n * kQuantCluster;
+        if (use_tma) return launch_pdl_smem(tma, ctas, kQuantThreads, smem, stream, b);
+        return launch_pdl(lmkv::quant_gather_kernel<B, kQuantRegThreads, kQuantVPT, kQuantCluster>,
+                          ctas, kQuantRegThreads, stream, b);
     });
 }
 

@@ -1,6 +1,7 @@
 // lmkv_kernels.cuh -- sm_103a kernels for the paged-KV chunk gather / scatter.
 //
-// The movement (LMCache paper notes, configurable chunk size section): a
+// The movement ("LMCache: An Efficient KV Cache Layer for Enterprise-Scale
+// LLM Inference", section on the configurable chunk size): a
 // kernel copies the scattered pages of many layers into a contiguous chunk
 // buffer on store and splits chunk buffers back into pages on load.  With
 // chunk_size a multiple of block_size, every (chunk, K/V, layer, block)
@@ -652,6 +653,169 @@ quant_gather_kernel(const __grid_constant__ B p) {
             quant_slice<true, kThreads, kVPT>(regs, valid, nvec, sm, tile_codes, make_quant(scale, true));
         } else {                                  // zero or tiny scale: IEEE division
             quant_slice<false, kThreads, kVPT>(regs, valid, nvec, sm, tile_codes, make_quant(scale, false));
+        }
+    }
+    cluster_wait_acquire();
+}
+
+// TMA-staged form of the quantising gather (the default when a CTA's slice
+// fits in shared memory).  One thread issues a cp.async.bulk copy per page run
+// of the slice into shared memory, completing one mbarrier; the CTA then
+// reads its slice from shared memory twice (absmax, then quantisation), so
+// registers stay few and three 512-thread CTAs fit on an SM.  Rows whose block
+// id is out of range are not copied and are skipped by both passes.
+template <bool kFastDiv, bool kCheckRows, int kThreads>
+__device__ __forceinline__ void quant_smem_slice(const uint8_t* slice, uint32_t nvec, const UDiv& vdiv,
+                                                 const uint32_t* row_ok, uint8_t* tile_codes,
+                                                 const QuantK& k) {
+    for (uint32_t v = threadIdx.x; v < nvec; v += kThreads) {
+        if (kCheckRows) {
+            const uint32_t row = vdiv.div(v);
+            if (!((row_ok[row >> 5] >> (row & 31)) & 1u)) continue;
+        }
+        const uint4 x = *reinterpret_cast<const uint4*>(slice + (size_t)v * 16);
+        *reinterpret_cast<uint2*>(tile_codes + (int64_t)v * 8) = quant_bf16x8<kFastDiv>(x, k);
+    }
+}
+
+template <bool kCheckRows, int kThreads>
+__device__ __forceinline__ uint32_t absmax_smem_slice(const uint8_t* slice, uint32_t nvec,
+                                                      const UDiv& vdiv, const uint32_t* row_ok) {
+    uint32_t acc = 0;
+    for (uint32_t v = threadIdx.x; v < nvec; v += kThreads) {
+        if (kCheckRows) {
+            const uint32_t row = vdiv.div(v);
+            if (!((row_ok[row >> 5] >> (row & 31)) & 1u)) continue;
+        }
+        acc = absmax_bf16x8(acc, *reinterpret_cast<const uint4*>(slice + (size_t)v * 16));
+    }
+    return acc;
+}
+
+template <class B, int kThreads, int kCluster>
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
+quant_gather_tma_kernel(const __grid_constant__ B p) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    extern __shared__ __align__(128) uint8_t slice[];
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ uint32_t warp_max[kThreads / 32];
+    __shared__ uint32_t row_ok[kQuantMaxRows / 32];
+    __shared__ uint32_t any_bad;
+    static_assert(kThreads / 32 <= 32, "one lane per warp slot");
+    pdl_launch_dependents();
+    pdl_wait();
+
+    const uint32_t rank = cluster.block_rank();
+    const uint32_t tile = blockIdx.x / kCluster;
+    const uint32_t ll = tile % (uint32_t)p.layer_n;
+    const uint32_t kv = (tile / (uint32_t)p.layer_n) & 1u;
+    const int gl = (int)(tile / (uint32_t)p.layer_n / 2u);
+    const int l = p.layer_lo + (int)ll;
+    const ChunkRef c = resolve_chunk(p, gl);
+    const uint32_t rows_per = (uint32_t)(c.ntok + kCluster - 1) / kCluster;
+    const uint32_t r0 = rank * rows_per;
+    const uint32_t nrows = (uint32_t)max(0, min(c.ntok, (int)(r0 + rows_per)) - (int)r0);
+    const uint32_t row_bytes = (uint32_t)p.row_bytes;
+    const uint32_t vpr = row_bytes >> 4;
+    const uint32_t nvec = nrows * vpr;
+    const int lane = threadIdx.x & 31;
+
+    uint8_t* codes = p.chunk_ptrs[p.chunk_base + gl];
+    const uint8_t* lb = p.layer_base[l];
+    const bool ptr_ok = codes != nullptr && lb != nullptr &&
+                        ((reinterpret_cast<uintptr_t>(codes) | reinterpret_cast<uintptr_t>(lb)) & 15) == 0;
+    if (threadIdx.x < 32) {
+        // Warp 0: lane i looks up page run i of the slice (rows r0 .. r0+nrows
+        // cut at block boundaries), the warp sums the bytes, lane 0 arms the
+        // mbarrier, then every lane issues its own bulk copy.
+        if (lane == 0) {
+            if (!ptr_ok && rank == 0) report(p, kStatusBadPointer);
+            mbar_init(&bar, 1);
+            fence_barrier_init();
+        }
+        for (int i = lane; i < kQuantMaxRows / 32; i += 32) row_ok[i] = 0;
+        __syncwarp();
+        const uint32_t bs = (uint32_t)p.block_size;
+        const UDiv bdiv(bs);
+        const int32_t* bt = p.block_table + (int64_t)c.req_row * p.bt_stride + c.col0;
+        const uint8_t* kv_base = lb + (int64_t)kv * p.num_blocks * p.block_size * row_bytes;
+        const uint32_t jb0 = nrows ? bdiv.div(r0) : 0u;
+        const uint32_t jb_end = nrows ? bdiv.div(r0 + nrows - 1) + 1 : 0u;
+        uint32_t bytes = 0;
+        bool bad = false;
+        for (uint32_t jb = jb0 + lane; ptr_ok && jb < jb_end; jb += 32) {
+            const uint32_t a = max(r0, jb * bs), e = min(r0 + nrows, (jb + 1) * bs);
+            const int32_t blk = bt[jb];
+            if ((uint32_t)blk < (uint32_t)p.num_blocks) {
+                bytes += (e - a) * row_bytes;
+                for (uint32_t r = a - r0; r < e - r0; ++r) atomicOr(&row_ok[r >> 5], 1u << (r & 31));
+            } else {
+                bad = true;
+            }
+        }
+        const uint32_t total = __reduce_add_sync(0xFFFFFFFFu, bytes);
+        const bool any = __any_sync(0xFFFFFFFFu, bad);
+        if (lane == 0) {
+            any_bad = any ? 1u : 0u;
+            if (any) report(p, kStatusBadBlock);
+            mbar_arrive_expect_tx(&bar, total);
+        }
+        __syncwarp();
+        for (uint32_t jb = jb0 + lane; ptr_ok && jb < jb_end; jb += 32) {
+            const uint32_t a = max(r0, jb * bs), e = min(r0 + nrows, (jb + 1) * bs);
+            const int32_t blk = bt[jb];
+            if ((uint32_t)blk < (uint32_t)p.num_blocks)
+                bulk_g2s(slice + (size_t)(a - r0) * row_bytes,
+                         kv_base + ((int64_t)blk * bs + (a - jb * bs)) * row_bytes, (e - a) * row_bytes, &bar);
+        }
+    }
+    __syncthreads();                                  // barrier initialised, row_ok / any_bad written
+    bool timed_out = false;
+    if (!mbar_wait_bounded(&bar, 0)) {
+        timed_out = true;
+        if (threadIdx.x == 0) report(p, kStatusTimeout);
+        (void)mbar_wait_bounded(&bar, 0);             // let copies in flight land before exit
+    }
+    const bool check_rows = any_bad != 0;
+    const UDiv vdiv(vpr);
+
+    // pass 1: absmax of the slice from shared memory
+    const uint32_t acc = check_rows ? absmax_smem_slice<true, kThreads>(slice, nvec, vdiv, row_ok)
+                                    : absmax_smem_slice<false, kThreads>(slice, nvec, vdiv, row_ok);
+    uint32_t m = max(acc & 0xFFFFu, acc >> 16);
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if (lane == 0) warp_max[threadIdx.x >> 5] = m;
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    uint32_t w = 0;
+    constexpr int kSlots = kCluster * (kThreads / 32);
+    for (int i = lane; i < kSlots; i += 32)
+        w = max(w, *cluster.map_shared_rank(&warp_max[i % (kThreads / 32)], (unsigned)(i / (kThreads / 32))));
+    w = __reduce_max_sync(0xFFFFFFFFu, w);
+    cluster_arrive_relaxed();          // this CTA's shared memory may be released after everyone arrives
+
+    const float amax = __uint_as_float(w << 16);
+    const float scale = __fdiv_rn(amax, 448.0f);
+    if (rank == 0 && threadIdx.x == 0 && p.scales != nullptr)
+        p.scales[((int64_t)(p.chunk_base + gl) * 2 + kv) * p.num_layers + l] = scale;
+    if (ptr_ok && !timed_out) {
+        // pass 2: quantise from shared memory, 8 codes per 16-byte vector
+        uint8_t* tile_codes = codes + (((int64_t)kv * p.num_layers + l) * c.ntok + r0) * (row_bytes >> 1);
+        if (scale == 0.0f) {
+            // all-zero tile: every code is 0
+            for (uint32_t v = threadIdx.x; v < nvec; v += kThreads) {
+                const uint32_t row = vdiv.div(v);
+                if (!check_rows || ((row_ok[row >> 5] >> (row & 31)) & 1u))
+                    *reinterpret_cast<uint2*>(tile_codes + (int64_t)v * 8) = make_uint2(0, 0);
+            }
+        } else if (scale >= kFastDivMinScale) {
+            const QuantK k = make_quant(scale, true);
+            if (check_rows) quant_smem_slice<true, true, kThreads>(slice, nvec, vdiv, row_ok, tile_codes, k);
+            else quant_smem_slice<true, false, kThreads>(slice, nvec, vdiv, row_ok, tile_codes, k);
+        } else {
+            const QuantK k = make_quant(scale, false);
+            quant_smem_slice<false, true, kThreads>(slice, nvec, vdiv, row_ok, tile_codes, k);
         }
     }
     cluster_wait_acquire();

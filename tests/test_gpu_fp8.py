@@ -4,7 +4,8 @@ Codes and scales must equal the oracle's bit for bit: the quantised code is
 an integer decided by fp32 arithmetic, and both sides take that decision in
 fp32 (absmax/448 by IEEE division, x/scale by IEEE division, round to nearest
 even with saturation).  The LMCache fp8 serde casts to float8_e4m3fn at one
-byte per element (serde guide, section 7.1); the per-(K/V, layer, chunk)
+byte per element ("LMCache 分布式 KV Cache 序列化框架：Serde 双层接口设计与自定义扩展实战",
+section 7.1); the per-(K/V, layer, chunk)
 scale is the fused variant's definition.
 """
 import numpy as np
@@ -49,6 +50,7 @@ SMALL = [
     (2, 8, 128, 32, 64, (900,), (0,), 256, True),
     (2, 8, 128, 64, 32, (1100,), (256,), 256, True),
     (1, 1, 32, 8, 600, (2000,), (0,), 1024, True),     # chunk larger than the cluster's registers
+    (1, 8, 128, 16, 256, (2048 + 700,), (0,), 2048, True),  # slice beyond shared memory: register path
 ]
 
 

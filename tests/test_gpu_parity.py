@@ -1,6 +1,7 @@
 """GPU parity of the copy kernels against the CPU oracle (bit-exact).
 
-Movement rule: LMCache paper notes, configurable chunk size section (pages ->
+Movement rule: "LMCache: An Efficient KV Cache Layer for Enterprise-Scale LLM Inference", section on the
+configurable chunk size (pages ->
 contiguous chunk buffers and back) and layer-wise pipeline section (one layer
 per call); chunking rule from the cache_engine.py walk-through, "store()".
 All calls go through the C ABI (liblmkv.so) via the ctypes binding.

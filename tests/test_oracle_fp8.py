@@ -1,8 +1,8 @@
 """Pins for the oracle's number formats and fp8 quantising gather (CPU only).
 
-The fp8 serde of LMCache casts each element to torch.float8_e4m3fn (LMCache
-serde guide, section 7.1).  The fused variant adds one fp32 absmax/448 scale
-per (K/V, layer, chunk).  Pins: the OCP E4M3 table (golden file), torch's own
+The fp8 serde of LMCache casts each element to torch.float8_e4m3fn
+("LMCache 分布式 KV Cache 序列化框架", section 7.1).  The fused variant adds one
+fp32 absmax/448 scale per (K/V, layer, chunk).  Pins: the OCP E4M3 table (golden file), torch's own
 float8_e4m3fn and bfloat16 conversions (independent implementations of the
 same formats), numpy's fp32 division, the unscaled special case that is
 exactly the serde's cast, closed-form error bounds.

@@ -4,7 +4,8 @@ Each test checks the oracle against something other than itself: the
 per-token dictionary model in brute.py, torch's strided copy for the
 identity block table, and invariants that hold for any correct
 implementation (round trip, bijection onto (block, slot), sentinels, layer
-union).  Movement rule: LMCache paper notes, configurable chunk size section
+union).  Movement rule: "LMCache: An Efficient KV Cache Layer for Enterprise-Scale LLM Inference",
+section on the configurable chunk size
 (pages -> contiguous 256-token chunks and back) and layer-wise pipeline
 section (one layer per call).
 """
