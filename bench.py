@@ -201,6 +201,7 @@ def setup(dev, w: wl.Workload) -> Ctx:
     c.scales = torch.empty((len(c.chunks), 2, w.num_layers), dtype=torch.float32, device=dev)
     c.status = torch.zeros(1, dtype=torch.int32, device=dev)
     c.flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize(dev)         # inputs are written on the default stream
     n_tok = sum(n for _, _, n in c.chunks)
     payload = n_tok * 2 * w.num_layers * w.row_bytes          # bf16 bytes of all moved rows
     tiles = len(c.chunks) * 2 * w.num_layers

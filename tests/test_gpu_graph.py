@@ -30,6 +30,7 @@ def test_graph_capture_matches_eager():
     pool_g = device_pool(w, None, fill="sentinel")
     st = new_status()
     s = torch.cuda.Stream()
+    torch.cuda.synchronize()            # buffers were filled on the default stream
 
     def seq(bufs, ptrs, codes_ptrs, scales, target):
         with torch.cuda.stream(s):
