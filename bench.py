@@ -82,6 +82,23 @@ def load_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def max_over_ranks(x: float, world: int) -> float:
+    """Largest value of x over all ranks (the job's time is its slowest rank's)."""
+    if world <= 1:
+        return x
+    dist = torch.distributed
+    dev = (torch.device("cuda", torch.cuda.current_device())
+           if dist.get_backend() == "nccl" else torch.device("cpu"))
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(step_bytes: int, world: int, steps: int, total_ms: float) -> float:
+    """Whole-job GB/s: bytes every rank moved over all steps / the slowest rank's time."""
+    return step_bytes * world * steps / (total_ms * 1e-3) / 1e9
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for p in KERNEL_SOURCES:
@@ -483,13 +500,9 @@ def main():
     per_phase, launches, clk, wall = bench_device(c, args, stream, rank, world, local)
     phase_ms = {n: statistics.mean(v) for n, v in per_phase.items()}
     step_ms = sum(phase_ms.values())
-    total_ms = step_ms * args.steps
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(step_ms * args.steps, world)
     step_bytes = sum(c.phase_bytes.values())
-    value = step_bytes * world * args.steps / (total_ms * 1e-3) / 1e9
+    value = job_value(step_bytes, world, args.steps, total_ms)
     peak, peak_src = load_peaks()
     g_ms = phase_ms["gather"]
     achieved = c.phase_bytes["gather"] / (g_ms * 1e-3) / 1e9

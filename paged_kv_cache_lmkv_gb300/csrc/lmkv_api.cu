@@ -22,10 +22,11 @@ std::atomic<int64_t> g_launches{0};
 // per-layer calls).
 constexpr int kLsuThreads = 256;
 constexpr int kLsuUnroll = 8;
-constexpr int kQuantThreads = 256;        // TMA-staged quantiser
+constexpr int kQuantThreads = 256;        // staged quantiser
 constexpr int kQuantRegThreads = 512;     // register-staged fallback (slices beyond shared memory)
 constexpr int kQuantVPT = 8;
 constexpr int kQuantCluster = 8;
+constexpr int kQuantHybridVPT = 4;        // register vectors per thread of the staged quantiser
 constexpr int kDequantThreads = 256;
 
 // Chunks of one request (cache_engine.py walk-through, "store()").
@@ -254,13 +255,6 @@ int check_fp8_pool(const lmkv_pool_t* pool, int32_t chunk_size) {
     return LMKV_OK;
 }
 
-// Shared-memory bytes the TMA-staged quantiser needs per CTA: one cluster
-// slice of a full chunk.
-int64_t quant_slice_bytes(const Call& c) {
-    const int64_t rows = (c.chunk_size + kQuantCluster - 1) / kQuantCluster;
-    return rows * c.pool->num_kv_heads * c.pool->head_dim * c.pool->elem_bytes;
-}
-
 // Opt a kernel into `bytes` of dynamic shared memory (once per device).
 template <class Kernel>
 bool ensure_smem(Kernel kernel, int64_t bytes, std::atomic<int>* cache) {
@@ -283,15 +277,31 @@ bool ensure_smem(Kernel kernel, int64_t bytes, std::atomic<int>* cache) {
 
 constexpr int64_t kQuantSmemMax = 200 * 1024;
 
+// Shared-memory bytes of the hybrid quantiser: the slice rows beyond those
+// its registers hold.
+int64_t quant_hybrid_smem_bytes(const Call& c) {
+    const int64_t row = (int64_t)c.pool->num_kv_heads * c.pool->head_dim * c.pool->elem_bytes;
+    const int64_t rows = (c.chunk_size + kQuantCluster - 1) / kQuantCluster;
+    const int64_t reg_rows = (int64_t)kQuantThreads * kQuantHybridVPT * 16 / row;
+    return (rows > reg_rows ? rows - reg_rows : 0) * row;
+}
+
 template <class B>
 int launch_quant(const Call& c, float* scales, cudaStream_t stream) {
-    const int64_t smem = quant_slice_bytes(c);
-    auto tma = lmkv::quant_gather_tma_kernel<B, kQuantThreads, kQuantCluster>;
-    static std::atomic<int> smem_cache[64];
-    const bool use_tma = smem <= kQuantSmemMax && ensure_smem(tma, smem, smem_cache);
+    const int64_t hsmem = quant_hybrid_smem_bytes(c);
+    if (hsmem <= kQuantSmemMax) {
+        auto hyb = lmkv::quant_gather_hybrid_kernel<B, kQuantThreads, kQuantHybridVPT, kQuantCluster>;
+        static std::atomic<int> hyb_cache[64];
+        const int64_t bytes = hsmem > 16 ? hsmem : 16;
+        if (!ensure_smem(hyb, bytes, hyb_cache)) return LMKV_ERR_CUDA;
+        return for_each_block<B>(c, scales, [&](const B& b) {
+            const int64_t ctas = (int64_t)b.num_chunks * 2 * b.layer_n * kQuantCluster;
+            return launch_pdl_smem(hyb, ctas, kQuantThreads, bytes, stream, b);
+        });
+    }
+    // rows beyond shared memory: register-staged kernel, re-reading what does not fit
     return for_each_block<B>(c, scales, [&](const B& b) {
         const int64_t ctas = (int64_t)b.num_chunks * 2 * b.layer_n * kQuantCluster;
-        if (use_tma) return launch_pdl_smem(tma, ctas, kQuantThreads, smem, stream, b);
         return launch_pdl(lmkv::quant_gather_kernel<B, kQuantRegThreads, kQuantVPT, kQuantCluster>,
                           ctas, kQuantRegThreads, stream, b);
     });
