@@ -59,6 +59,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-pipeline", action="store_true",
+                    help="skip the layer-wise pipeline measurement (host round trip per layer)")
     ap.add_argument("--case", choices=["llama8b", "profile-small"], default="llama8b",
                     help="profile-small: the 8B shape with a 1024-block pool and a 4096-token "
                          "request (16 chunks), for ncu captures only")
@@ -297,40 +299,70 @@ def bench_device(c: Ctx, args, stream, rank, world, gpu_index):
     return per_phase_ms, launches, clk, wall
 
 
+def pinned_arena(bufs):
+    """Pinned host copies of the chunk buffers' shapes as consecutive slices of
+    one allocation (the staged pipeline moves a run of such full chunks with
+    one 3-D copy per layer)."""
+    flat = torch.empty(sum(b.numel() for b in bufs), dtype=bufs[0].dtype, pin_memory=True)
+    out, off = [], 0
+    for b in bufs:
+        out.append(flat[off:off + b.numel()].view(b.shape))
+        off += b.numel()
+    return out
+
+
 def bench_e2e(c: Ctx, args, stream):
-    """Store + retrieve through host memory with the public API.  The chunk
-    buffers live in pinned host memory: the gather kernel writes each chunk
-    straight into it over the GPU-host link, and the scatter kernel reads it
-    back from there (the store / retrieve round trip of KV offloading to CPU
-    memory).  Per step: H2D of the block tables, gather to host, scatter from
-    host, D2H of the status word; timed with events on the stream."""
+    """Store + retrieve through host memory with the public API, as a serving
+    step does them: the batch's KV is stored to pinned host memory while an
+    earlier stored batch of the same shape is retrieved into the second pool
+    (independent data, so the two run at once on two streams, one per transfer
+    direction).  Both use the staged layer-wise pipeline (kernel <-> one-layer
+    device staging buffer, copy engine <-> host).  Per step: H2D of the block
+    tables, the store and the retrieve of every layer, D2H of the status word;
+    timed with events, copies included."""
     w = c.w
+    L = w.num_layers
+    a = (w.starts, w.ends, w.chunk_size, w.save_unfull)
     host_bt = torch.from_numpy(c.table).pin_memory()
     host_bt2 = torch.from_numpy(c.table2).pin_memory()
-    host_chunks = [torch.empty(b.shape, dtype=b.dtype, pin_memory=True) for b in c.bufs]
-    host_ptrs = pkg.pointer_array(host_chunks, c.dev)
+    stored = pinned_arena(c.bufs)
+    earlier = pinned_arena(c.bufs)
+    nst = pkg.staging_bytes(c.pool, *a)
+    stage_s = torch.empty(nst, dtype=torch.uint8, device=c.dev)
+    stage_r = torch.empty(nst, dtype=torch.uint8, device=c.dev)
     host_status = torch.zeros(1, dtype=torch.int32, pin_memory=True)
-    a = (w.starts, w.ends, w.chunk_size, w.save_unfull)
-    chunk_bytes = sum(h.numel() * h.element_size() for h in host_chunks)
+    other = torch.cuda.Stream(c.dev)
+    fork, join = torch.cuda.Event(), torch.cuda.Event()
+    # the earlier batch: store it once (untimed)
+    pkg.check(pkg.store_layers_staged(c.pool, c.bt, *a, earlier, stage_s, 0, L, None, None,
+                                      c.status, stream))
+    torch.cuda.synchronize(c.dev)
+    chunk_bytes = sum(h.numel() * h.element_size() for h in stored)
     h2d = host_bt.numel() * 4 + host_bt2.numel() * 4 + chunk_bytes
     d2h = chunk_bytes + 4
 
     def one():
-        c.bt.copy_(host_bt, non_blocking=True)
-        c.bt2.copy_(host_bt2, non_blocking=True)
-        pkg.check(pkg.gather_chunks(c.pool, c.bt, *a, host_ptrs, c.status, stream))
-        pkg.check(pkg.scatter_chunks(c.pool2, c.bt2, *a, host_ptrs, c.status, stream))
-        host_status.copy_(c.status, non_blocking=True)
+        with torch.cuda.stream(stream):
+            c.bt.copy_(host_bt, non_blocking=True)
+            c.bt2.copy_(host_bt2, non_blocking=True)
+            fork.record(stream)
+            other.wait_event(fork)
+            pkg.check(pkg.store_layers_staged(c.pool, c.bt, *a, stored, stage_s, 0, L, None, None,
+                                              c.status, stream))
+            pkg.check(pkg.retrieve_layers_staged(c.pool2, c.bt2, *a, earlier, stage_r, 0, L, None,
+                                                 None, c.status, other))
+            join.record(other)
+            stream.wait_event(join)
+            host_status.copy_(c.status, non_blocking=True)
 
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            one()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.e2e_steps):
-            one()
-        e1.record(stream)
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        one()
+    e1.record(stream)
     torch.cuda.synchronize()
     assert int(host_status.item()) == 0
     ms = e0.elapsed_time(e1) / args.e2e_steps
@@ -338,9 +370,106 @@ def bench_e2e(c: Ctx, args, stream):
     return {"value": round(bytes_step / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "ms_per_step": round(ms, 4),
-            "what": "store + retrieve round trip through pinned host memory: H2D block tables, "
-                    "gather kernel writing the chunks into host memory, scatter kernel reading "
-                    "them back, D2H status; bytes counted as the two kernels' (read + write)"}
+            "what": "store of the batch to pinned host memory concurrent with the retrieve of an "
+                    "earlier stored batch, both through the staged layer-wise pipeline (kernel + "
+                    "copy engine), H2D block tables and D2H status included; bytes counted as "
+                    "the gather's and the scatter's (read + write)"}
+
+
+def bench_layer_pipeline(c: Ctx, reps: int = 5):
+    """The layer-wise pipeline with chunk buffers in pinned host memory, in two
+    forms: "direct" (lmkv_store_layers / lmkv_retrieve_layers: the kernels move
+    each layer straight over the GPU-host link) and "staged"
+    (lmkv_*_layers_staged: the kernel moves a layer to / from a one-layer device
+    staging buffer and the copy engine does the host transfer).  Each is timed
+    alone and overlapped with a compute stand-in on another stream (a bf16 GEMM
+    per layer sized to about one layer's transfer, the case where overlap
+    matters most): overlap = (t_move + t_compute - t_both) / min(t_move, t_compute).
+    Also staged store and retrieve of independent batches on two streams at once."""
+    w = c.w
+    L = w.num_layers
+    a = (w.starts, w.ends, w.chunk_size, w.save_unfull)
+    host = pinned_arena(c.bufs)
+    host2 = pinned_arena(c.bufs)
+    hptr = pkg.pointer_array(host, c.dev)
+    nst = pkg.staging_bytes(c.pool, *a)
+    stage = torch.empty(nst, dtype=torch.uint8, device=c.dev)
+    stage2 = torch.empty(nst, dtype=torch.uint8, device=c.dev)
+    compute, copy, copy2 = (torch.cuda.Stream(c.dev) for _ in range(3))
+    ready = [torch.cuda.Event() for _ in range(L)]
+    done = [torch.cuda.Event() for _ in range(L)]
+    for e in ready + done:
+        e.record(copy)
+    torch.cuda.synchronize(c.dev)
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize(c.dev)
+        ts = []
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize(c.dev)
+            ts.append(time.perf_counter() - t0)
+        return statistics.median(ts) * 1e3
+
+    moves = {
+        "direct_store": lambda r=None, d=None: pkg.check(pkg.store_layers(
+            c.pool, c.bt, *a, hptr, 0, L, r, d, c.status, copy)),
+        "direct_retrieve": lambda r=None, d=None: pkg.check(pkg.retrieve_layers(
+            c.pool2, c.bt2, *a, hptr, 0, L, r, d, c.status, copy)),
+        "staged_store": lambda r=None, d=None: pkg.check(pkg.store_layers_staged(
+            c.pool, c.bt, *a, host, stage, 0, L, r, d, c.status, copy)),
+        "staged_retrieve": lambda r=None, d=None: pkg.check(pkg.retrieve_layers_staged(
+            c.pool2, c.bt2, *a, host, stage, 0, L, r, d, c.status, copy)),
+    }
+    t_move = {k: timed(f) for k, f in moves.items()}
+    # compute stand-in: square bf16 GEMM whose duration is about one layer's transfer
+    target = t_move["staged_store"] / L
+    n = 1024
+    while True:
+        x = torch.randn(n, n, device=c.dev, dtype=torch.bfloat16)
+        y = torch.empty_like(x)
+        with torch.cuda.stream(compute):
+            t_one = timed(lambda: torch.matmul(x, x, out=y))
+        if t_one >= target or n >= 16384:
+            break
+        n = (int(n * 1.15) + 255) // 256 * 256
+
+    def compute_layers(signal=None, wait=None):
+        with torch.cuda.stream(compute):
+            for l in range(L):
+                if wait is not None:
+                    compute.wait_event(wait[l])
+                torch.matmul(x, x, out=y)
+                if signal is not None:
+                    signal[l].record(compute)
+
+    t_comp = timed(lambda: compute_layers())
+    out = {"compute_stand_in": f"{L} x bf16 GEMM {n}^3 on a compute stream",
+           "compute_ms": round(t_comp, 3)}
+    payload = c.payload
+    for k, f in moves.items():
+        if k.endswith("store"):
+            both = timed(lambda: (compute_layers(signal=ready), f(r=ready)))
+        else:
+            both = timed(lambda: (f(d=done), compute_layers(wait=done)))
+        out[k] = {"ms": round(t_move[k], 3),
+                  "GBps": round(payload / (t_move[k] * 1e-3) / 1e9, 1),
+                  "with_compute_ms": round(both, 3),
+                  "overlap": round((t_move[k] + t_comp - both) / min(t_move[k], t_comp), 3)}
+
+    def duplex():
+        pkg.check(pkg.store_layers_staged(c.pool, c.bt, *a, host2, stage2, 0, L, None, None,
+                                          c.status, copy2))
+        pkg.check(pkg.retrieve_layers_staged(c.pool2, c.bt2, *a, host, stage, 0, L, None, None,
+                                             c.status, copy))
+    t_dup = timed(duplex)
+    out["staged_store_and_retrieve_concurrent"] = {
+        "ms": round(t_dup, 3), "GBps_both_directions": round(2 * payload / (t_dup * 1e-3) / 1e9, 1)}
+    out["retrieve_from_host_Gbps"] = round(8 * payload / (t_move["staged_retrieve"] * 1e-3) / 1e9)
+    out["bytes"] = "payload bytes crossing the GPU-host link per direction (1,342,177,280)"
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -514,6 +643,7 @@ def main():
     breakdown["gather_layer"]["us_per_call"] = round(phase_ms["gather_layer"] * 1e3 / w.num_layers, 2)
     breakdown["scatter_layer"]["us_per_call"] = round(phase_ms["scatter_layer"] * 1e3 / w.num_layers, 2)
     e2e = bench_e2e(c, args, stream)
+    pipeline = bench_layer_pipeline(c) if not args.no_pipeline else None
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(c)
@@ -533,6 +663,7 @@ def main():
                          "algorithmic_bytes_per_launch": int(c.phase_bytes["gather"])},
             "breakdown": breakdown,
             "e2e": e2e,
+            "layer_pipeline": pipeline,
             "cpu_baseline": cpu,
             "gpu_launches": int(launches),
             "clocks": clk,

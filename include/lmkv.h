@@ -146,6 +146,75 @@ int lmkv_scatter_layer(const lmkv_pool_t* pool, const int32_t* block_table, int3
                        int32_t chunk_size, int32_t save_unfull_chunk,
                        void* const* chunk_ptrs, int32_t layer, int32_t* d_status, void* stream);
 
+/* Layer-wise pipeline (LMCache paper, layer-wise pipeline section: compute and
+ * data movement on separate CUDA streams; while layer i computes, layer i+1's
+ * KV is being moved; connector hooks start_store_kv / wait_store_kv and
+ * start_load_kv / wait_load_kv).
+ *
+ * lmkv_store_layers: for each layer l = layer_lo .. layer_lo+layer_n-1 in order,
+ * make `stream` (the copy stream) wait on layer_ready[l - layer_lo] if that
+ * entry is non-NULL, enqueue lmkv_gather_layer(l), then record
+ * layer_done[l - layer_lo] on `stream` if non-NULL.  lmkv_retrieve_layers does
+ * the same with lmkv_scatter_layer.  A typical store records layer_ready[i] on
+ * the compute stream after layer i's KV is written; a typical retrieve lets the
+ * compute stream wait on layer_done[i] before computing layer i.
+ *   layer_ready, layer_done : HOST arrays of layer_n cudaEvent_t handles (as
+ *                             void*), or NULL; entries may be NULL.  The events
+ *                             must exist (created by the caller).
+ *   chunk_ptrs              : as lmkv_gather_chunks; the buffers may be pinned
+ *                             host memory mapped into the device address space,
+ *                             in which case the kernels are the host transfer.
+ * Nothing is allocated or synchronised.  Errors: as lmkv_gather_layer, checked
+ * for the whole call before anything is enqueued; LMKV_ERR_CUDA if an event
+ * wait or record fails (earlier layers may already be enqueued). */
+int lmkv_store_layers(const lmkv_pool_t* pool, const int32_t* block_table, int32_t max_blocks,
+                      const int64_t* start, const int64_t* end, int32_t num_req,
+                      int32_t chunk_size, int32_t save_unfull_chunk, void* const* chunk_ptrs,
+                      int32_t layer_lo, int32_t layer_n, void* const* layer_ready,
+                      void* const* layer_done, int32_t* d_status, void* stream);
+
+int lmkv_retrieve_layers(const lmkv_pool_t* pool, const int32_t* block_table, int32_t max_blocks,
+                         const int64_t* start, const int64_t* end, int32_t num_req,
+                         int32_t chunk_size, int32_t save_unfull_chunk, void* const* chunk_ptrs,
+                         int32_t layer_lo, int32_t layer_n, void* const* layer_ready,
+                         void* const* layer_done, int32_t* d_status, void* stream);
+
+/* Staged layer-wise pipeline to / from pinned host memory (the same section
+ * of the LMCache paper: a GPU buffer of one layer's KV between the paged pool
+ * and the DMA engine).  Per layer l (in order; layer_ready / layer_done as in
+ * lmkv_store_layers):
+ *   store    : gather layer l into `staging`, then one cudaMemcpy2DAsync per
+ *              chunk moves that chunk's K and V slices of layer l from
+ *              `staging` to host_chunks[g] (device-to-host);
+ *   retrieve : the 2-D copies move the slices from host_chunks[g] into
+ *              `staging` (host-to-device), then layer l is scattered from it.
+ * The copies run on the copy engine, so the transfer uses no SMs while it
+ * overlaps compute on another stream; only the short gather / scatter kernel
+ * needs SMs.
+ *   host_chunks   : HOST array [num_chunks] of pinned HOST pointers, chunk g's
+ *                   buffer [2][L][n_g][HD] (the layout of lmkv_gather_chunks)
+ *   staging       : DEVICE buffer, 16-byte aligned, of staging_bytes >=
+ *                   2 * row_bytes * (tokens enumerated in the batch) -- one
+ *                   layer of the batch; chunk g's slices sit at
+ *                   2 * row_bytes * (tokens of the chunks before g)
+ * Everything is enqueued on `stream`; consecutive layers reuse the staging
+ * buffer in stream order.  Errors: as lmkv_store_layers; INVALID_ARG if the
+ * staging buffer is null or too small or a host pointer is null; MISALIGNED
+ * if staging is not 16-byte aligned. */
+int lmkv_store_layers_staged(const lmkv_pool_t* pool, const int32_t* block_table,
+                             int32_t max_blocks, const int64_t* start, const int64_t* end,
+                             int32_t num_req, int32_t chunk_size, int32_t save_unfull_chunk,
+                             void* const* host_chunks, void* staging, int64_t staging_bytes,
+                             int32_t layer_lo, int32_t layer_n, void* const* layer_ready,
+                             void* const* layer_done, int32_t* d_status, void* stream);
+
+int lmkv_retrieve_layers_staged(const lmkv_pool_t* pool, const int32_t* block_table,
+                                int32_t max_blocks, const int64_t* start, const int64_t* end,
+                                int32_t num_req, int32_t chunk_size, int32_t save_unfull_chunk,
+                                void* const* host_chunks, void* staging, int64_t staging_bytes,
+                                int32_t layer_lo, int32_t layer_n, void* const* layer_ready,
+                                void* const* layer_done, int32_t* d_status, void* stream);
+
 /* Quantising store (bf16 pool only, elem_bytes == 2).  For every tile
  * (chunk g, kv, layer l):
  *   amax  = max |x| over the tile's n_g x HD values

@@ -87,6 +87,7 @@ struct Call {
     int32_t parts;
     int64_t num_chunks;
     int32_t nonempty;
+    void* staging;       // one-layer DEVICE staging buffer (staged pipeline), else null
 };
 
 int validate(Call& c) {
@@ -133,7 +134,10 @@ int for_each_block(const Call& c, float* scales, LaunchFn&& launch) {
     b.chunk_base = 0;
     b.num_chunks = 0;
     b.pad_ = 0;
+    b.staging = static_cast<uint8_t*>(c.staging);
+    b.stage_tok_base = 0;
     b.req_chunk_begin[0] = 0;
+    int64_t tok_in_launch = 0;
     for (int32_t r = 0; r < c.num_req; ++r) {
         const int64_t nch = request_chunks(c.start[r], c.end[r], c.chunk_size, c.save_unfull);
         if (nch == 0) continue;
@@ -141,6 +145,8 @@ int for_each_block(const Call& c, float* scales, LaunchFn&& launch) {
             const int rc = launch(b);
             if (rc != LMKV_OK) return rc;
             b.chunk_base += b.num_chunks;
+            b.stage_tok_base += tok_in_launch;
+            tok_in_launch = 0;
             b.num_chunks = 0;
             b.num_req = 0;
             b.req_chunk_begin[0] = 0;
@@ -152,6 +158,8 @@ int for_each_block(const Call& c, float* scales, LaunchFn&& launch) {
         b.req_col0[i] = (int32_t)(c.start[r] / c.pool->block_size);
         b.req_tok_end[i] = c.save_unfull ? c.end[r]
                                           : c.start[r] + (c.end[r] - c.start[r]) / c.chunk_size * c.chunk_size;
+        b.req_tok_prefix[i] = tok_in_launch;
+        tok_in_launch += b.req_tok_end[i] - b.req_tok0[i];
         b.num_chunks += (int32_t)nch;
         b.req_chunk_begin[i + 1] = b.num_chunks;
     }
@@ -226,11 +234,11 @@ int32_t choose_parts(const lmkv_pool_t* pool, int32_t layer_n) {
 int move_entry(bool gather, const lmkv_pool_t* pool, const int32_t* block_table,
                int32_t max_blocks, const int64_t* start, const int64_t* end, int32_t num_req,
                int32_t chunk_size, int32_t save_unfull, void* const* chunk_ptrs,
-               int32_t layer, int32_t* d_status, void* stream) {
+               int32_t layer, int32_t* d_status, void* stream, void* staging = nullptr) {
     const int rc0 = check_pool(pool);
     if (rc0 != LMKV_OK) return rc0;
     Call c{pool, block_table, max_blocks, start, end, num_req, chunk_size, save_unfull,
-           chunk_ptrs, d_status, 0, pool->num_layers, 1, 0, 0};
+           chunk_ptrs, d_status, 0, pool->num_layers, 1, 0, 0, staging};
     if (layer >= 0) {
         if (layer >= pool->num_layers) return LMKV_ERR_INVALID_ARG;
         c.layer_lo = layer;
@@ -244,6 +252,149 @@ int move_entry(bool gather, const lmkv_pool_t* pool, const int32_t* block_table,
         return gather ? launch_move<lmkv::BatchSmall, true>(c, s)
                       : launch_move<lmkv::BatchSmall, false>(c, s);
     return gather ? launch_move<lmkv::Batch, true>(c, s) : launch_move<lmkv::Batch, false>(c, s);
+}
+
+// Layer-wise pipeline: per layer, wait on its ready event, move it, record its
+// done event, all on one stream.
+int layers_entry(bool gather, const lmkv_pool_t* pool, const int32_t* block_table,
+                 int32_t max_blocks, const int64_t* start, const int64_t* end, int32_t num_req,
+                 int32_t chunk_size, int32_t save_unfull, void* const* chunk_ptrs, int32_t layer_lo,
+                 int32_t layer_n, void* const* ready, void* const* done, int32_t* d_status,
+                 void* stream) {
+    int rc = check_pool(pool);
+    if (rc != LMKV_OK) return rc;
+    if (layer_lo < 0 || layer_n < 0 || (int64_t)layer_lo + layer_n > pool->num_layers)
+        return LMKV_ERR_INVALID_ARG;
+    if (layer_n == 0) return LMKV_OK;
+    // validate the whole call once (same checks as every per-layer call)
+    Call c{pool, block_table, max_blocks, start, end, num_req, chunk_size, save_unfull,
+           chunk_ptrs, d_status, layer_lo, layer_n, 1, 0, 0, nullptr};
+    rc = validate(c);
+    if (rc != LMKV_OK) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    for (int32_t i = 0; i < layer_n; ++i) {
+        if (ready != nullptr && ready[i] != nullptr &&
+            cudaStreamWaitEvent(s, reinterpret_cast<cudaEvent_t>(ready[i]), 0) != cudaSuccess)
+            return LMKV_ERR_CUDA;
+        rc = move_entry(gather, pool, block_table, max_blocks, start, end, num_req, chunk_size,
+                        save_unfull, chunk_ptrs, layer_lo + i, d_status, stream);
+        if (rc != LMKV_OK) return rc;
+        if (done != nullptr && done[i] != nullptr &&
+            cudaEventRecord(reinterpret_cast<cudaEvent_t>(done[i]), s) != cudaSuccess)
+            return LMKV_ERR_CUDA;
+    }
+    return LMKV_OK;
+}
+
+// Staged layer-wise pipeline: per layer, the kernel moves the layer between
+// the pool and a one-layer DEVICE staging buffer, and one 2-D copy per chunk
+// (the copy engine, no SMs) moves the chunk's K and V slices of that layer
+// between the staging buffer and the chunk's pinned host buffer.
+int staged_entry(bool store, const lmkv_pool_t* pool, const int32_t* block_table,
+                 int32_t max_blocks, const int64_t* start, const int64_t* end, int32_t num_req,
+                 int32_t chunk_size, int32_t save_unfull, void* const* host_chunks, void* staging,
+                 int64_t staging_bytes, int32_t layer_lo, int32_t layer_n, void* const* ready,
+                 void* const* done, int32_t* d_status, void* stream) {
+    int rc = check_pool(pool);
+    if (rc != LMKV_OK) return rc;
+    if (layer_lo < 0 || layer_n < 0 || (int64_t)layer_lo + layer_n > pool->num_layers)
+        return LMKV_ERR_INVALID_ARG;
+    if (layer_n == 0) return LMKV_OK;
+    Call c{pool, block_table, max_blocks, start, end, num_req, chunk_size, save_unfull,
+           host_chunks, d_status, layer_lo, layer_n, 1, 0, 0, staging};
+    rc = validate(c);
+    if (rc != LMKV_OK || c.num_chunks == 0) return rc;
+    const int64_t rb = (int64_t)pool->num_kv_heads * pool->head_dim * pool->elem_bytes;
+    int64_t tokens = 0;
+    for (int32_t r = 0; r < num_req; ++r) {
+        const int64_t nch = request_chunks(start[r], end[r], chunk_size, save_unfull);
+        if (nch > 0)
+            tokens += save_unfull ? end[r] - start[r] : (end[r] - start[r]) / chunk_size * chunk_size;
+    }
+    if (staging == nullptr || staging_bytes < 2 * rb * tokens) return LMKV_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(staging) & 15) return LMKV_ERR_MISALIGNED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t L = pool->num_layers;
+    // Per chunk, rows {K, V} of layer l: n_g * rb bytes each; host pitch
+    // L * n_g * rb, staging pitch n_g * rb.  A run of full chunks whose host
+    // buffers are consecutive slices of one allocation (chunk g+1 starts where
+    // chunk g ends) is one 3-D copy (depth = chunks); anything else is one 2-D
+    // copy per chunk.
+    auto copy_run = [&](int32_t l, int64_t g0, int64_t count, int64_t n, int64_t tok_before) -> int {
+        uint8_t* host = static_cast<uint8_t*>(host_chunks[g0]) + (int64_t)l * n * rb;
+        uint8_t* stage = static_cast<uint8_t*>(staging) + 2 * rb * tok_before;
+        cudaError_t e;
+        if (count == 1) {
+            e = store ? cudaMemcpy2DAsync(host, L * n * rb, stage, n * rb, n * rb, 2,
+                                          cudaMemcpyDeviceToHost, s)
+                      : cudaMemcpy2DAsync(stage, n * rb, host, L * n * rb, n * rb, 2,
+                                          cudaMemcpyHostToDevice, s);
+        } else {
+            cudaMemcpy3DParms m = {};
+            const cudaPitchedPtr hp = make_cudaPitchedPtr(host, (size_t)(L * n * rb), (size_t)(n * rb), 2);
+            const cudaPitchedPtr sp = make_cudaPitchedPtr(stage, (size_t)(n * rb), (size_t)(n * rb), 2);
+            m.srcPtr = store ? sp : hp;
+            m.dstPtr = store ? hp : sp;
+            m.extent = make_cudaExtent((size_t)(n * rb), 2, (size_t)count);
+            m.kind = store ? cudaMemcpyDeviceToHost : cudaMemcpyHostToDevice;
+            e = cudaMemcpy3DAsync(&m, s);
+        }
+        return e == cudaSuccess ? LMKV_OK : LMKV_ERR_CUDA;
+    };
+    auto copies = [&](int32_t l) -> int {
+        int64_t g = 0, tok_before = 0;
+        int64_t run_g0 = -1, run_len = 0, run_tok = 0;
+        const int64_t full_bytes = 2 * L * (int64_t)chunk_size * rb;
+        int rc2 = LMKV_OK;
+        for (int32_t r = 0; r < num_req && rc2 == LMKV_OK; ++r) {
+            const int64_t nch = request_chunks(start[r], end[r], chunk_size, save_unfull);
+            for (int64_t j = 0; j < nch && rc2 == LMKV_OK; ++j, ++g) {
+                const int64_t t0 = start[r] + j * chunk_size;
+                const int64_t n = (t0 + chunk_size < end[r] ? t0 + chunk_size : end[r]) - t0;
+                if (host_chunks[g] == nullptr) return LMKV_ERR_INVALID_ARG;
+                const bool extends = run_len > 0 && n == chunk_size &&
+                    static_cast<uint8_t*>(host_chunks[g]) ==
+                        static_cast<uint8_t*>(host_chunks[run_g0]) + run_len * full_bytes;
+                if (extends) {
+                    ++run_len;
+                } else {
+                    if (run_len > 0) rc2 = copy_run(l, run_g0, run_len, chunk_size, run_tok);
+                    if (n == chunk_size) {
+                        run_g0 = g;
+                        run_len = 1;
+                        run_tok = tok_before;
+                    } else {
+                        run_len = 0;
+                        if (rc2 == LMKV_OK) rc2 = copy_run(l, g, 1, n, tok_before);
+                    }
+                }
+                tok_before += n;
+            }
+        }
+        if (rc2 == LMKV_OK && run_len > 0) rc2 = copy_run(l, run_g0, run_len, chunk_size, run_tok);
+        return rc2;
+    };
+    for (int32_t i = 0; i < layer_n; ++i) {
+        const int32_t l = layer_lo + i;
+        if (ready != nullptr && ready[i] != nullptr &&
+            cudaStreamWaitEvent(s, reinterpret_cast<cudaEvent_t>(ready[i]), 0) != cudaSuccess)
+            return LMKV_ERR_CUDA;
+        if (store) {
+            rc = move_entry(true, pool, block_table, max_blocks, start, end, num_req, chunk_size,
+                            save_unfull, host_chunks, l, d_status, stream, staging);
+            if (rc == LMKV_OK) rc = copies(l);
+        } else {
+            rc = copies(l);
+            if (rc == LMKV_OK)
+                rc = move_entry(false, pool, block_table, max_blocks, start, end, num_req,
+                                chunk_size, save_unfull, host_chunks, l, d_status, stream, staging);
+        }
+        if (rc != LMKV_OK) return rc;
+        if (done != nullptr && done[i] != nullptr &&
+            cudaEventRecord(reinterpret_cast<cudaEvent_t>(done[i]), s) != cudaSuccess)
+            return LMKV_ERR_CUDA;
+    }
+    return LMKV_OK;
 }
 
 int check_fp8_pool(const lmkv_pool_t* pool, int32_t chunk_size) {
@@ -323,7 +474,7 @@ int fp8_entry(bool gather, const lmkv_pool_t* pool, const int32_t* block_table, 
     int rc = check_fp8_pool(pool, chunk_size);
     if (rc != LMKV_OK) return rc;
     Call c{pool, block_table, max_blocks, start, end, num_req, chunk_size, save_unfull,
-           code_ptrs, d_status, 0, pool->num_layers, 1, 0, 0};
+           code_ptrs, d_status, 0, pool->num_layers, 1, 0, 0, nullptr};
     rc = validate(c);
     if (rc != LMKV_OK || c.num_chunks == 0) return rc;
     if (scales == nullptr) return LMKV_ERR_INVALID_ARG;
@@ -403,6 +554,48 @@ int lmkv_scatter_layer(const lmkv_pool_t* pool, const int32_t* block_table, int3
     if (layer < 0) return LMKV_ERR_INVALID_ARG;
     return move_entry(false, pool, block_table, max_blocks, start, end, num_req, chunk_size,
                       save_unfull_chunk, chunk_ptrs, layer, d_status, stream);
+}
+
+int lmkv_store_layers(const lmkv_pool_t* pool, const int32_t* block_table, int32_t max_blocks,
+                      const int64_t* start, const int64_t* end, int32_t num_req,
+                      int32_t chunk_size, int32_t save_unfull_chunk, void* const* chunk_ptrs,
+                      int32_t layer_lo, int32_t layer_n, void* const* layer_ready,
+                      void* const* layer_done, int32_t* d_status, void* stream) {
+    return layers_entry(true, pool, block_table, max_blocks, start, end, num_req, chunk_size,
+                        save_unfull_chunk, chunk_ptrs, layer_lo, layer_n, layer_ready, layer_done,
+                        d_status, stream);
+}
+
+int lmkv_retrieve_layers(const lmkv_pool_t* pool, const int32_t* block_table, int32_t max_blocks,
+                         const int64_t* start, const int64_t* end, int32_t num_req,
+                         int32_t chunk_size, int32_t save_unfull_chunk, void* const* chunk_ptrs,
+                         int32_t layer_lo, int32_t layer_n, void* const* layer_ready,
+                         void* const* layer_done, int32_t* d_status, void* stream) {
+    return layers_entry(false, pool, block_table, max_blocks, start, end, num_req, chunk_size,
+                        save_unfull_chunk, chunk_ptrs, layer_lo, layer_n, layer_ready, layer_done,
+                        d_status, stream);
+}
+
+int lmkv_store_layers_staged(const lmkv_pool_t* pool, const int32_t* block_table,
+                             int32_t max_blocks, const int64_t* start, const int64_t* end,
+                             int32_t num_req, int32_t chunk_size, int32_t save_unfull_chunk,
+                             void* const* host_chunks, void* staging, int64_t staging_bytes,
+                             int32_t layer_lo, int32_t layer_n, void* const* layer_ready,
+                             void* const* layer_done, int32_t* d_status, void* stream) {
+    return staged_entry(true, pool, block_table, max_blocks, start, end, num_req, chunk_size,
+                        save_unfull_chunk, host_chunks, staging, staging_bytes, layer_lo, layer_n,
+                        layer_ready, layer_done, d_status, stream);
+}
+
+int lmkv_retrieve_layers_staged(const lmkv_pool_t* pool, const int32_t* block_table,
+                                int32_t max_blocks, const int64_t* start, const int64_t* end,
+                                int32_t num_req, int32_t chunk_size, int32_t save_unfull_chunk,
+                                void* const* host_chunks, void* staging, int64_t staging_bytes,
+                                int32_t layer_lo, int32_t layer_n, void* const* layer_ready,
+                                void* const* layer_done, int32_t* d_status, void* stream) {
+    return staged_entry(false, pool, block_table, max_blocks, start, end, num_req, chunk_size,
+                        save_unfull_chunk, host_chunks, staging, staging_bytes, layer_lo, layer_n,
+                        layer_ready, layer_done, d_status, stream);
 }
 
 int lmkv_gather_chunks_fp8e4m3(const lmkv_pool_t* pool, const int32_t* block_table,

@@ -62,7 +62,10 @@ struct BatchT {
     int32_t chunk_base;                 // global index of this launch's chunk 0
     int32_t num_chunks;                 // chunks in this launch
     int32_t pad_;
+    uint8_t* staging;                   // DEVICE one-layer staging buffer, or null (see item_run)
+    int64_t stage_tok_base;             // enumerated tokens of the call before this launch
     int64_t req_tok0[kCap];             // first enumerated token of packed request i
+    int64_t req_tok_prefix[kCap];       // enumerated tokens of packed requests before i
     int64_t req_tok_end[kCap];          // end (exclusive) of its enumerated tokens
     int32_t req_row[kCap];              // its block-table row
     int32_t req_col0[kCap];             // block-table column of its first token (tok0 / B)
@@ -93,6 +96,7 @@ struct ChunkRef {
     int32_t req_row;
     int32_t ntok;
     int32_t col0;       // block-table column of the chunk's first token
+    int32_t req;        // packed request index in the launch
     int64_t tok0;
 };
 
@@ -105,6 +109,7 @@ __device__ __forceinline__ ChunkRef resolve_chunk(const B& p, int32_t gl) {
         if (p.req_chunk_begin[mid] <= gl) lo = mid; else hi = mid - 1;
     }
     ChunkRef c;
+    c.req = lo;
     c.req_row = p.req_row[lo];
     c.tok0 = p.req_tok0[lo] + (int64_t)(gl - p.req_chunk_begin[lo]) * p.chunk_size;
     c.col0 = p.req_col0[lo] + (gl - p.req_chunk_begin[lo]) * p.blocks_per_chunk;
@@ -146,15 +151,30 @@ __device__ __forceinline__ bool item_run(const B& p, int64_t item, Run& run) {
     const int64_t blk = p.block_table[(int64_t)c.req_row * p.bt_stride + col];
     if (blk < 0 || blk >= p.num_blocks) { report(p, kStatusBadBlock); return false; }
     uint8_t* lb = const_cast<uint8_t*>(p.layer_base[l]);
-    uint8_t* cb = p.chunk_ptrs[p.chunk_base + gl];
+    const int64_t rb = p.row_bytes;
+    // Chunk side: chunk g's buffer [2][L][n_g][row], or -- in staging mode --
+    // the one-layer staging buffer, where chunk g's [2][n_g][row] slices sit
+    // at 2 * row * (tokens enumerated before chunk g).
+    uint8_t* cb;
+    int64_t chunk_layers, layer_slot;
+    if (p.staging != nullptr) {
+        const int64_t tok_before = p.stage_tok_base + p.req_tok_prefix[c.req] +
+                                   (int64_t)(gl - p.req_chunk_begin[c.req]) * p.chunk_size;
+        cb = p.staging + 2 * rb * tok_before;
+        chunk_layers = 1;
+        layer_slot = 0;
+    } else {
+        cb = p.chunk_ptrs[p.chunk_base + gl];
+        chunk_layers = p.num_layers;
+        layer_slot = l;
+    }
     if (lb == nullptr || cb == nullptr || ((reinterpret_cast<uintptr_t>(lb) |
                                             reinterpret_cast<uintptr_t>(cb)) & 15)) {
         report(p, kStatusBadPointer);
         return false;
     }
-    const int64_t rb = p.row_bytes;
     run.pool = lb + ((kv * p.num_blocks + blk) * p.block_size + q * part_rows) * rb;
-    run.chunk = cb + (((int64_t)kv * p.num_layers + l) * c.ntok + row0) * rb;
+    run.chunk = cb + (((int64_t)kv * chunk_layers + layer_slot) * c.ntok + row0) * rb;
     run.bytes = (uint32_t)(rows * rb);
     return true;
 }

@@ -31,7 +31,8 @@ ENTRY_POINTS = (
     "lmkv_count_chunks", "lmkv_enumerate_chunks", "lmkv_gather_chunks", "lmkv_scatter_chunks",
     "lmkv_gather_layer", "lmkv_scatter_layer", "lmkv_gather_chunks_fp8e4m3",
     "lmkv_scatter_chunks_fp8e4m3", "lmkv_status_string", "lmkv_abi_version",
-    "lmkv_launch_count",
+    "lmkv_launch_count", "lmkv_store_layers", "lmkv_retrieve_layers",
+    "lmkv_store_layers_staged", "lmkv_retrieve_layers_staged",
 )
 
 
@@ -77,13 +78,20 @@ def load() -> ctypes.CDLL:
         layer = [pool_p, P, i32, P, P, i32, i32, i32, P, i32, P, P]
         lib.lmkv_gather_layer.argtypes = layer
         lib.lmkv_scatter_layer.argtypes = layer
+        layers = [pool_p, P, i32, P, P, i32, i32, i32, P, i32, i32, P, P, P, P]
+        lib.lmkv_store_layers.argtypes = layers
+        lib.lmkv_retrieve_layers.argtypes = layers
+        staged = [pool_p, P, i32, P, P, i32, i32, i32, P, P, i64, i32, i32, P, P, P, P]
+        lib.lmkv_store_layers_staged.argtypes = staged
+        lib.lmkv_retrieve_layers_staged.argtypes = staged
         fp8 = [pool_p, P, i32, P, P, i32, i32, i32, P, P, P, P]
         lib.lmkv_gather_chunks_fp8e4m3.argtypes = fp8
         lib.lmkv_scatter_chunks_fp8e4m3.argtypes = fp8
         for name in ("lmkv_count_chunks", "lmkv_enumerate_chunks", "lmkv_gather_chunks",
                      "lmkv_scatter_chunks", "lmkv_gather_layer", "lmkv_scatter_layer",
                      "lmkv_gather_chunks_fp8e4m3", "lmkv_scatter_chunks_fp8e4m3",
-                     "lmkv_abi_version"):
+                     "lmkv_abi_version", "lmkv_store_layers", "lmkv_retrieve_layers",
+                     "lmkv_store_layers_staged", "lmkv_retrieve_layers_staged"):
             getattr(lib, name).restype = ctypes.c_int
         lib.lmkv_status_string.argtypes = [ctypes.c_int]
         lib.lmkv_status_string.restype = ctypes.c_char_p
@@ -236,6 +244,81 @@ def scatter_chunks_fp8e4m3(pool, block_table, start, end, chunk_size, save_unful
     a, _keep = _common(pool, block_table, start, end)
     return load().lmkv_scatter_chunks_fp8e4m3(*a, chunk_size, int(save_unfull), _ptr(code_ptrs),
                                               _ptr(scales), _ptr(status), _stream_handle(stream))
+
+
+def _event_array(events, n):
+    """HOST array of n cudaEvent_t handles (0 = none) from torch.cuda.Event objects."""
+    if events is None:
+        return None
+    if len(events) != n:
+        raise ValueError("one event (or None) per layer")
+    arr = (ctypes.c_void_p * max(n, 1))()
+    for i, e in enumerate(events):
+        if e is None:
+            continue
+        handle = e.cuda_event if isinstance(e, torch.cuda.Event) else int(e)
+        if not handle:
+            raise ValueError("event has no CUDA event yet: record it once first")
+        arr[i] = handle
+    return arr
+
+
+def store_layers(pool, block_table, start, end, chunk_size, save_unfull, chunk_ptrs, layer_lo,
+                 layer_n, layer_ready=None, layer_done=None, status=None, stream=None) -> int:
+    """lmkv_store_layers: per layer, wait on layer_ready[i], gather, record layer_done[i]."""
+    a, _keep = _common(pool, block_table, start, end)
+    r, d = _event_array(layer_ready, layer_n), _event_array(layer_done, layer_n)
+    return load().lmkv_store_layers(*a, chunk_size, int(save_unfull), _ptr(chunk_ptrs), int(layer_lo),
+                                    int(layer_n), r, d, _ptr(status), _stream_handle(stream))
+
+
+def retrieve_layers(pool, block_table, start, end, chunk_size, save_unfull, chunk_ptrs, layer_lo,
+                    layer_n, layer_ready=None, layer_done=None, status=None, stream=None) -> int:
+    """lmkv_retrieve_layers: per layer, wait on layer_ready[i], scatter, record layer_done[i]."""
+    a, _keep = _common(pool, block_table, start, end)
+    r, d = _event_array(layer_ready, layer_n), _event_array(layer_done, layer_n)
+    return load().lmkv_retrieve_layers(*a, chunk_size, int(save_unfull), _ptr(chunk_ptrs),
+                                       int(layer_lo), int(layer_n), r, d, _ptr(status),
+                                       _stream_handle(stream))
+
+
+def _host_ptr_array(tensors):
+    """HOST array of the (pinned host) tensors' data pointers."""
+    arr = (ctypes.c_void_p * max(len(tensors), 1))()
+    for i, t in enumerate(tensors):
+        arr[i] = t.data_ptr()
+    return arr
+
+
+def staging_bytes(pool, start, end, chunk_size, save_unfull) -> int:
+    """Bytes of the one-layer staging buffer the staged pipeline needs."""
+    n = sum(ntok for _, _, ntok in enumerate_chunks(start, end, chunk_size, save_unfull))
+    return 2 * pool.num_kv_heads * pool.head_dim * pool.elem_bytes * n
+
+
+def store_layers_staged(pool, block_table, start, end, chunk_size, save_unfull, host_chunks,
+                        staging, layer_lo, layer_n, layer_ready=None, layer_done=None,
+                        status=None, stream=None) -> int:
+    """lmkv_store_layers_staged; host_chunks: pinned host tensors, staging: device tensor."""
+    a, _keep = _common(pool, block_table, start, end)
+    h = _host_ptr_array(host_chunks)
+    r, d = _event_array(layer_ready, layer_n), _event_array(layer_done, layer_n)
+    return load().lmkv_store_layers_staged(*a, chunk_size, int(save_unfull), h, _ptr(staging),
+                                           staging.numel() * staging.element_size(), int(layer_lo),
+                                           int(layer_n), r, d, _ptr(status), _stream_handle(stream))
+
+
+def retrieve_layers_staged(pool, block_table, start, end, chunk_size, save_unfull, host_chunks,
+                           staging, layer_lo, layer_n, layer_ready=None, layer_done=None,
+                           status=None, stream=None) -> int:
+    """lmkv_retrieve_layers_staged (host -> staging by 2-D copies, then scatter)."""
+    a, _keep = _common(pool, block_table, start, end)
+    h = _host_ptr_array(host_chunks)
+    r, d = _event_array(layer_ready, layer_n), _event_array(layer_done, layer_n)
+    return load().lmkv_retrieve_layers_staged(*a, chunk_size, int(save_unfull), h, _ptr(staging),
+                                              staging.numel() * staging.element_size(),
+                                              int(layer_lo), int(layer_n), r, d, _ptr(status),
+                                              _stream_handle(stream))
 
 
 def check(rc: int, what: str = "lmkv") -> None:

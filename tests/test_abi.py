@@ -112,3 +112,33 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(lmkv, "LIB_PATH", str(tmp_path / "nope.so"))
     with pytest.raises(RuntimeError, match="no fallback"):
         lmkv.load()
+
+
+def test_layer_pipeline_host_validation(lib):
+    pool = fake_pool(num_layers=4)
+    bt = FakeTensor(shape=(1, 64))
+    for fn in (lmkv.store_layers, lmkv.retrieve_layers):
+        ptrs = FakeTensor(0x30000)
+        assert fn(pool, bt, [0], [512], 256, True, ptrs, 2, 3, None, None, None, 0) == lmkv.ERR_INVALID_ARG
+        assert fn(pool, bt, [0], [512], 256, True, ptrs, -1, 1, None, None, None, 0) == lmkv.ERR_INVALID_ARG
+        assert fn(pool, bt, [17], [512], 256, True, ptrs, 0, 4, None, None, None, 0) == lmkv.ERR_INVALID_ARG
+        before = lmkv.launch_count()
+        assert fn(pool, bt, [0], [512], 256, True, ptrs, 1, 0, None, None, None, 0) == lmkv.OK
+        assert lmkv.launch_count() == before
+
+
+def test_staged_pipeline_host_validation(lib):
+    import ctypes as C
+    pool = fake_pool(num_layers=4)
+    bt = FakeTensor(shape=(1, 64))
+    need = 2 * 2 * 64 * 2 * 512          # 2 * row_bytes * tokens
+    for fn in (lib.lmkv_store_layers_staged, lib.lmkv_retrieve_layers_staged):
+        s, e = (C.c_int64 * 1)(0), (C.c_int64 * 1)(512)
+        h = (C.c_void_p * 2)(0x50000, 0x60000)
+        args = lambda stage, nbytes, lo=0, n=4: fn(pool.struct, 0x10000, 64, s, e, 1, 256, 1, h,
+                                                   stage, nbytes, lo, n, None, None, None, 0)
+        assert args(0x70000, need - 16) == lmkv.ERR_INVALID_ARG        # staging too small
+        assert args(None, need) == lmkv.ERR_INVALID_ARG                # no staging
+        assert args(0x70008, need) == lmkv.ERR_MISALIGNED              # misaligned staging
+        assert args(0x70000, need, 3, 2) == lmkv.ERR_INVALID_ARG       # layers out of range
+        assert args(0x70000, need, 1, 0) == lmkv.OK                    # nothing to do
