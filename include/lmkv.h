@@ -72,7 +72,8 @@ typedef enum lmkv_status {
     LMKV_ERR_UNSUPPORTED = 4,   /* host: e.g. the fp8 variant on a pool that is not bf16 */
     LMKV_ERR_BAD_BLOCK = 5,     /* device: a block id outside [0, num_blocks); token skipped */
     LMKV_ERR_BAD_POINTER = 6,   /* device: null or misaligned entry in a pointer array; skipped */
-    LMKV_ERR_TIMEOUT = 7        /* device: a bounded wait on an asynchronous copy gave up */
+    LMKV_ERR_TIMEOUT = 7,       /* device: a bounded wait on an asynchronous copy gave up */
+    LMKV_ERR_SCRATCH_LIMIT = 8  /* host: the batch needs more than the library's built-in scratch */
 } lmkv_status;
 
 /* The paged KV pool.  layer_base is a DEVICE array of num_layers DEVICE
@@ -214,6 +215,42 @@ int lmkv_retrieve_layers_staged(const lmkv_pool_t* pool, const int32_t* block_ta
                                 void* const* host_chunks, void* staging, int64_t staging_bytes,
                                 int32_t layer_lo, int32_t layer_n, void* const* layer_ready,
                                 void* const* layer_done, int32_t* d_status, void* stream);
+
+/* Size of the built-in staging area of lmkv_store_layers_staged_noalloc. */
+#define LMKV_NOALLOC_STAGING_BYTES (64u << 20)
+
+/* lmkv_store_layers_staged without a caller-provided staging buffer, for
+ * callers that cannot allocate device memory: code running where a device
+ * allocation is not allowed or not possible (inside a memory-pool or
+ * arena-managed runtime that forbids other allocations, under a strict device
+ * memory budget, or in a host callback path that must not call cudaMalloc).
+ * The paper has no counterpart; this is a convenience of this library.
+ *
+ * The staging area is a fixed device array of LMKV_NOALLOC_STAGING_BYTES
+ * (64 MiB) inside the library: every GPU that loads the library holds it until
+ * the process exits.  The first call on a device looks up that array's device
+ * address for the device that is current at the time (a one-time set-up per
+ * device), so make that first call before any stream capture.  All other
+ * arguments, the layout of the host chunks and the per-layer behaviour are
+ * those of lmkv_store_layers_staged.  The call allocates and frees nothing.
+ *
+ * Every call on a device uses the same staging area, and it keeps whatever
+ * the last call left there; nothing in it needs to start at zero (each layer's
+ * rows are written by the gather before the copies read them).  Calls whose
+ * work overlaps on the GPU (on different streams, or on different host
+ * threads without ordering) race on the staging area: order them on one
+ * stream or with events.
+ *
+ * Errors: LMKV_ERR_SCRATCH_LIMIT if 2 * row_bytes * (tokens enumerated in the
+ * batch) exceeds LMKV_NOALLOC_STAGING_BYTES (nothing is enqueued: split the
+ * batch); LMKV_ERR_CUDA if the set-up fails; otherwise as
+ * lmkv_store_layers_staged. */
+int lmkv_store_layers_staged_noalloc(const lmkv_pool_t* pool, const int32_t* block_table,
+                                     int32_t max_blocks, const int64_t* start, const int64_t* end,
+                                     int32_t num_req, int32_t chunk_size, int32_t save_unfull_chunk,
+                                     void* const* host_chunks, int32_t layer_lo, int32_t layer_n,
+                                     void* const* layer_ready, void* const* layer_done,
+                                     int32_t* d_status, void* stream);
 
 /* Quantising store (bf16 pool only, elem_bytes == 2).  For every tile
  * (chunk g, kv, layer l):

@@ -10,6 +10,7 @@
 #include "lmkv_kernels.cuh"
 
 #include <atomic>
+#include <mutex>
 
 namespace {
 
@@ -487,6 +488,34 @@ int fp8_entry(bool gather, const lmkv_pool_t* pool, const int32_t* block_table, 
 
 }  // namespace
 
+// Built-in staging area of lmkv_store_layers_staged_noalloc.  In host code the
+// name only stands for the device array: the kernels get its device address,
+// looked up once per device with that device current.
+static __device__ __align__(256) uint8_t g_noalloc_staging[LMKV_NOALLOC_STAGING_BYTES];
+
+namespace {
+
+std::mutex g_noalloc_mutex;
+void* g_noalloc_address[64] = {};
+
+// Device address of g_noalloc_staging on the current device (null on error).
+void* noalloc_staging_address() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_address[dev] == nullptr) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_staging) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return nullptr;
+        }
+        g_noalloc_address[dev] = ptr;
+    }
+    return g_noalloc_address[dev];
+}
+
+}  // namespace
+
 extern "C" {
 
 int lmkv_count_chunks(const int64_t* start, const int64_t* end, int32_t num_req,
@@ -626,8 +655,36 @@ const char* lmkv_status_string(int status) {
         case LMKV_ERR_BAD_BLOCK: return "block id out of range (token skipped)";
         case LMKV_ERR_BAD_POINTER: return "null or misaligned device pointer in an array (skipped)";
         case LMKV_ERR_TIMEOUT: return "bounded device wait gave up";
+        case LMKV_ERR_SCRATCH_LIMIT: return "batch needs more than the built-in staging area";
         default: return "unknown status";
     }
+}
+
+// lmkv_store_layers_staged_noalloc: the staged store with the library's own
+// staging area, for callers that must not allocate device memory.
+int lmkv_store_layers_staged_noalloc(const lmkv_pool_t* pool, const int32_t* block_table,
+                                     int32_t max_blocks, const int64_t* start, const int64_t* end,
+                                     int32_t num_req, int32_t chunk_size, int32_t save_unfull_chunk,
+                                     void* const* host_chunks, int32_t layer_lo, int32_t layer_n,
+                                     void* const* layer_ready, void* const* layer_done,
+                                     int32_t* d_status, void* stream) {
+    const int rc = check_pool(pool);
+    if (rc != LMKV_OK) return rc;
+    int64_t chunks = 0;
+    if (check_requests(start, end, num_req, chunk_size, save_unfull_chunk, &chunks, nullptr) != LMKV_OK)
+        return LMKV_ERR_INVALID_ARG;
+    int64_t tokens = 0;
+    for (int32_t r = 0; r < num_req; ++r)
+        if (request_chunks(start[r], end[r], chunk_size, save_unfull_chunk) > 0)
+            tokens += save_unfull_chunk ? end[r] - start[r]
+                                        : (end[r] - start[r]) / chunk_size * chunk_size;
+    const int64_t row = (int64_t)pool->num_kv_heads * pool->head_dim * pool->elem_bytes;
+    if (2 * row * tokens > (int64_t)LMKV_NOALLOC_STAGING_BYTES) return LMKV_ERR_SCRATCH_LIMIT;
+    void* staging = noalloc_staging_address();
+    if (staging == nullptr) return LMKV_ERR_CUDA;
+    return staged_entry(true, pool, block_table, max_blocks, start, end, num_req, chunk_size,
+                        save_unfull_chunk, host_chunks, staging, (int64_t)LMKV_NOALLOC_STAGING_BYTES,
+                        layer_lo, layer_n, layer_ready, layer_done, d_status, stream);
 }
 
 int lmkv_abi_version(void) { return LMKV_ABI_VERSION; }

@@ -26,6 +26,8 @@ ERR_UNSUPPORTED = 4
 ERR_BAD_BLOCK = 5
 ERR_BAD_POINTER = 6
 ERR_TIMEOUT = 7
+ERR_SCRATCH_LIMIT = 8
+NOALLOC_STAGING_BYTES = 64 << 20
 
 ENTRY_POINTS = (
     "lmkv_count_chunks", "lmkv_enumerate_chunks", "lmkv_gather_chunks", "lmkv_scatter_chunks",
@@ -33,6 +35,7 @@ ENTRY_POINTS = (
     "lmkv_scatter_chunks_fp8e4m3", "lmkv_status_string", "lmkv_abi_version",
     "lmkv_launch_count", "lmkv_store_layers", "lmkv_retrieve_layers",
     "lmkv_store_layers_staged", "lmkv_retrieve_layers_staged",
+    "lmkv_store_layers_staged_noalloc",
 )
 
 
@@ -84,6 +87,8 @@ def load() -> ctypes.CDLL:
         staged = [pool_p, P, i32, P, P, i32, i32, i32, P, P, i64, i32, i32, P, P, P, P]
         lib.lmkv_store_layers_staged.argtypes = staged
         lib.lmkv_retrieve_layers_staged.argtypes = staged
+        lib.lmkv_store_layers_staged_noalloc.argtypes = [pool_p, P, i32, P, P, i32, i32, i32, P,
+                                                         i32, i32, P, P, P, P]
         fp8 = [pool_p, P, i32, P, P, i32, i32, i32, P, P, P, P]
         lib.lmkv_gather_chunks_fp8e4m3.argtypes = fp8
         lib.lmkv_scatter_chunks_fp8e4m3.argtypes = fp8
@@ -91,7 +96,8 @@ def load() -> ctypes.CDLL:
                      "lmkv_scatter_chunks", "lmkv_gather_layer", "lmkv_scatter_layer",
                      "lmkv_gather_chunks_fp8e4m3", "lmkv_scatter_chunks_fp8e4m3",
                      "lmkv_abi_version", "lmkv_store_layers", "lmkv_retrieve_layers",
-                     "lmkv_store_layers_staged", "lmkv_retrieve_layers_staged"):
+                     "lmkv_store_layers_staged", "lmkv_retrieve_layers_staged",
+                     "lmkv_store_layers_staged_noalloc"):
             getattr(lib, name).restype = ctypes.c_int
         lib.lmkv_status_string.argtypes = [ctypes.c_int]
         lib.lmkv_status_string.restype = ctypes.c_char_p
@@ -319,6 +325,21 @@ def retrieve_layers_staged(pool, block_table, start, end, chunk_size, save_unful
                                               staging.numel() * staging.element_size(),
                                               int(layer_lo), int(layer_n), r, d, _ptr(status),
                                               _stream_handle(stream))
+
+
+def store_layers_staged_noalloc(pool, block_table, start, end, chunk_size, save_unfull,
+                                host_chunks, layer_lo, layer_n, layer_ready=None, layer_done=None,
+                                status=None, stream=None) -> int:
+    """lmkv_store_layers_staged_noalloc: the staged store using the library's
+    built-in 64 MiB device staging area instead of a caller buffer, for callers
+    that cannot allocate device memory.  Make the first call on a device before
+    any stream capture; calls that overlap on the GPU share the staging area."""
+    a, _keep = _common(pool, block_table, start, end)
+    h = _host_ptr_array(host_chunks)
+    r, d = _event_array(layer_ready, layer_n), _event_array(layer_done, layer_n)
+    return load().lmkv_store_layers_staged_noalloc(*a, chunk_size, int(save_unfull), h,
+                                                   int(layer_lo), int(layer_n), r, d,
+                                                   _ptr(status), _stream_handle(stream))
 
 
 def check(rc: int, what: str = "lmkv") -> None:
