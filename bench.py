@@ -472,6 +472,44 @@ def bench_layer_pipeline(c: Ctx, reps: int = 5):
     return out
 
 
+def bench_decode_store(c: Ctx, reps: int = 50):
+    """Deferred decode-KV store, the small-batch latency case: per decode step
+    the requests that just completed a chunk store it (decode_store_ranges +
+    gather_chunks, save_unfull_chunk = 0).  Event-timed per call for 1 and 8
+    completed chunks (8B shape, all 32 layers), on the bench stream."""
+    w = c.w
+    C = w.chunk_size
+    out = {}
+    stream = torch.cuda.Stream(c.dev)
+    for k in (1, 8):
+        # k requests sharing the 8B pool, each with one chunk completed this step
+        stored = np.arange(k, dtype=np.int64) * 0 + C * 4
+        cur = stored + C + 3
+        s, e, n = pkg.decode_store_ranges(stored, cur, C)
+        table = np.stack([c.table[0]] * k).astype(np.int32)
+        bt = torch.from_numpy(table).to(c.dev)
+        bufs = [torch.empty((2, w.num_layers, C, w.row_elems), dtype=torch.bfloat16, device=c.dev)
+                for _ in range(n)]
+        ptrs = pkg.pointer_array(bufs, c.dev)
+        torch.cuda.synchronize(c.dev)
+        with torch.cuda.stream(stream):
+            for _ in range(5):
+                pkg.check(pkg.gather_chunks(c.pool, bt, s, e, C, False, ptrs, c.status, stream))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                pkg.check(pkg.gather_chunks(c.pool, bt, s, e, C, False, ptrs, c.status, stream))
+            e1.record(stream)
+        torch.cuda.synchronize(c.dev)
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        byt = 2 * n * C * 2 * w.num_layers * w.row_bytes
+        out[f"{k}_chunk_us"] = round(us, 2)
+        out[f"{k}_chunk_GBps"] = round(byt / (us * 1e-6) / 1e9, 1)
+    out["what"] = ("store of the chunks completed in one decode step (all 32 layers), "
+                   "back-to-back calls on one stream; L2 not flushed (small working set)")
+    return out
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle (baseline leg and --impl reference).
 
@@ -644,6 +682,7 @@ def main():
     breakdown["scatter_layer"]["us_per_call"] = round(phase_ms["scatter_layer"] * 1e3 / w.num_layers, 2)
     e2e = bench_e2e(c, args, stream)
     pipeline = bench_layer_pipeline(c) if not args.no_pipeline else None
+    decode = bench_decode_store(c) if not args.no_pipeline else None
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(c)
@@ -664,6 +703,7 @@ def main():
             "breakdown": breakdown,
             "e2e": e2e,
             "layer_pipeline": pipeline,
+            "decode_store": decode,
             "cpu_baseline": cpu,
             "gpu_launches": int(launches),
             "clocks": clk,

@@ -104,6 +104,22 @@ int lmkv_enumerate_chunks(const int64_t* start, const int64_t* end, int32_t num_
                           int32_t* out_req, int64_t* out_tok0, int32_t* out_ntok,
                           int32_t capacity);
 
+/* Deferred decode-KV store (LMCache paper, section on delayed storing of
+ * decode KV: instead of writing every generated token's KV, buffer it and
+ * store in batch once a whole chunk has been generated).  The decode KV stays
+ * in the paged pool; this host-only helper turns each request's stored prefix
+ * and current length into the range of chunks completed since the last store:
+ *   out_start[r] = stored_end[r]
+ *   out_end[r]   = stored_end[r] + floor((cur_end[r] - stored_end[r]) / C) * C
+ * and *out_num_chunks = the number of those chunks.  Passing out_start /
+ * out_end with save_unfull_chunk = 0 to lmkv_gather_chunks (or a staged
+ * store) stores exactly them; the caller then sets stored_end = out_end.
+ * INVALID_ARG if a stored_end is not a multiple of chunk_size, is negative, or
+ * exceeds cur_end.  All arrays are HOST, num_req entries. */
+int lmkv_decode_store_ranges(const int64_t* stored_end, const int64_t* cur_end, int32_t num_req,
+                             int32_t chunk_size, int64_t* out_start, int64_t* out_end,
+                             int32_t* out_num_chunks);
+
 /* Store path: X_g[kv][l][t][:] = P_l[kv][BT[r][tok/B]][tok % B][:] for every
  * chunk g (request r, tok = first token of g + t), kv, layer l, t < n_g.
  * Configurable chunk size section of the LMCache paper (pages -> contiguous

@@ -551,6 +551,29 @@ int lmkv_enumerate_chunks(const int64_t* start, const int64_t* end, int32_t num_
     return LMKV_OK;
 }
 
+int lmkv_decode_store_ranges(const int64_t* stored_end, const int64_t* cur_end, int32_t num_req,
+                             int32_t chunk_size, int64_t* out_start, int64_t* out_end,
+                             int32_t* out_num_chunks) {
+    if (num_req < 0 || chunk_size <= 0 || out_num_chunks == nullptr) return LMKV_ERR_INVALID_ARG;
+    if (num_req > 0 && (stored_end == nullptr || cur_end == nullptr || out_start == nullptr ||
+                        out_end == nullptr))
+        return LMKV_ERR_INVALID_ARG;
+    int64_t n = 0;
+    for (int32_t r = 0; r < num_req; ++r) {
+        const int64_t s = stored_end[r], e = cur_end[r];
+        if (s < 0 || e < s || s % chunk_size != 0) return LMKV_ERR_INVALID_ARG;
+    }
+    for (int32_t r = 0; r < num_req; ++r) {
+        const int64_t full = (cur_end[r] - stored_end[r]) / chunk_size;
+        out_start[r] = stored_end[r];
+        out_end[r] = stored_end[r] + full * chunk_size;
+        n += full;
+    }
+    if (n > INT32_MAX) return LMKV_ERR_INVALID_ARG;
+    *out_num_chunks = (int32_t)n;
+    return LMKV_OK;
+}
+
 int lmkv_gather_chunks(const lmkv_pool_t* pool, const int32_t* block_table, int32_t max_blocks,
                        const int64_t* start, const int64_t* end, int32_t num_req,
                        int32_t chunk_size, int32_t save_unfull_chunk, void* const* chunk_ptrs,

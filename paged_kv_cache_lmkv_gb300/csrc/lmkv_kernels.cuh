@@ -13,15 +13,15 @@
 // bytes of the chunk buffers:
 //   item = (((g * 2 + kv) * layer_n + ll) * blocks_per_chunk + j) * parts + q
 //
-// Two copy engines are provided for the same item stream:
-//  * move_lsu_kernel : CTA-wide 16-byte vector loads into registers, then
-//                      stores; one CTA per item (or grid-stride).
-//  * move_bulk_kernel: one thread per CTA drives the TMA bulk-copy engine
-//                      (cp.async.bulk global->shared->global) through a ring
-//                      of shared-memory stages with mbarrier completion.
+// Copies use move_lsu_kernel: CTA-wide 16-byte vector loads into registers,
+// then stores, one CTA per item (grid-stride when the grid is capped).  (A
+// TMA bulk-copy engine -- cp.async.bulk global->shared->global through a ring
+// of shared-memory stages -- measured slower on GB300 for every stage count
+// and grid shape tried, for whole-batch and per-layer calls.)
 // The fp8 variant quantises one (chunk, K/V, layer) tile per thread-block
-// cluster, keeping the tile in registers and reducing the absmax across the
-// cluster through distributed shared memory, so HBM is read once.
+// cluster: each CTA stages its rows in registers and in shared memory (TMA
+// bulk copies), and the absmax is reduced across the cluster through
+// distributed shared memory, so HBM is read once.
 #pragma once
 
 #include <cstdint>
@@ -231,7 +231,7 @@ move_lsu_kernel(const __grid_constant__ B p, int64_t num_items) {
 }
 
 // ---------------------------------------------------------------------------
-// TMA bulk-copy engine primitives (inline PTX).
+// TMA bulk-copy and mbarrier primitives (inline PTX).
 __device__ __forceinline__ uint32_t smem_addr(const void* ptr) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
 }
@@ -270,122 +270,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 __device__ __forceinline__ void bulk_g2s(void* sdst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  :: "r"(smem_addr(sdst)), "l"(gsrc), "r"(bytes), "r"(smem_addr(bar)) : "memory");
-}
-
-__device__ __forceinline__ void bulk_s2g(void* gdst, const void* ssrc, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
-                 :: "l"(gdst), "r"(smem_addr(ssrc)), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() {
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-__device__ __forceinline__ void bulk_wait_read_1() {
-    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-}
-
-__device__ __forceinline__ void bulk_wait_all() {
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
-// A piece is at most one stage of an item's run.
-struct Piece {
-    const uint8_t* src;
-    uint8_t* dst;
-    uint32_t bytes;
-};
-
-// Sequential cursor over the pieces of the items this CTA owns.
-template <class B, bool kGather, int kStageBytes>
-struct PieceCursor {
-    int64_t item;
-    int64_t num_items;
-    int64_t stride;
-    Run run;
-    uint32_t off;
-    bool have_run;
-
-    __device__ __forceinline__ void init(const B& p, int64_t first, int64_t n, int64_t s) {
-        item = first;
-        num_items = n;
-        stride = s;
-        have_run = false;
-        off = 0;
-        advance_item(p);
-    }
-    __device__ __forceinline__ void advance_item(const B& p) {
-        have_run = false;
-        while (item < num_items) {
-            const bool ok = item_run(p, item, run);
-            item += stride;
-            if (ok && run.bytes > 0) { have_run = true; off = 0; return; }
-        }
-    }
-    __device__ __forceinline__ bool next(const B& p, Piece& pc) {
-        if (!have_run) return false;
-        const uint32_t left = run.bytes - off;
-        const uint32_t n = left < (uint32_t)kStageBytes ? left : (uint32_t)kStageBytes;
-        if (kGather) { pc.src = run.pool + off; pc.dst = run.chunk + off; }
-        else { pc.src = run.chunk + off; pc.dst = run.pool + off; }
-        pc.bytes = n;
-        off += n;
-        if (off >= run.bytes) advance_item(p);
-        return true;
-    }
-};
-
-// TMA engine: lane 0 of a single warp streams pieces through kStages shared
-// stages.  Loads run kStages-1 ahead of stores; a stage is refilled once the
-// bulk store that read it has finished reading (wait_group.read with one
-// group of slack).
-template <class B, bool kGather, int kStages, int kStageBytes>
-__global__ void __launch_bounds__(32)
-move_bulk_kernel(const __grid_constant__ B p, int64_t num_items) {
-    extern __shared__ __align__(128) uint8_t stage_mem[];
-    __shared__ __align__(8) uint64_t bar[kStages];
-    pdl_launch_dependents();
-    pdl_wait();
-    if (threadIdx.x != 0) return;
-    for (int s = 0; s < kStages; ++s) mbar_init(&bar[s], 1);
-    fence_barrier_init();
-
-    PieceCursor<B, kGather, kStageBytes> cur;
-    cur.init(p, blockIdx.x, num_items, gridDim.x);
-    Piece ring[kStages];
-    uint32_t k_load = 0, k_store = 0;
-    Piece pc;
-    while (k_load < (uint32_t)kStages && cur.next(p, pc)) {
-        const int s = (int)(k_load % kStages);
-        ring[s] = pc;
-        mbar_arrive_expect_tx(&bar[s], pc.bytes);
-        bulk_g2s(stage_mem + (size_t)s * kStageBytes, pc.src, pc.bytes, &bar[s]);
-        ++k_load;
-    }
-    bool timed_out = false;
-    while (k_store < k_load) {
-        const int s = (int)(k_store % kStages);
-        if (!mbar_wait_bounded(&bar[s], (k_store / kStages) & 1)) { timed_out = true; break; }
-        bulk_s2g(ring[s].dst, stage_mem + (size_t)s * kStageBytes, ring[s].bytes);
-        bulk_commit();
-        ++k_store;
-        if (k_store >= 2 && cur.next(p, pc)) {
-            // stage of piece k_store-2 is free once its store has read shared memory
-            bulk_wait_read_1();
-            const int sf = (int)(k_load % kStages);
-            ring[sf] = pc;
-            mbar_arrive_expect_tx(&bar[sf], pc.bytes);
-            bulk_g2s(stage_mem + (size_t)sf * kStageBytes, pc.src, pc.bytes, &bar[sf]);
-            ++k_load;
-        }
-    }
-    if (timed_out) {
-        report(p, kStatusTimeout);
-        // let the loads already in flight land before shared memory is released
-        for (uint32_t k = k_store; k < k_load; ++k)
-            (void)mbar_wait_bounded(&bar[k % kStages], (k / kStages) & 1);
-    }
-    bulk_wait_all();
 }
 
 // ---------------------------------------------------------------------------

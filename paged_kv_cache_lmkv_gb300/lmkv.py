@@ -35,7 +35,7 @@ ENTRY_POINTS = (
     "lmkv_scatter_chunks_fp8e4m3", "lmkv_status_string", "lmkv_abi_version",
     "lmkv_launch_count", "lmkv_store_layers", "lmkv_retrieve_layers",
     "lmkv_store_layers_staged", "lmkv_retrieve_layers_staged",
-    "lmkv_store_layers_staged_noalloc",
+    "lmkv_store_layers_staged_noalloc", "lmkv_decode_store_ranges",
 )
 
 
@@ -74,6 +74,7 @@ def load() -> ctypes.CDLL:
         P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
         pool_p = ctypes.POINTER(_PoolT)
         lib.lmkv_count_chunks.argtypes = [P, P, i32, i32, i32, P]
+        lib.lmkv_decode_store_ranges.argtypes = [P, P, i32, i32, P, P, P]
         lib.lmkv_enumerate_chunks.argtypes = [P, P, i32, i32, i32, P, P, P, i32]
         move = [pool_p, P, i32, P, P, i32, i32, i32, P, P, P]
         lib.lmkv_gather_chunks.argtypes = move
@@ -93,6 +94,7 @@ def load() -> ctypes.CDLL:
         lib.lmkv_gather_chunks_fp8e4m3.argtypes = fp8
         lib.lmkv_scatter_chunks_fp8e4m3.argtypes = fp8
         for name in ("lmkv_count_chunks", "lmkv_enumerate_chunks", "lmkv_gather_chunks",
+                     "lmkv_decode_store_ranges",
                      "lmkv_scatter_chunks", "lmkv_gather_layer", "lmkv_scatter_layer",
                      "lmkv_gather_chunks_fp8e4m3", "lmkv_scatter_chunks_fp8e4m3",
                      "lmkv_abi_version", "lmkv_store_layers", "lmkv_retrieve_layers",
@@ -177,6 +179,20 @@ def count_chunks(start, end, chunk_size: int, save_unfull: bool) -> int:
     if rc != OK:
         raise LmkvError(rc, "lmkv_count_chunks")
     return out.value
+
+
+def decode_store_ranges(stored_end, cur_end, chunk_size: int):
+    """lmkv_decode_store_ranges -> (start, end, number of completed chunks)."""
+    lib = load()
+    s, e = _i64_array(stored_end), _i64_array(cur_end)
+    out_s = np.zeros(len(s), np.int64)
+    out_e = np.zeros(len(s), np.int64)
+    n = ctypes.c_int32(0)
+    rc = lib.lmkv_decode_store_ranges(s.ctypes.data, e.ctypes.data, len(s), chunk_size,
+                                      out_s.ctypes.data, out_e.ctypes.data, ctypes.byref(n))
+    if rc != OK:
+        raise LmkvError(rc, "lmkv_decode_store_ranges")
+    return out_s, out_e, n.value
 
 
 def enumerate_chunks(start, end, chunk_size: int, save_unfull: bool):
