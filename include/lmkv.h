@@ -120,6 +120,57 @@ int lmkv_decode_store_ranges(const int64_t* stored_end, const int64_t* cur_end, 
                              int32_t chunk_size, int64_t* out_start, int64_t* out_end,
                              int32_t* out_num_chunks);
 
+/* Dynamic offloading of free pages (LMCache paper, section on the dynamic
+ * offloading mechanism and its Figure 7).  The engine keeps freed pages, whose
+ * KV is still valid, in an ordered free list; before a freed page is handed
+ * to a new query its KV is backed up to CPU memory, so it stays reusable.
+ * Only part of the free list is backed up, tracked by three positions in the
+ * free-list order, with start <= current <= end at all times:
+ *   start   : the next free page the engine will hand out;
+ *   current : pages before it have been backed up;
+ *   end     : pages before it are planned for backup.
+ * The four states of the mechanism: #1 initialised (current == start),
+ * #2 in progress (current moves toward end), #3 a query arrives (it takes
+ * backed-up pages from start, and end moves forward by the number taken),
+ * #4 steady (current == end: every planned page is backed up).  A larger
+ * window (end - start) makes it less likely that a query must wait for
+ * backups, at the cost of more copying.  The struct is caller-owned; these
+ * calls are host-only and never touch the GPU.  The backup copy of positions
+ * [current, current + count) is an ordinary store with block_size-token
+ * chunks (one page per chunk) whose block table is the free list, e.g.
+ * lmkv_store_layers_staged with start = current * B, end = (current+count) * B,
+ * chunk_size = B. */
+typedef struct lmkv_offload {
+    int64_t start;
+    int64_t current;
+    int64_t end;
+    int64_t limit;    /* free-list positions that exist (pages freed so far) */
+    int64_t window;   /* planned backup pages beyond start: end - start <= window */
+} lmkv_offload_t;
+
+/* State #1: start = current = 0, end = min(window, num_free).  INVALID_ARG for
+ * negative sizes or a null state. */
+int lmkv_offload_init(lmkv_offload_t* st, int64_t num_free, int64_t window);
+
+/* The next backup range: *first = current, *count = min(max_pages, end - current).
+ * A count of 0 means steady state (#4). */
+int lmkv_offload_plan(const lmkv_offload_t* st, int64_t max_pages, int64_t* first,
+                      int64_t* count);
+
+/* Record that `count` planned pages starting at `current` were backed up
+ * (state #2).  INVALID_ARG if that would pass end. */
+int lmkv_offload_copied(lmkv_offload_t* st, int64_t count);
+
+/* A query takes up to `want` pages from start (state #3).  Only backed-up
+ * pages can be handed out: *granted = min(want, current - start); start and
+ * end advance by *granted (end capped at limit); *stalled = want - *granted
+ * pages must wait for backups. */
+int lmkv_offload_allocate(lmkv_offload_t* st, int64_t want, int64_t* granted, int64_t* stalled);
+
+/* `n` more pages were freed (appended to the free-list order): limit += n,
+ * and end grows toward start + window. */
+int lmkv_offload_add_free(lmkv_offload_t* st, int64_t n);
+
 /* Store path: X_g[kv][l][t][:] = P_l[kv][BT[r][tok/B]][tok % B][:] for every
  * chunk g (request r, tok = first token of g + t), kv, layer l, t < n_g.
  * Configurable chunk size section of the LMCache paper (pages -> contiguous
@@ -205,6 +256,10 @@ int lmkv_retrieve_layers(const lmkv_pool_t* pool, const int32_t* block_table, in
  *              `staging` to host_chunks[g] (device-to-host);
  *   retrieve : the 2-D copies move the slices from host_chunks[g] into
  *              `staging` (host-to-device), then layer l is scattered from it.
+ * A run of full chunks whose host buffers follow each other in memory is
+ * first tried as one cudaMemcpy3DAsync per layer (much cheaper to issue than
+ * one copy per chunk); the driver accepts that only when the run lies in one
+ * allocation, and otherwise the run is copied chunk by chunk.
  * The copies run on the copy engine, so the transfer uses no SMs while it
  * overlaps compute on another stream; only the short gather / scatter kernel
  * needs SMs.

@@ -318,19 +318,21 @@ int staged_entry(bool store, const lmkv_pool_t* pool, const int32_t* block_table
     const int64_t L = pool->num_layers;
     // Per chunk, rows {K, V} of layer l: n_g * rb bytes each; host pitch
     // L * n_g * rb, staging pitch n_g * rb.  A run of full chunks whose host
-    // buffers are consecutive slices of one allocation (chunk g+1 starts where
-    // chunk g ends) is one 3-D copy (depth = chunks); anything else is one 2-D
-    // copy per chunk.
+    // buffers follow each other in memory (chunk g+1 starts where chunk g
+    // ends) is tried as one 3-D copy (depth = chunks); the driver accepts that
+    // only within one allocation, so if it declines, the run falls back to one
+    // 2-D copy per chunk and no further 3-D copy is tried in this call.
+    bool try_3d = true;
+    auto copy_2d = [&](uint8_t* host, uint8_t* stage, int64_t n) {
+        return store ? cudaMemcpy2DAsync(host, L * n * rb, stage, n * rb, n * rb, 2,
+                                         cudaMemcpyDeviceToHost, s)
+                     : cudaMemcpy2DAsync(stage, n * rb, host, L * n * rb, n * rb, 2,
+                                         cudaMemcpyHostToDevice, s);
+    };
     auto copy_run = [&](int32_t l, int64_t g0, int64_t count, int64_t n, int64_t tok_before) -> int {
         uint8_t* host = static_cast<uint8_t*>(host_chunks[g0]) + (int64_t)l * n * rb;
         uint8_t* stage = static_cast<uint8_t*>(staging) + 2 * rb * tok_before;
-        cudaError_t e;
-        if (count == 1) {
-            e = store ? cudaMemcpy2DAsync(host, L * n * rb, stage, n * rb, n * rb, 2,
-                                          cudaMemcpyDeviceToHost, s)
-                      : cudaMemcpy2DAsync(stage, n * rb, host, L * n * rb, n * rb, 2,
-                                          cudaMemcpyHostToDevice, s);
-        } else {
+        if (count > 1 && try_3d) {
             cudaMemcpy3DParms m = {};
             const cudaPitchedPtr hp = make_cudaPitchedPtr(host, (size_t)(L * n * rb), (size_t)(n * rb), 2);
             const cudaPitchedPtr sp = make_cudaPitchedPtr(stage, (size_t)(n * rb), (size_t)(n * rb), 2);
@@ -338,9 +340,16 @@ int staged_entry(bool store, const lmkv_pool_t* pool, const int32_t* block_table
             m.dstPtr = store ? hp : sp;
             m.extent = make_cudaExtent((size_t)(n * rb), 2, (size_t)count);
             m.kind = store ? cudaMemcpyDeviceToHost : cudaMemcpyHostToDevice;
-            e = cudaMemcpy3DAsync(&m, s);
+            if (cudaMemcpy3DAsync(&m, s) == cudaSuccess) return LMKV_OK;
+            (void)cudaGetLastError();
+            try_3d = false;
         }
-        return e == cudaSuccess ? LMKV_OK : LMKV_ERR_CUDA;
+        const int64_t chunk_bytes = 2 * L * n * rb;
+        for (int64_t k = 0; k < count; ++k) {
+            if (copy_2d(host + k * chunk_bytes, stage + k * 2 * n * rb, n) != cudaSuccess)
+                return LMKV_ERR_CUDA;
+        }
+        return LMKV_OK;
     };
     auto copies = [&](int32_t l) -> int {
         int64_t g = 0, tok_before = 0;
@@ -571,6 +580,64 @@ int lmkv_decode_store_ranges(const int64_t* stored_end, const int64_t* cur_end, 
     }
     if (n > INT32_MAX) return LMKV_ERR_INVALID_ARG;
     *out_num_chunks = (int32_t)n;
+    return LMKV_OK;
+}
+
+// Dynamic offloading of free pages: host-only bookkeeping of the three
+// positions; every call keeps start <= current <= end <= limit.
+static bool offload_ok(const lmkv_offload_t* st) {
+    return st != nullptr && 0 <= st->start && st->start <= st->current && st->current <= st->end &&
+           st->end <= st->limit && st->window >= 0;
+}
+
+static int64_t offload_target_end(const lmkv_offload_t* st) {
+    const int64_t t = st->start + st->window;
+    return t < st->limit ? t : st->limit;
+}
+
+int lmkv_offload_init(lmkv_offload_t* st, int64_t num_free, int64_t window) {
+    if (st == nullptr || num_free < 0 || window < 0) return LMKV_ERR_INVALID_ARG;
+    st->start = 0;
+    st->current = 0;
+    st->limit = num_free;
+    st->window = window;
+    st->end = offload_target_end(st);
+    return LMKV_OK;
+}
+
+int lmkv_offload_plan(const lmkv_offload_t* st, int64_t max_pages, int64_t* first, int64_t* count) {
+    if (!offload_ok(st) || max_pages < 0 || first == nullptr || count == nullptr)
+        return LMKV_ERR_INVALID_ARG;
+    const int64_t left = st->end - st->current;
+    *first = st->current;
+    *count = left < max_pages ? left : max_pages;
+    return LMKV_OK;
+}
+
+int lmkv_offload_copied(lmkv_offload_t* st, int64_t count) {
+    if (!offload_ok(st) || count < 0 || st->current + count > st->end) return LMKV_ERR_INVALID_ARG;
+    st->current += count;
+    return LMKV_OK;
+}
+
+int lmkv_offload_allocate(lmkv_offload_t* st, int64_t want, int64_t* granted, int64_t* stalled) {
+    if (!offload_ok(st) || want < 0 || granted == nullptr || stalled == nullptr)
+        return LMKV_ERR_INVALID_ARG;
+    const int64_t ready = st->current - st->start;
+    const int64_t g = want < ready ? want : ready;
+    st->start += g;
+    const int64_t e = st->end + g;
+    st->end = e < st->limit ? e : st->limit;
+    *granted = g;
+    *stalled = want - g;
+    return LMKV_OK;
+}
+
+int lmkv_offload_add_free(lmkv_offload_t* st, int64_t n) {
+    if (!offload_ok(st) || n < 0) return LMKV_ERR_INVALID_ARG;
+    st->limit += n;
+    const int64_t t = offload_target_end(st);
+    if (st->end < t) st->end = t;
     return LMKV_OK;
 }
 

@@ -36,6 +36,8 @@ ENTRY_POINTS = (
     "lmkv_launch_count", "lmkv_store_layers", "lmkv_retrieve_layers",
     "lmkv_store_layers_staged", "lmkv_retrieve_layers_staged",
     "lmkv_store_layers_staged_noalloc", "lmkv_decode_store_ranges",
+    "lmkv_offload_init", "lmkv_offload_plan", "lmkv_offload_copied", "lmkv_offload_allocate",
+    "lmkv_offload_add_free",
 )
 
 
@@ -43,6 +45,15 @@ class LmkvError(RuntimeError):
     def __init__(self, code: int, what: str = ""):
         self.code = code
         super().__init__(f"{what}: lmkv status {code} ({status_string(code)})")
+
+
+class OffloadState(ctypes.Structure):
+    """lmkv_offload_t: positions in the free-page order, start <= current <= end."""
+    _fields_ = [("start", ctypes.c_int64), ("current", ctypes.c_int64), ("end", ctypes.c_int64),
+                ("limit", ctypes.c_int64), ("window", ctypes.c_int64)]
+
+    def as_tuple(self):
+        return (self.start, self.current, self.end, self.limit, self.window)
 
 
 class _PoolT(ctypes.Structure):
@@ -75,6 +86,12 @@ def load() -> ctypes.CDLL:
         pool_p = ctypes.POINTER(_PoolT)
         lib.lmkv_count_chunks.argtypes = [P, P, i32, i32, i32, P]
         lib.lmkv_decode_store_ranges.argtypes = [P, P, i32, i32, P, P, P]
+        off_p = ctypes.POINTER(OffloadState)
+        lib.lmkv_offload_init.argtypes = [off_p, i64, i64]
+        lib.lmkv_offload_plan.argtypes = [off_p, i64, P, P]
+        lib.lmkv_offload_copied.argtypes = [off_p, i64]
+        lib.lmkv_offload_allocate.argtypes = [off_p, i64, P, P]
+        lib.lmkv_offload_add_free.argtypes = [off_p, i64]
         lib.lmkv_enumerate_chunks.argtypes = [P, P, i32, i32, i32, P, P, P, i32]
         move = [pool_p, P, i32, P, P, i32, i32, i32, P, P, P]
         lib.lmkv_gather_chunks.argtypes = move
@@ -94,7 +111,8 @@ def load() -> ctypes.CDLL:
         lib.lmkv_gather_chunks_fp8e4m3.argtypes = fp8
         lib.lmkv_scatter_chunks_fp8e4m3.argtypes = fp8
         for name in ("lmkv_count_chunks", "lmkv_enumerate_chunks", "lmkv_gather_chunks",
-                     "lmkv_decode_store_ranges",
+                     "lmkv_decode_store_ranges", "lmkv_offload_init", "lmkv_offload_plan",
+                     "lmkv_offload_copied", "lmkv_offload_allocate", "lmkv_offload_add_free",
                      "lmkv_scatter_chunks", "lmkv_gather_layer", "lmkv_scatter_layer",
                      "lmkv_gather_chunks_fp8e4m3", "lmkv_scatter_chunks_fp8e4m3",
                      "lmkv_abi_version", "lmkv_store_layers", "lmkv_retrieve_layers",
@@ -193,6 +211,37 @@ def decode_store_ranges(stored_end, cur_end, chunk_size: int):
     if rc != OK:
         raise LmkvError(rc, "lmkv_decode_store_ranges")
     return out_s, out_e, n.value
+
+
+class Offload:
+    """Thin wrapper of the lmkv_offload_* calls on one caller-owned state."""
+
+    def __init__(self, num_free: int, window: int):
+        self.state = OffloadState()
+        self._call("lmkv_offload_init", ctypes.byref(self.state), int(num_free), int(window))
+
+    def _call(self, name, *args):
+        rc = getattr(load(), name)(*args)
+        if rc != OK:
+            raise LmkvError(rc, name)
+
+    def plan(self, max_pages: int):
+        first, count = ctypes.c_int64(0), ctypes.c_int64(0)
+        self._call("lmkv_offload_plan", ctypes.byref(self.state), int(max_pages),
+                   ctypes.byref(first), ctypes.byref(count))
+        return first.value, count.value
+
+    def copied(self, count: int):
+        self._call("lmkv_offload_copied", ctypes.byref(self.state), int(count))
+
+    def allocate(self, want: int):
+        g, s = ctypes.c_int64(0), ctypes.c_int64(0)
+        self._call("lmkv_offload_allocate", ctypes.byref(self.state), int(want), ctypes.byref(g),
+                   ctypes.byref(s))
+        return g.value, s.value
+
+    def add_free(self, n: int):
+        self._call("lmkv_offload_add_free", ctypes.byref(self.state), int(n))
 
 
 def enumerate_chunks(start, end, chunk_size: int, save_unfull: bool):
