@@ -139,3 +139,143 @@ def test_unmodified_oracle_passes_every_pin(tmp_path):
 def test_planted_mistake_is_caught(tmp_path, name):
     failed = pins(load_oracle(tmp_path, name, MUTANTS[name]))
     assert failed, f"mutant {name} passed every pin"
+
+
+# ---- the CacheGen codec oracle ----
+
+CG_SRC = os.path.join(ROOT, "oracle", "cachegen_oracle.c")
+
+CG_MUTANTS = {
+    "max_is_half_bins": ("int32_t MAX = bins / 2 - 1;", "int32_t MAX = bins / 2;", "all"),
+    "cdf_floor": ("        if (2 * r > (uint64_t)n || (2 * r == (uint64_t)n && (q & 1))) q += 1;\n", ""),
+    "cdf_ties_up": ("(2 * r == (uint64_t)n && (q & 1))", "(2 * r == (uint64_t)n)"),
+    "cdf_no_ramp": ("C[k] = (uint32_t)(q + (uint64_t)k);", "C[k] = (uint32_t)q;"),
+    "cdf_inclusive_cumsum": ("uint64_t num = cum * M;", "uint64_t num = (cum + (uint64_t)count[k]) * M;"),
+    "follow_bits_same_value": ("write_bit(w, !bit);", "write_bit(w, bit);"),
+    "final_bits_flipped": ("low < CG_QUARTER ? 0 : 1", "low < CG_QUARTER ? 1 : 0"),
+    "decoder_keeps_top_half": ("                value -= CG_HALF;\n", ""),
+    "batch_of_128": ("#define CG_BATCH 256", "#define CG_BATCH 128"),
+    "v_bins_like_k": ("bins[num_layers + l] = (all32 || l < 2)", "bins[num_layers + l] = (all32 || l < 10)"),
+    "max1_skips_first_channel": ("        for (int32_t c = 0; c < H; ++c) {\n            float a",
+                                 "        for (int32_t c = 1; c < H; ++c) {\n            float a"),
+    "dequant_without_offset": ("(float)((int32_t)sym[(int64_t)t * H + c] - MAX) / (float)MAX",
+                               "(float)((int32_t)sym[(int64_t)t * H + c]) / (float)MAX"),
+    "quant_truncates": ("q = (int32_t)nearbyintf(z);", "q = (int32_t)z;"),
+}
+
+
+def load_cachegen(tmp_path, name, mutation=None):
+    src = open(CG_SRC).read()
+    if mutation is not None:
+        old, new = mutation[:2]
+        assert src.count(old) >= 1, f"mutation site not found: {name}"
+        src = src.replace(old, new, -1 if mutation[2:] == ("all",) else 1)
+    d = tmp_path / ("cg_" + name)
+    d.mkdir()
+    (d / "cachegen_oracle.c").write_text(src)
+    spec = importlib.util.spec_from_file_location(f"cachegen_{name}", os.path.join(ROOT, "oracle", "cachegen.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod._SRC = str(d / "cachegen_oracle.c")
+    mod._LIB = str(d / "libcachegen_oracle.so")
+    mod._lib = None
+    return mod
+
+
+def cachegen_pins(o):
+    """Names of the CacheGen pins that fail for oracle module `o` (the same
+    kinds of check as tests/test_oracle_cachegen.py, compacted)."""
+    import test_oracle_cachegen as t
+    failed = []
+
+    def run(name, fn):
+        try:
+            if fn() is False:
+                failed.append(name)
+        except Exception:       # a crash or a rejected call fails the pin too
+            failed.append(name)
+
+    def golden_bins():
+        for case in t._golden("bins"):
+            lhs, rhs = case.split("->")
+            L = int(lhs)
+            k_part, v_part = rhs.split("V:")
+            expect = [[int(b) for run in part.split() for b in [run.split("x")[1]] * int(run.split("x")[0])]
+                      for part in (k_part.replace("K:", ""), v_part)]
+            if o.default_bins(L).tolist() != expect:
+                return False
+
+    def golden_cdf():
+        for case in t._golden("cdf"):
+            lhs, rhs = case.split("->")
+            bins, *syms = [int(v) for v in lhs.split()]
+            if o.cdf(np.array(syms, np.uint8), o.nsym(bins)).tolist() != [int(v) for v in rhs.split()]:
+                return False
+        rng = np.random.default_rng(1)
+        for n in (3, 256):
+            syms = rng.integers(0, 15, n)
+            if o.cdf(syms.astype(np.uint8), 15).tolist() != t._cdf_exact(syms, 15):
+                return False
+
+    def golden_code():
+        for case in t._golden("code"):
+            lhs, rhs = case.split("->")
+            cdf_part, sym_part = lhs.split(":")
+            C = np.array([int(v) for v in cdf_part.split()], np.uint32)
+            syms = np.array([int(v) for v in sym_part.split()], np.uint8)
+            code = o.encode(syms, C)
+            if code != t._hex(rhs) or not np.array_equal(o.decode(code, len(syms), C), syms):
+                return False
+
+    def round_trip():
+        rng = np.random.default_rng(2)
+        for trial in range(12):
+            C = t._random_cdf(rng, 15, trial % 2 == 0)
+            syms = rng.integers(0, 15, 200).astype(np.uint8)
+            code = o.encode(syms, C)
+            ideal = t._ideal_bits(syms, C)
+            if not np.array_equal(o.decode(code, 200, C), syms) or not ideal <= 8 * len(code) <= ideal + 10:
+                return False
+
+    def golden_quant():
+        for case in t._golden("quant"):
+            lhs, rhs = case.split("->")
+            bins, *vals = lhs.split()
+            sym_part, deq_part = rhs.split("|")
+            row = t._bf16([float(v) for v in vals])[None, :]
+            sym, max1 = o.quantize(row, int(bins))
+            if sym[0].tolist() != [int(v) for v in sym_part.split()]:
+                return False
+            if [f"{v:04x}" for v in o.dequantize(sym, max1, int(bins))[0]] != deq_part.split():
+                return False
+
+    def chunk():
+        L, n, H = 2, 300, 16
+        bins = o.default_bins(L)
+        x = t._chunk(L, n, H, 3)
+        blob = o.encode_chunk(x, bins)
+        parts = o.parse(blob, L, n, H, bins)
+        if parts["lengths"].shape[0] != 2 or len(blob) != parts["layout"]["bytes"] + int(parts["lengths"].sum()):
+            return False
+        xb = x.view(torch.int16).numpy().view(np.uint16)
+        got = o.decode_chunk(blob, L, n, H, bins)
+        xf = (xb.astype(np.uint32) << 16).view(np.float32)
+        yf = (got.astype(np.uint32) << 16).view(np.float32)
+        max1 = np.abs(xf).max(axis=3, keepdims=True)
+        MAX = (bins // 2 - 1)[:, :, None, None]
+        return bool(np.all(np.abs(yf - xf) <= max1 * (0.5 / MAX * (1 + 1e-5) + 2.0 ** -8)))
+
+    for name, fn in [("bins", golden_bins), ("cdf", golden_cdf), ("code", golden_code),
+                     ("round_trip", round_trip), ("quant", golden_quant), ("chunk", chunk)]:
+        run(name, fn)
+    return failed
+
+
+def test_unmodified_cachegen_oracle_passes_every_pin(tmp_path):
+    assert cachegen_pins(load_cachegen(tmp_path, "clean")) == []
+
+
+@pytest.mark.parametrize("name", sorted(CG_MUTANTS))
+def test_planted_cachegen_mistake_is_caught(tmp_path, name):
+    failed = cachegen_pins(load_cachegen(tmp_path, name, CG_MUTANTS[name]))
+    assert failed, f"mutant {name} passed every pin"
