@@ -73,7 +73,8 @@ typedef enum lmkv_status {
     LMKV_ERR_BAD_BLOCK = 5,     /* device: a block id outside [0, num_blocks); token skipped */
     LMKV_ERR_BAD_POINTER = 6,   /* device: null or misaligned entry in a pointer array; skipped */
     LMKV_ERR_TIMEOUT = 7,       /* device: a bounded wait on an asynchronous copy gave up */
-    LMKV_ERR_SCRATCH_LIMIT = 8  /* host: the batch needs more than the library's built-in scratch */
+    LMKV_ERR_SCRATCH_LIMIT = 8, /* host: the batch needs more than the library's built-in scratch */
+    LMKV_ERR_BAD_DATA = 9       /* device: an encoded blob is inconsistent (stream skipped) */
 } lmkv_status;
 
 /* The paged KV pool.  layer_base is a DEVICE array of num_layers DEVICE
@@ -351,6 +352,99 @@ int lmkv_scatter_chunks_fp8e4m3(const lmkv_pool_t* pool, const int32_t* block_ta
                                 int32_t num_req, int32_t chunk_size, int32_t save_unfull_chunk,
                                 void* const* code_ptrs, const float* scales, int32_t* d_status,
                                 void* stream);
+
+/* ---- CacheGen KV codec ------------------------------------------------
+ * "LMCache 中的 KV Cache 压缩：CacheGen 编解码原理、配置方式与源码解析",
+ * sections 1-5.  A chunk buffer [2][L][n][H] of bf16 (H = num_kv_heads *
+ * head_dim channels, the layout of lmkv_gather_chunks) is quantised per
+ * (K/V, layer) with that slice's bin count, the symbols of every
+ * (K/V, layer, channel) get a CDF over the chunk's n tokens, and every
+ * channel's symbols are arithmetic-coded in batches of at most 256 tokens:
+ *
+ *   MAX     = bins/2 - 1,  nsym = 2*MAX + 1 symbols, Lp = nsym + 1
+ *   max1[t] = max over the row's H channels of |x|           (section 2)
+ *   q       = clamp(round(x * (MAX / max1) + MAX), 0, 2*MAX)  each step one
+ *             IEEE fp32 operation, ties to even; max1 == 0 gives q = MAX
+ *   C[k]    = round(cum[k] * (2^16 - (Lp - 1)) / n) + k, k = 0..nsym, cum[k]
+ *             the tokens whose symbol is below k, the division exact, ties
+ *             to even (section 3); C[0] = 0, C[nsym] = 2^16
+ *   coder   = Witten-Neal-Cleary arithmetic coding ("Arithmetic coding for
+ *             data compression", CACM 30(6), 1987), 32-bit low/high,
+ *             frequencies out of 2^16, bits most significant first, the
+ *             last byte zero-padded (section 4)
+ *   decode  = y = bf16(((q - MAX) / MAX) * max1), two fp32 operations
+ *             (section 5)
+ * Inputs must be finite.  bins are 4..32 per (K/V, layer):
+ * bins[kv * L + l]; lmkv_cachegen_default_bins gives the page's rule.
+ *
+ * Encoded chunk ("blob", one per chunk; integers little-endian):
+ *   max1     float32 [2][L][n]                       at max1_offset (0)
+ *   cdf      uint16: for each (kv, l) in order, [H][nsym(kv,l) - 1] holding
+ *            C[1..nsym-1]                            at cdf_offset
+ *   lengths  uint32 [nb][2][L][H], nb = ceil(n/256)  at lengths_offset
+ *   bytes    the streams back to back in (batch, kv, l, channel) order,
+ *            each channel's symbols for the batch's tokens; a stream starts
+ *            at the prefix sum of the lengths before it    at bytes_offset
+ * size = bytes_offset + sum(lengths) <= max_bytes.
+ */
+#define LMKV_CACHEGEN_BATCH 256
+#define LMKV_CACHEGEN_MAX_CHANNELS 2048
+#define LMKV_CACHEGEN_MAX_TOKENS 4096
+#define LMKV_CACHEGEN_MAX_LAYERS 128
+
+typedef struct lmkv_cachegen_layout {
+    uint64_t max1_offset;
+    uint64_t cdf_offset;
+    uint64_t lengths_offset;
+    uint64_t bytes_offset;
+    uint64_t max_bytes;   /* bound on the size: a stream of nt symbols takes at
+                             most ceil((18 * nt + 2) / 8) bytes */
+} lmkv_cachegen_layout_t;
+
+/* The page's bins (section 1): K 32 bins for layers 0-9 and 16 after, V 32
+ * bins for layers 0-1 and 16 after; fewer than 10 layers: 32 everywhere.
+ * bins: HOST int32 [2 * num_layers].  INVALID_ARG for num_layers outside
+ * 1..LMKV_CACHEGEN_MAX_LAYERS or a null pointer.  Host only. */
+int lmkv_cachegen_default_bins(int32_t num_layers, int32_t* bins);
+
+/* Offsets of one chunk's blob.  INVALID_ARG unless 1 <= num_layers <=
+ * LMKV_CACHEGEN_MAX_LAYERS, 1 <= num_tokens <= LMKV_CACHEGEN_MAX_TOKENS,
+ * 4 <= channels <= LMKV_CACHEGEN_MAX_CHANNELS with channels % 4 == 0, and
+ * every bins entry in 4..32.  Host only. */
+int lmkv_cachegen_layout(int32_t num_layers, int32_t num_tokens, int32_t channels,
+                         const int32_t* bins, lmkv_cachegen_layout_t* out);
+
+/* Device workspace the two calls below need for these chunks (HOST
+ * num_tokens[num_chunks]); the same size serves encode and decode. */
+int lmkv_cachegen_workspace_bytes(int32_t num_layers, int32_t channels, const int32_t* num_tokens,
+                                  int32_t num_chunks, uint64_t* bytes);
+
+/* Encode chunk g (DEVICE chunk_ptrs[g] -> [2][L][n_g][H] bf16, 16-byte
+ * aligned) into DEVICE blob_ptrs[g] (at least max_bytes of its layout) and
+ * store its size into DEVICE sizes[g] (uint64).  num_tokens and bins are
+ * HOST arrays; workspace is DEVICE memory of lmkv_cachegen_workspace_bytes
+ * bytes (16-byte aligned, contents irrelevant, not shared with calls in
+ * flight).  Enqueues three kernels per group of up to 64 chunks on `stream`:
+ * quantise + CDF per (chunk, kv, l), code per (chunk, batch, kv, l),
+ * compact the streams.  Host errors as lmkv_cachegen_layout, plus
+ * INVALID_ARG for null arrays or a workspace that is too small; device
+ * errors (a null chunk pointer: BAD_POINTER) go to *d_status. */
+int lmkv_cachegen_encode(void* const* chunk_ptrs, const int32_t* num_tokens, int32_t num_chunks,
+                         int32_t num_layers, int32_t channels, const int32_t* bins,
+                         void* const* blob_ptrs, uint64_t* sizes, void* workspace,
+                         uint64_t workspace_bytes, int32_t* d_status, void* stream);
+
+/* Decode blob g (DEVICE blob_ptrs[g], DEVICE sizes[g] bytes) into DEVICE
+ * chunk_ptrs[g] ([2][L][n_g][H] bf16, 16-byte aligned).  Streams are found
+ * through the prefix sums of the lengths (section 5).  A blob whose lengths
+ * do not add up to its size, or a stream that would run past it, is not
+ * decoded (its rows keep their contents) and sets *d_status to BAD_DATA.
+ * Two kernels per group of up to 64 chunks: region totals, then decode +
+ * dequantise per (chunk, batch, kv, l). */
+int lmkv_cachegen_decode(void* const* blob_ptrs, const uint64_t* sizes, const int32_t* num_tokens,
+                         int32_t num_chunks, int32_t num_layers, int32_t channels,
+                         const int32_t* bins, void* const* chunk_ptrs, void* workspace,
+                         uint64_t workspace_bytes, int32_t* d_status, void* stream);
 
 /* Human-readable name of a status code (static storage). */
 const char* lmkv_status_string(int status);

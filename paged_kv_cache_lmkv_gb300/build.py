@@ -10,8 +10,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "liblmkv.so")
-SOURCES = [os.path.join(CSRC, "lmkv_api.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, "lmkv_kernels.cuh"), os.path.join(INCLUDE, "lmkv.h")]
+SOURCES = [os.path.join(CSRC, "lmkv_api.cu"), os.path.join(CSRC, "lmkv_cachegen.cu")]
+DEPS = SOURCES + [os.path.join(CSRC, "lmkv_kernels.cuh"), os.path.join(CSRC, "lmkv_internal.h"),
+                  os.path.join(INCLUDE, "lmkv.h")]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 
@@ -33,11 +34,29 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if not force and not is_stale():
         return LIB
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc_path(), ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared",
-           "-Xcompiler", "-fPIC", "-I", INCLUDE, "-o", tmp] + SOURCES
-    if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    subprocess.run(cmd, check=True)
+    nvcc = nvcc_path()
+    # one object per translation unit, compiled in parallel, then one link
+    objs, procs = [], []
+    for src in SOURCES:
+        obj = f"{tmp}.{os.path.basename(src)}.o"
+        cmd = [nvcc, ARCH, "-O3", "-lineinfo", "-std=c++17", "-c", "-Xcompiler", "-fPIC",
+               "-I", INCLUDE, "-o", obj, src]
+        if verbose:
+            cmd.insert(1, "-Xptxas=-v")
+        objs.append(obj)
+        procs.append((subprocess.Popen(cmd), cmd))
+    try:
+        for proc, cmd in procs:
+            if proc.wait() != 0:
+                raise subprocess.CalledProcessError(proc.returncode, cmd)
+        subprocess.run([nvcc, ARCH, "-shared", "-o", tmp] + objs, check=True)
+    finally:
+        for proc, _ in procs:
+            if proc.poll() is None:
+                proc.kill()
+        for obj in objs:
+            if os.path.exists(obj):
+                os.remove(obj)
     os.replace(tmp, LIB)
     return LIB
 

@@ -7,6 +7,7 @@
 // kernels of lmkv_kernels.cuh on the caller's stream.  Nothing is allocated
 // and nothing is synchronised.
 #include "lmkv.h"
+#include "lmkv_internal.h"
 #include "lmkv_kernels.cuh"
 
 #include <atomic>
@@ -525,6 +526,8 @@ void* noalloc_staging_address() {
 
 }  // namespace
 
+void lmkv_internal_add_launches(int64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
 extern "C" {
 
 int lmkv_count_chunks(const int64_t* start, const int64_t* end, int32_t num_req,
@@ -746,6 +749,7 @@ const char* lmkv_status_string(int status) {
         case LMKV_ERR_BAD_POINTER: return "null or misaligned device pointer in an array (skipped)";
         case LMKV_ERR_TIMEOUT: return "bounded device wait gave up";
         case LMKV_ERR_SCRATCH_LIMIT: return "batch needs more than the built-in staging area";
+        case LMKV_ERR_BAD_DATA: return "encoded blob inconsistent with its size (stream skipped)";
         default: return "unknown status";
     }
 }

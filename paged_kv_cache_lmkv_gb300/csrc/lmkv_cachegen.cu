@@ -1,0 +1,817 @@
+// lmkv_cachegen.cu -- the CacheGen KV codec on sm_103a ("LMCache 中的 KV Cache
+// 压缩：CacheGen 编解码原理、配置方式与源码解析", sections 1-5).
+//
+// Encode, per group of up to kMaxChunks chunks (three kernels):
+//   cg_cdf_kernel     one CTA per (chunk, kv, layer): per-token absmax over the
+//                     row (section 2), the symbols (into the workspace), a
+//                     per-channel histogram in shared memory and the 2^16 CDF
+//                     with its arange ramp (section 3), written to the blob.
+//   cg_code_kernel    one CTA per (chunk, 256-token batch, kv, layer): every
+//                     thread runs kStreams independent arithmetic coders, one
+//                     per channel (section 4), into fixed-size slots.
+//   cg_compact_kernel one CTA per region: the prefix sums of the stream lengths
+//                     place each slot's bytes into the blob.
+// Decode (two kernels): cg_total_kernel sums each region's lengths, then
+// cg_decode_kernel finds each stream by the prefix sums (section 5), decodes
+// kStreams channels per thread and writes the dequantised bf16 rows.
+//
+// The coder is the integer arithmetic coder of Witten, Neal and Cleary
+// (CACM 30(6), 1987) with 32-bit registers and frequencies out of 2^16.  Its
+// bit-at-a-time renormalisation is taken here in two jumps: the run of
+// leading bits where low and high agree (count leading zeros of low ^ high)
+// is shifted out at once, then the run of middle-straddling steps (low =
+// 01..., high = 10...) is counted and folded into the pending bits.  The bits
+// produced are those of the one-bit-per-step loop.
+#include "lmkv.h"
+#include "lmkv_internal.h"
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace {
+
+constexpr int kBatch = LMKV_CACHEGEN_BATCH;
+constexpr int kMaxChunks = 64;                 // chunks per launch
+constexpr int kMaxSlices = 2 * LMKV_CACHEGEN_MAX_LAYERS;
+constexpr int kStreams = 4;                    // channels (streams) per thread
+constexpr int kRows = 8;                       // rows per block-wide absmax round
+constexpr int kMaxThreads = LMKV_CACHEGEN_MAX_CHANNELS / kStreams;
+constexpr uint32_t kHalf = 0x80000000u;
+constexpr uint32_t kQuarter = 0x40000000u;
+
+struct CgParams {
+    const uint8_t* const* chunk_ptrs;   // DEVICE array of chunk buffers
+    uint8_t* const* blob_ptrs;          // DEVICE array of blobs
+    uint64_t* sizes;                    // DEVICE blob sizes (encode writes, decode reads)
+    int32_t* status;
+    uint8_t* ws;
+    int32_t L, H, nchunks, cdf_entries;
+    int32_t ntok[kMaxChunks];
+    uint64_t tot_off[kMaxChunks];       // workspace byte offsets per chunk
+    uint64_t sym_off[kMaxChunks];
+    uint64_t slot_off[kMaxChunks];
+    int32_t cdf_prefix[kMaxSlices];     // cdf entries before slice s
+    uint8_t bins[kMaxSlices];
+};
+
+__host__ __device__ inline int nsym_of(int bins) { return 2 * (bins / 2 - 1) + 1; }
+__host__ __device__ inline int batches_of(int n) { return (n + kBatch - 1) / kBatch; }
+
+// Blob offsets (the layout in lmkv.h).
+__host__ __device__ inline uint64_t cdf_offset(int L, int n) { return 8ull * (uint64_t)L * n; }
+__host__ __device__ inline uint64_t lengths_offset(int L, int n, int cdf_entries) {
+    return (cdf_offset(L, n) + 2ull * (uint64_t)cdf_entries + 3) & ~3ull;
+}
+__host__ __device__ inline uint64_t bytes_offset(int L, int n, int H, int cdf_entries) {
+    return lengths_offset(L, n, cdf_entries) + 4ull * batches_of(n) * 2ull * L * H;
+}
+// Largest stream of nt symbols: every symbol leaves an interval of at least
+// 2^14 of at most 2^32 and each emitted or pending bit doubles it, so at most
+// 18 bits per symbol, plus the two final bits.
+__host__ __device__ inline uint64_t stream_bound(int nt) { return (18ull * nt + 2 + 7) / 8; }
+// Slot stride in the workspace: the bound rounded up to 16 bytes.
+__host__ __device__ inline uint64_t slot_stride(int n) {
+    const int nt = n < kBatch ? n : kBatch;
+    return (stream_bound(nt) + 15) & ~15ull;
+}
+
+__device__ __forceinline__ void set_status(int32_t* st, int code) {
+    if (st != nullptr) atomicCAS(st, 0, code);
+}
+
+__device__ __forceinline__ uint2 ld_nc_v2(const void* p) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
+                 : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+
+// |x| of two packed bf16 as the larger fp32 bit pattern (non-negative floats
+// order like their bit patterns).
+__device__ __forceinline__ uint32_t abs_max_bits(uint32_t two_bf16) {
+    const uint32_t a = (two_bf16 << 16) & 0x7FFF0000u;
+    const uint32_t b = two_bf16 & 0x7FFF0000u;
+    return a > b ? a : b;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// q = clamp(round(x * factor + MAX), 0, 2*MAX), one fp32 operation per step.
+__device__ __forceinline__ uint32_t quantise(float x, float factor, float maxf, int two_max) {
+    const float z = __fadd_rn(__fmul_rn(x, factor), maxf);
+    int q = __float2int_rn(z);
+    q = q < 0 ? 0 : (q > two_max ? two_max : q);
+    return (uint32_t)q;
+}
+
+// ---- arithmetic encoder state, one per stream ----
+struct Enc {
+    uint32_t low, high, follow, nacc, words;
+    uint64_t acc;          // pending output bits, the last nacc valid
+};
+
+__device__ __forceinline__ void enc_init(Enc& e) {
+    e.low = 0;
+    e.high = 0xFFFFFFFFu;
+    e.follow = 0;
+    e.nacc = 0;
+    e.words = 0;
+    e.acc = 0;
+}
+
+// Append the c (0..32) low bits of v; full 32-bit words go to the slot,
+// most significant byte first.
+__device__ __forceinline__ void put_bits(Enc& e, uint32_t v, uint32_t c, uint32_t* slot,
+                                         uint32_t cap_words, bool& overflow) {
+    e.acc = (e.acc << c) | v;
+    e.nacc += c;
+    if (e.nacc >= 32) {
+        e.nacc -= 32;
+        const uint32_t w = (uint32_t)(e.acc >> e.nacc);
+        if (e.words < cap_words) slot[e.words] = __byte_perm(w, 0, 0x0123);
+        else overflow = true;
+        ++e.words;
+    }
+}
+
+// The decided bit `bit`, then e.follow opposite bits, then the k-1 bits `rest`.
+__device__ __forceinline__ void emit(Enc& e, uint32_t bit, uint32_t k, uint32_t rest, uint32_t* slot,
+                                     uint32_t cap_words, bool& overflow) {
+    const uint32_t f = e.follow;
+    if (f + k <= 32) {
+        const uint32_t run = bit ? 0u : (f ? (0xFFFFFFFFu >> (32 - f)) : 0u);
+        const uint64_t v = ((uint64_t)bit << (f + k - 1)) | ((uint64_t)run << (k - 1)) | rest;
+        put_bits(e, (uint32_t)v, f + k, slot, cap_words, overflow);
+    } else {
+        put_bits(e, bit, 1, slot, cap_words, overflow);
+        for (uint32_t left = f; left > 0;) {
+            const uint32_t c = left < 32 ? left : 32;
+            put_bits(e, bit ? 0u : (0xFFFFFFFFu >> (32 - c)), c, slot, cap_words, overflow);
+            left -= c;
+        }
+        put_bits(e, rest, k - 1, slot, cap_words, overflow);
+    }
+    e.follow = 0;
+}
+
+// Narrow [low, high] to the symbol's [lo, hi) out of 2^16 and renormalise.
+__device__ __forceinline__ void enc_symbol(Enc& e, uint32_t lo, uint32_t hi, uint32_t* slot,
+                                           uint32_t cap_words, bool& overflow) {
+    const uint32_t rm1 = e.high - e.low;                       // range - 1
+    const uint64_t top = (uint64_t)rm1 * hi + hi;              // range * hi
+    const uint64_t bot = (uint64_t)rm1 * lo + lo;              // range * lo
+    e.high = e.low + (uint32_t)(top >> 16) - 1;
+    e.low = e.low + (uint32_t)(bot >> 16);
+    const uint32_t k = __clz(e.low ^ e.high);                  // leading agreed bits
+    if (k) {
+        const uint32_t rest = k > 1 ? (e.low << 1) >> (33 - k) : 0u;
+        emit(e, e.low >> 31, k, rest, slot, cap_words, overflow);
+        e.low <<= k;
+        e.high = (e.high << k) | ((1u << k) - 1);
+    }
+    const uint32_t a = __clz(~(e.low << 1)), b = __clz(e.high << 1);
+    const uint32_t m = a < b ? a : b;                          // straddling steps
+    if (m) {
+        e.follow += m;
+        e.low = (e.low << m) & 0x7FFFFFFFu;
+        e.high = (e.high << m) | kHalf | ((1u << m) - 1);
+    }
+}
+
+// Two final bits select a point inside the last interval; returns the
+// stream's length in bytes.
+__device__ __forceinline__ uint32_t enc_finish(Enc& e, uint32_t* slot, uint32_t cap_words,
+                                               bool& overflow) {
+    e.follow += 1;
+    emit(e, e.low >= kQuarter ? 1u : 0u, 1, 0, slot, cap_words, overflow);
+    const uint32_t bits = e.words * 32 + e.nacc;
+    if (e.nacc) {
+        const uint32_t w = (uint32_t)(e.acc << (32 - e.nacc));
+        if (e.words < cap_words) slot[e.words] = __byte_perm(w, 0, 0x0123);
+        else overflow = true;
+    }
+    return (bits + 7) >> 3;
+}
+
+// ---- arithmetic decoder state, one per stream ----
+struct Dec {
+    uint32_t low, high, value, nbuf, left;
+    uint64_t buf;           // upcoming bits, most significant first; nbuf valid
+    const uint8_t* p;       // next unread byte; `left` bytes remain in the stream
+};
+
+// Top the bit buffer up to more than 32 bits; past the stream's end the
+// stream reads as zeros.
+__device__ __forceinline__ void dec_refill(Dec& d) {
+    while (d.nbuf <= 32) {
+        uint32_t w = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w = (w << 8) | (d.left > (uint32_t)i ? (uint32_t)__ldg(d.p + i) : 0u);
+        d.p += 4;
+        d.left = d.left > 4 ? d.left - 4 : 0;
+        d.buf |= (uint64_t)w << (32 - d.nbuf);
+        d.nbuf += 32;
+    }
+}
+
+__device__ __forceinline__ uint32_t dec_take(Dec& d, uint32_t c) {   // 1 <= c <= 32
+    const uint32_t r = (uint32_t)(d.buf >> (64 - c));
+    d.buf <<= c;
+    d.nbuf -= c;
+    return r;
+}
+
+__device__ __forceinline__ void dec_init(Dec& d, const uint8_t* p, uint32_t len) {
+    d.low = 0;
+    d.high = 0xFFFFFFFFu;
+    d.p = p;
+    d.left = len;
+    d.buf = 0;
+    d.nbuf = 0;
+    dec_refill(d);
+    d.value = dec_take(d, 32);
+}
+
+// One symbol.  table[k * H] holds C[k] of this stream's channel for k < nsym
+// (C[nsym] = 2^16).  The symbol is the largest k with
+// floor(range * C[k] / 2^16) <= value - low: the interval the encoder chose.
+__device__ __forceinline__ uint32_t dec_symbol(Dec& d, const uint16_t* table, int H, int nsym) {
+    if (d.nbuf < 32) dec_refill(d);
+    const uint32_t v = d.value - d.low;
+    const uint32_t rm1 = d.high - d.low;
+    int s = 0;
+#pragma unroll
+    for (int step = 16; step >= 1; step >>= 1) {
+        const int cand = s + step;
+        if (cand < nsym) {
+            const uint32_t C = table[cand * H];
+            if ((uint32_t)(((uint64_t)rm1 * C + C) >> 16) <= v) s = cand;
+        }
+    }
+    const uint32_t lo = table[s * H];
+    const uint32_t hi = s + 1 < nsym ? (uint32_t)table[(s + 1) * H] : 65536u;
+    const uint64_t top = (uint64_t)rm1 * hi + hi;
+    const uint64_t bot = (uint64_t)rm1 * lo + lo;
+    d.high = d.low + (uint32_t)(top >> 16) - 1;
+    d.low = d.low + (uint32_t)(bot >> 16);
+    const uint32_t k = __clz(d.low ^ d.high);
+    if (k) {
+        d.value = (d.value << k) | dec_take(d, k);
+        d.low <<= k;
+        d.high = (d.high << k) | ((1u << k) - 1);
+    }
+    const uint32_t a = __clz(~(d.low << 1)), b = __clz(d.high << 1);
+    const uint32_t m = a < b ? a : b;
+    if (m) {
+        d.value = (d.value & kHalf) | ((d.value << m) & 0x7FFFFFFFu) | dec_take(d, m);
+        d.low = (d.low << m) & 0x7FFFFFFFu;
+        d.high = (d.high << m) | kHalf | ((1u << m) - 1);
+    }
+    return (uint32_t)s;
+}
+
+// Block-wide sum; every thread gets the result.  `red` holds >= 32 words.
+__device__ __forceinline__ uint64_t block_sum(uint64_t v, uint64_t* red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    uint64_t t = 0;
+    for (int w = 0; w < nw; ++w) t += red[w];
+    return t;
+}
+
+// Exclusive block-wide prefix sum of v (in thread order); `red` >= 32 words.
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+    uint32_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += y;
+    }
+    __syncthreads();
+    if (lane == 31) red[warp] = x;
+    __syncthreads();
+    uint32_t before = 0;
+    for (int w = 0; w < warp; ++w) before += red[w];
+    (void)nw;
+    return before + x - v;
+}
+
+// ---- encode 1: absmax, symbols, histogram, CDF ----
+// grid (2L, chunks), block = threads covering H / kStreams channel groups.
+// Shared memory: uint16 hist[kMaxSym][H].
+__global__ void __launch_bounds__(kMaxThreads) cg_cdf_kernel(const __grid_constant__ CgParams p) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ uint32_t part[2][kRows][kMaxThreads / 32];
+    const int s = blockIdx.x, gi = blockIdx.y;
+    const int n = p.ntok[gi], H = p.H, L = p.L;
+    const int bins = p.bins[s], MAX = bins / 2 - 1, nsym = 2 * MAX + 1;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = (blockDim.x + 31) >> 5;
+    const int c0 = tid * kStreams;
+    const bool active = c0 < H;
+    uint16_t* hist = reinterpret_cast<uint16_t*>(smem);
+
+    const uint8_t* chunk = p.chunk_ptrs[gi];
+    uint8_t* blob = p.blob_ptrs[gi];
+    if (chunk == nullptr || blob == nullptr) {
+        if (tid == 0) set_status(p.status, LMKV_ERR_BAD_POINTER);
+        return;
+    }
+    if (active)
+        for (int k = 0; k < nsym; ++k)
+            *reinterpret_cast<uint2*>(hist + k * H + c0) = make_uint2(0, 0);
+
+    const uint8_t* x = chunk + ((uint64_t)s * n * H + c0) * 2;
+    uint32_t* sym = reinterpret_cast<uint32_t*>(p.ws + p.sym_off[gi] + (uint64_t)s * n * H + c0);
+    float* max1_out = reinterpret_cast<float*>(blob) + (uint64_t)s * n;
+    const float maxf = (float)MAX;
+
+    for (int t0 = 0, buf = 0; t0 < n; t0 += kRows, buf ^= 1) {
+        uint2 v[kRows];
+#pragma unroll
+        for (int r = 0; r < kRows; ++r)
+            v[r] = (active && t0 + r < n) ? ld_nc_v2(x + (uint64_t)(t0 + r) * H * 2) : make_uint2(0, 0);
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+            const uint32_t a = abs_max_bits(v[r].x), b = abs_max_bits(v[r].y);
+            const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, a > b ? a : b);
+            if (lane == 0) part[buf][r][warp] = m;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+            const int t = t0 + r;
+            if (t >= n) break;
+            uint32_t mb = 0;
+            for (int w = 0; w < nw; ++w) mb = mb > part[buf][r][w] ? mb : part[buf][r][w];
+            const float m = __uint_as_float(mb);
+            if (tid == r) max1_out[t] = m;
+            if (!active) continue;
+            uint32_t q0, q1, q2, q3;
+            if (m == 0.0f) {
+                q0 = q1 = q2 = q3 = (uint32_t)MAX;
+            } else {
+                const float factor = __fdiv_rn(maxf, m);
+                q0 = quantise(bf16_lo(v[r].x), factor, maxf, 2 * MAX);
+                q1 = quantise(bf16_hi(v[r].x), factor, maxf, 2 * MAX);
+                q2 = quantise(bf16_lo(v[r].y), factor, maxf, 2 * MAX);
+                q3 = quantise(bf16_hi(v[r].y), factor, maxf, 2 * MAX);
+            }
+            sym[(uint64_t)t * (H / 4)] = q0 | (q1 << 8) | (q2 << 16) | (q3 << 24);
+            hist[q0 * H + c0 + 0] += 1;
+            hist[q1 * H + c0 + 1] += 1;
+            hist[q2 * H + c0 + 2] += 1;
+            hist[q3 * H + c0 + 3] += 1;
+        }
+    }
+    if (!active) return;
+    // C[k] = round(cum[k] * (2^16 - (Lp - 1)) / n) + k, ties to even; the
+    // blob keeps C[1..nsym-1] per channel.
+    const uint32_t M = 65536u - (uint32_t)nsym;
+    uint16_t* cdf = reinterpret_cast<uint16_t*>(blob + cdf_offset(L, n)) + p.cdf_prefix[s] +
+                    (uint64_t)c0 * (nsym - 1);
+#pragma unroll
+    for (int j = 0; j < kStreams; ++j) {
+        uint32_t cum = 0;
+        for (int k = 0; k < nsym; ++k) {
+            const uint32_t num = cum * M;
+            uint32_t q = num / (uint32_t)n;
+            const uint32_t r = num - q * (uint32_t)n;
+            if (2 * r > (uint32_t)n || (2 * r == (uint32_t)n && (q & 1))) ++q;
+            if (k > 0) cdf[j * (nsym - 1) + k - 1] = (uint16_t)(q + k);
+            cum += hist[k * H + c0 + j];
+        }
+    }
+}
+
+// Load one slice's CDF table from the blob into shared memory:
+// table[k * H + c] = C[k] for k < nsym (C[0] = 0).
+__device__ __forceinline__ void load_table(uint16_t* table, const uint8_t* blob, const CgParams& p,
+                                           int s, int n, int nsym, int c0, bool active) {
+    if (!active) return;
+    const int H = p.H;
+    const uint16_t* src = reinterpret_cast<const uint16_t*>(blob + cdf_offset(p.L, n)) +
+                          p.cdf_prefix[s] + (uint64_t)c0 * (nsym - 1);
+#pragma unroll
+    for (int j = 0; j < kStreams; ++j) {
+        table[c0 + j] = 0;
+        for (int k = 1; k < nsym; ++k) table[k * H + c0 + j] = src[j * (nsym - 1) + k - 1];
+    }
+}
+
+// ---- encode 2: one CTA per (chunk, batch, kv, layer) region ----
+// grid (nb_max * 2L, chunks).  Shared memory: uint16 table[kMaxSym][H].
+__global__ void __launch_bounds__(kMaxThreads) cg_code_kernel(const __grid_constant__ CgParams p) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ uint64_t red[32];
+    const int gi = blockIdx.y, n = p.ntok[gi], H = p.H, L = p.L;
+    const int region = blockIdx.x, b = region / (2 * L), s = region % (2 * L);
+    if (b >= batches_of(n)) return;
+    const int nsym = nsym_of(p.bins[s]);
+    const int t0 = b * kBatch, nt = n - t0 < kBatch ? n - t0 : kBatch;
+    const int tid = threadIdx.x, c0 = tid * kStreams;
+    const bool active = c0 < H;
+    uint8_t* blob = p.blob_ptrs[gi];
+    if (p.chunk_ptrs[gi] == nullptr || blob == nullptr) return;   // reported by the CDF kernel
+    uint16_t* table = reinterpret_cast<uint16_t*>(smem);
+    load_table(table, blob, p, s, n, nsym, c0, active);
+    __syncthreads();
+
+    const uint64_t stride = slot_stride(n);
+    const uint32_t cap_words = (uint32_t)(stride / 4);
+    uint32_t len[kStreams] = {0, 0, 0, 0};
+    bool overflow = false;
+    if (active) {
+        uint32_t* slot[kStreams];
+        Enc e[kStreams];
+#pragma unroll
+        for (int j = 0; j < kStreams; ++j) {
+            slot[j] = reinterpret_cast<uint32_t*>(p.ws + p.slot_off[gi] +
+                                                  ((uint64_t)region * H + c0 + j) * stride);
+            enc_init(e[j]);
+        }
+        const uint32_t* sym = reinterpret_cast<const uint32_t*>(p.ws + p.sym_off[gi] +
+                                                                ((uint64_t)s * n + t0) * H + c0);
+        const int hw = H / 4;
+        uint32_t w_next = sym[0];
+        for (int t = 0; t < nt; ++t) {
+            const uint32_t w = w_next;
+            if (t + 1 < nt) w_next = sym[(uint64_t)(t + 1) * hw];
+#pragma unroll
+            for (int j = 0; j < kStreams; ++j) {
+                const uint32_t q = (w >> (8 * j)) & 0xFFu;
+                const uint32_t lo = table[q * H + c0 + j];
+                const uint32_t hi = (int)q + 1 < nsym ? (uint32_t)table[(q + 1) * H + c0 + j] : 65536u;
+                enc_symbol(e[j], lo, hi, slot[j], cap_words, overflow);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kStreams; ++j) {
+            len[j] = enc_finish(e[j], slot[j], cap_words, overflow);
+            // never past the slot (excluded by the bound; keeps the blob in bounds)
+            len[j] = len[j] < cap_words * 4 ? len[j] : cap_words * 4;
+        }
+        uint32_t* lengths = reinterpret_cast<uint32_t*>(blob + lengths_offset(L, n, p.cdf_entries)) +
+                            (uint64_t)region * H + c0;
+#pragma unroll
+        for (int j = 0; j < kStreams; ++j) lengths[j] = len[j];
+    }
+    if (overflow) set_status(p.status, LMKV_ERR_SCRATCH_LIMIT);   // excluded by the bound
+    const uint64_t total = block_sum((uint64_t)len[0] + len[1] + len[2] + len[3], red);
+    if (tid == 0)
+        reinterpret_cast<uint32_t*>(p.ws + p.tot_off[gi])[region] = (uint32_t)total;
+}
+
+// Byte offset of region `region` within the chunk's streams, and the total
+// of all regions (both from the per-region totals).
+__device__ __forceinline__ void region_base(const uint32_t* totals, int region, int nregions,
+                                            uint64_t* red, uint64_t* before, uint64_t* all) {
+    uint64_t a = 0, c = 0;
+    for (int i = threadIdx.x; i < nregions; i += blockDim.x) {
+        const uint64_t v = totals[i];
+        c += v;
+        if (i < region) a += v;
+    }
+    *before = block_sum(a, red);
+    *all = block_sum(c, red);
+}
+
+// ---- encode 3: place every stream at its prefix-sum offset ----
+// grid (nb_max * 2L, chunks), block as the coder.
+__global__ void __launch_bounds__(kMaxThreads) cg_compact_kernel(const __grid_constant__ CgParams p) {
+    __shared__ uint64_t red[32];
+    __shared__ uint32_t sred[32];
+    extern __shared__ __align__(16) uint8_t smem[];
+    uint32_t* off = reinterpret_cast<uint32_t*>(smem);           // [H] offset within the region
+    uint32_t* lens = off + p.H;                                   // [H]
+    const int gi = blockIdx.y, n = p.ntok[gi], H = p.H, L = p.L;
+    const int region = blockIdx.x, b = region / (2 * L);
+    const int nb = batches_of(n), nregions = nb * 2 * L;
+    if (b >= nb) return;
+    uint8_t* blob = p.blob_ptrs[gi];
+    if (p.chunk_ptrs[gi] == nullptr || blob == nullptr) return;
+    const int tid = threadIdx.x, c0 = tid * kStreams;
+    const bool active = c0 < H;
+    const uint32_t* totals = reinterpret_cast<const uint32_t*>(p.ws + p.tot_off[gi]);
+    uint64_t before, all;
+    region_base(totals, region, nregions, red, &before, &all);
+    const uint64_t bytes0 = bytes_offset(L, n, H, p.cdf_entries);
+    if (region == 0 && tid == 0) p.sizes[gi] = bytes0 + all;
+
+    const uint32_t* lengths = reinterpret_cast<const uint32_t*>(blob + lengths_offset(L, n, p.cdf_entries)) +
+                              (uint64_t)region * H;
+    uint32_t l[kStreams] = {0, 0, 0, 0};
+    if (active)
+#pragma unroll
+        for (int j = 0; j < kStreams; ++j) l[j] = lengths[c0 + j];
+    uint32_t o = block_exclusive_scan(l[0] + l[1] + l[2] + l[3], sred);
+    if (active)
+#pragma unroll
+        for (int j = 0; j < kStreams; ++j) {
+            off[c0 + j] = o;
+            lens[c0 + j] = l[j];
+            o += l[j];
+        }
+    __syncthreads();
+    // one warp per stream, lanes on consecutive bytes
+    const int lane = tid & 31, warp = tid >> 5, nw = (blockDim.x + 31) >> 5;
+    const uint64_t stride = slot_stride(n);
+    uint8_t* dst0 = blob + bytes0 + before;
+    const uint8_t* src0 = p.ws + p.slot_off[gi] + (uint64_t)region * H * stride;
+    for (int c = warp; c < H; c += nw) {
+        const uint32_t nbytes = lens[c];
+        const uint8_t* src = src0 + (uint64_t)c * stride;
+        uint8_t* dst = dst0 + off[c];
+        for (uint32_t i = lane; i < nbytes; i += 32) dst[i] = src[i];
+    }
+}
+
+// ---- decode 1: per-region totals of the stream lengths ----
+// grid (nb_max * 2L, chunks), 256 threads.
+__global__ void __launch_bounds__(256) cg_total_kernel(const __grid_constant__ CgParams p) {
+    __shared__ uint64_t red[32];
+    const int gi = blockIdx.y, n = p.ntok[gi], H = p.H, L = p.L;
+    const int region = blockIdx.x;
+    if (region / (2 * L) >= batches_of(n)) return;
+    const uint8_t* blob = p.blob_ptrs[gi];
+    if (blob == nullptr || p.chunk_ptrs[gi] == nullptr) {
+        if (region == 0 && threadIdx.x == 0) set_status(p.status, LMKV_ERR_BAD_POINTER);
+        return;
+    }
+    const uint32_t* lengths = reinterpret_cast<const uint32_t*>(blob + lengths_offset(L, n, p.cdf_entries)) +
+                              (uint64_t)region * H;
+    uint64_t a = 0;
+    for (int c = threadIdx.x; c < H; c += blockDim.x) a += lengths[c];
+    a = block_sum(a, red);
+    if (threadIdx.x == 0) {
+        // a region total above its streams' bound cannot come from the encoder
+        const int nt = n - (region / (2 * L)) * kBatch;
+        const uint64_t cap = (uint64_t)H * stream_bound(nt < kBatch ? nt : kBatch);
+        reinterpret_cast<uint32_t*>(p.ws + p.tot_off[gi])[region] = a > cap ? 0xFFFFFFFFu : (uint32_t)a;
+    }
+}
+
+// ---- decode 2: one CTA per (chunk, batch, kv, layer) region ----
+// grid (nb_max * 2L, chunks).  Shared memory: uint16 table[kMaxSym][H].
+__global__ void __launch_bounds__(kMaxThreads) cg_decode_kernel(const __grid_constant__ CgParams p) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ uint64_t red[32];
+    __shared__ uint32_t sred[32];
+    __shared__ float deq[32];
+    __shared__ float max1s[kBatch];
+    const int gi = blockIdx.y, n = p.ntok[gi], H = p.H, L = p.L;
+    const int region = blockIdx.x, b = region / (2 * L), s = region % (2 * L);
+    const int nb = batches_of(n), nregions = nb * 2 * L;
+    if (b >= nb) return;
+    const uint8_t* blob = p.blob_ptrs[gi];
+    uint8_t* chunk = const_cast<uint8_t*>(p.chunk_ptrs[gi]);
+    if (blob == nullptr || chunk == nullptr) return;   // reported by the totals kernel
+    const int tid = threadIdx.x, c0 = tid * kStreams;
+    const bool active = c0 < H;
+    const int bins = p.bins[s], MAX = bins / 2 - 1, nsym = 2 * MAX + 1;
+    const int t0 = b * kBatch, nt = n - t0 < kBatch ? n - t0 : kBatch;
+
+    uint64_t before, all;
+    region_base(reinterpret_cast<const uint32_t*>(p.ws + p.tot_off[gi]), region, nregions, red,
+                &before, &all);
+    const uint64_t bytes0 = bytes_offset(L, n, H, p.cdf_entries);
+    if (bytes0 + all != p.sizes[gi]) {          // the lengths do not add up to the blob
+        if (tid == 0) set_status(p.status, LMKV_ERR_BAD_DATA);
+        return;
+    }
+    uint16_t* table = reinterpret_cast<uint16_t*>(smem);
+    load_table(table, blob, p, s, n, nsym, c0, active);
+    if (tid < nsym) deq[tid] = __fdiv_rn((float)(tid - MAX), (float)MAX);
+    const float* max1 = reinterpret_cast<const float*>(blob) + (uint64_t)s * n + t0;
+    for (int t = tid; t < nt; t += blockDim.x) max1s[t] = max1[t];
+
+    const uint32_t* lengths = reinterpret_cast<const uint32_t*>(blob + lengths_offset(L, n, p.cdf_entries)) +
+                              (uint64_t)region * H;
+    uint32_t l[kStreams] = {0, 0, 0, 0};
+    if (active)
+#pragma unroll
+        for (int j = 0; j < kStreams; ++j) l[j] = lengths[c0 + j];
+    const uint32_t o = block_exclusive_scan(l[0] + l[1] + l[2] + l[3], sred);   // syncs the block
+    __syncthreads();
+    if (!active) return;
+    const uint64_t bound = stream_bound(nt);
+    bool bad = false;
+#pragma unroll
+    for (int j = 0; j < kStreams; ++j) bad |= l[j] > bound;
+    if (bad) {
+        set_status(p.status, LMKV_ERR_BAD_DATA);
+        return;
+    }
+    Dec d[kStreams];
+    const uint8_t* src = blob + bytes0 + before + o;
+#pragma unroll
+    for (int j = 0; j < kStreams; ++j) {
+        dec_init(d[j], src, l[j]);
+        src += l[j];
+    }
+    uint8_t* out = chunk + (((uint64_t)s * n + t0) * H + c0) * 2;
+    for (int t = 0; t < nt; ++t) {
+        const float m = max1s[t];
+        float y[kStreams];
+#pragma unroll
+        for (int j = 0; j < kStreams; ++j) {
+            const uint32_t q = dec_symbol(d[j], table + c0 + j, H, nsym);
+            y[j] = __fmul_rn(deq[q], m);
+        }
+        const __nv_bfloat162 a = __floats2bfloat162_rn(y[0], y[1]);
+        const __nv_bfloat162 c = __floats2bfloat162_rn(y[2], y[3]);
+        uint2 v;
+        v.x = *reinterpret_cast<const uint32_t*>(&a);
+        v.y = *reinterpret_cast<const uint32_t*>(&c);
+        *reinterpret_cast<uint2*>(out + (uint64_t)t * H * 2) = v;
+    }
+}
+
+// ---- host side ----
+
+int check_shape(int32_t L, int32_t H, const int32_t* bins, int32_t* cdf_prefix, int32_t* cdf_entries,
+                int* max_nsym) {
+    if (L < 1 || L > LMKV_CACHEGEN_MAX_LAYERS || H < 4 || H > LMKV_CACHEGEN_MAX_CHANNELS || H % 4 != 0 ||
+        bins == nullptr)
+        return LMKV_ERR_INVALID_ARG;
+    int64_t e = 0;
+    int mx = 0;
+    for (int s = 0; s < 2 * L; ++s) {
+        if (bins[s] < 4 || bins[s] > 32) return LMKV_ERR_INVALID_ARG;
+        if (cdf_prefix) cdf_prefix[s] = (int32_t)e;
+        e += (int64_t)H * (nsym_of(bins[s]) - 1);
+        mx = nsym_of(bins[s]) > mx ? nsym_of(bins[s]) : mx;
+    }
+    if (cdf_entries) *cdf_entries = (int32_t)e;
+    if (max_nsym) *max_nsym = mx;
+    return LMKV_OK;
+}
+
+// Workspace of one chunk: [totals | symbols | slots], each 256-byte aligned.
+struct ChunkWs {
+    uint64_t tot, sym, slot, end;
+};
+
+ChunkWs chunk_ws(uint64_t at, int L, int H, int n) {
+    auto up = [](uint64_t v) { return (v + 255) & ~255ull; };
+    const uint64_t nregions = (uint64_t)batches_of(n) * 2 * L;
+    ChunkWs w;
+    w.tot = up(at);
+    w.sym = up(w.tot + 4 * nregions);
+    w.slot = up(w.sym + 2ull * L * n * H);
+    w.end = w.slot + nregions * H * slot_stride(n);
+    return w;
+}
+
+int workspace_size(int32_t L, int32_t H, const int32_t* ntok, int32_t num_chunks, uint64_t* out) {
+    if (num_chunks < 0 || (num_chunks > 0 && ntok == nullptr)) return LMKV_ERR_INVALID_ARG;
+    uint64_t at = 0;
+    for (int32_t g = 0; g < num_chunks; ++g) {
+        if (ntok[g] < 1 || ntok[g] > LMKV_CACHEGEN_MAX_TOKENS) return LMKV_ERR_INVALID_ARG;
+        at = chunk_ws(at, L, H, ntok[g]).end;
+    }
+    *out = at;
+    return LMKV_OK;
+}
+
+int threads_for(int H) { return ((H / kStreams + 31) / 32) * 32; }
+
+int set_smem(const void* fn, size_t bytes) {
+    if (bytes <= 48 * 1024) return LMKV_OK;
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) == cudaSuccess
+               ? LMKV_OK : LMKV_ERR_CUDA;
+}
+
+enum class Dir { kEncode, kDecode };
+
+int run(Dir dir, void* const* chunk_ptrs, void* const* blob_ptrs, uint64_t* sizes, const int32_t* ntok,
+        int32_t num_chunks, int32_t L, int32_t H, const int32_t* bins, void* workspace,
+        uint64_t workspace_bytes, int32_t* d_status, void* stream) {
+    CgParams p{};
+    int max_nsym = 0;
+    int rc = check_shape(L, H, bins, p.cdf_prefix, &p.cdf_entries, &max_nsym);
+    if (rc != LMKV_OK) return rc;
+    if (num_chunks < 0) return LMKV_ERR_INVALID_ARG;
+    if (num_chunks == 0) return LMKV_OK;
+    if (chunk_ptrs == nullptr || blob_ptrs == nullptr || sizes == nullptr || ntok == nullptr ||
+        workspace == nullptr)
+        return LMKV_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return LMKV_ERR_MISALIGNED;
+    uint64_t need = 0;
+    rc = workspace_size(L, H, ntok, num_chunks, &need);
+    if (rc != LMKV_OK) return rc;
+    if (need > workspace_bytes) return LMKV_ERR_INVALID_ARG;
+    for (int s = 0; s < 2 * L; ++s) p.bins[s] = (uint8_t)bins[s];
+    p.L = L;
+    p.H = H;
+    p.status = d_status;
+    p.ws = static_cast<uint8_t*>(workspace);
+    const int threads = threads_for(H);
+    const size_t table_bytes = (size_t)max_nsym * H * 2;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dir == Dir::kEncode) {
+        if (set_smem((const void*)cg_cdf_kernel, table_bytes) != LMKV_OK ||
+            set_smem((const void*)cg_code_kernel, table_bytes) != LMKV_OK)
+            return LMKV_ERR_CUDA;
+    } else if (set_smem((const void*)cg_decode_kernel, table_bytes) != LMKV_OK) {
+        return LMKV_ERR_CUDA;
+    }
+    uint64_t at = 0;
+    for (int32_t g0 = 0; g0 < num_chunks; g0 += kMaxChunks) {
+        const int cnt = num_chunks - g0 < kMaxChunks ? num_chunks - g0 : kMaxChunks;
+        int nb_max = 0;
+        for (int i = 0; i < cnt; ++i) {
+            const int n = ntok[g0 + i];
+            const ChunkWs w = chunk_ws(at, L, H, n);
+            p.ntok[i] = n;
+            p.tot_off[i] = w.tot;
+            p.sym_off[i] = w.sym;
+            p.slot_off[i] = w.slot;
+            at = w.end;
+            nb_max = batches_of(n) > nb_max ? batches_of(n) : nb_max;
+        }
+        p.nchunks = cnt;
+        p.chunk_ptrs = reinterpret_cast<const uint8_t* const*>(chunk_ptrs) + g0;
+        p.blob_ptrs = reinterpret_cast<uint8_t* const*>(blob_ptrs) + g0;
+        p.sizes = sizes + g0;
+        const dim3 slices(2 * L, cnt), regions(nb_max * 2 * L, cnt);
+        if (dir == Dir::kEncode) {
+            cg_cdf_kernel<<<slices, threads, table_bytes, st>>>(p);
+            cg_code_kernel<<<regions, threads, table_bytes, st>>>(p);
+            cg_compact_kernel<<<regions, threads, (size_t)H * 8, st>>>(p);
+            lmkv_internal_add_launches(3);
+        } else {
+            cg_total_kernel<<<regions, 256, 0, st>>>(p);
+            cg_decode_kernel<<<regions, threads, table_bytes, st>>>(p);
+            lmkv_internal_add_launches(2);
+        }
+        if (cudaGetLastError() != cudaSuccess) return LMKV_ERR_CUDA;
+    }
+    return LMKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int lmkv_cachegen_default_bins(int32_t num_layers, int32_t* bins) {
+    if (num_layers < 1 || num_layers > LMKV_CACHEGEN_MAX_LAYERS || bins == nullptr) return LMKV_ERR_INVALID_ARG;
+    const bool all32 = num_layers < 10;
+    for (int32_t l = 0; l < num_layers; ++l) {
+        bins[l] = (all32 || l < 10) ? 32 : 16;
+        bins[num_layers + l] = (all32 || l < 2) ? 32 : 16;
+    }
+    return LMKV_OK;
+}
+
+int lmkv_cachegen_layout(int32_t num_layers, int32_t num_tokens, int32_t channels, const int32_t* bins,
+                         lmkv_cachegen_layout_t* out) {
+    int32_t entries = 0;
+    const int rc = check_shape(num_layers, channels, bins, nullptr, &entries, nullptr);
+    if (rc != LMKV_OK) return rc;
+    if (out == nullptr || num_tokens < 1 || num_tokens > LMKV_CACHEGEN_MAX_TOKENS) return LMKV_ERR_INVALID_ARG;
+    out->max1_offset = 0;
+    out->cdf_offset = cdf_offset(num_layers, num_tokens);
+    out->lengths_offset = lengths_offset(num_layers, num_tokens, entries);
+    out->bytes_offset = bytes_offset(num_layers, num_tokens, channels, entries);
+    uint64_t bound = out->bytes_offset;
+    for (int t0 = 0; t0 < num_tokens; t0 += kBatch) {
+        const int nt = num_tokens - t0 < kBatch ? num_tokens - t0 : kBatch;
+        bound += 2ull * num_layers * channels * stream_bound(nt);
+    }
+    out->max_bytes = bound;
+    return LMKV_OK;
+}
+
+int lmkv_cachegen_workspace_bytes(int32_t num_layers, int32_t channels, const int32_t* num_tokens,
+                                  int32_t num_chunks, uint64_t* bytes) {
+    if (bytes == nullptr || num_layers < 1 || num_layers > LMKV_CACHEGEN_MAX_LAYERS || channels < 4 ||
+        channels > LMKV_CACHEGEN_MAX_CHANNELS || channels % 4 != 0)
+        return LMKV_ERR_INVALID_ARG;
+    return workspace_size(num_layers, channels, num_tokens, num_chunks, bytes);
+}
+
+int lmkv_cachegen_encode(void* const* chunk_ptrs, const int32_t* num_tokens, int32_t num_chunks,
+                         int32_t num_layers, int32_t channels, const int32_t* bins,
+                         void* const* blob_ptrs, uint64_t* sizes, void* workspace,
+                         uint64_t workspace_bytes, int32_t* d_status, void* stream) {
+    return run(Dir::kEncode, chunk_ptrs, blob_ptrs, sizes, num_tokens, num_chunks, num_layers, channels,
+               bins, workspace, workspace_bytes, d_status, stream);
+}
+
+int lmkv_cachegen_decode(void* const* blob_ptrs, const uint64_t* sizes, const int32_t* num_tokens,
+                         int32_t num_chunks, int32_t num_layers, int32_t channels,
+                         const int32_t* bins, void* const* chunk_ptrs, void* workspace,
+                         uint64_t workspace_bytes, int32_t* d_status, void* stream) {
+    return run(Dir::kDecode, chunk_ptrs, blob_ptrs, const_cast<uint64_t*>(sizes), num_tokens, num_chunks,
+               num_layers, channels, bins, workspace, workspace_bytes, d_status, stream);
+}
+
+}  // extern "C"

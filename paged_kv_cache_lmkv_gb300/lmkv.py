@@ -27,7 +27,12 @@ ERR_BAD_BLOCK = 5
 ERR_BAD_POINTER = 6
 ERR_TIMEOUT = 7
 ERR_SCRATCH_LIMIT = 8
+ERR_BAD_DATA = 9
 NOALLOC_STAGING_BYTES = 64 << 20
+CACHEGEN_BATCH = 256
+CACHEGEN_MAX_CHANNELS = 2048
+CACHEGEN_MAX_TOKENS = 4096
+CACHEGEN_MAX_LAYERS = 128
 
 ENTRY_POINTS = (
     "lmkv_count_chunks", "lmkv_enumerate_chunks", "lmkv_gather_chunks", "lmkv_scatter_chunks",
@@ -37,7 +42,8 @@ ENTRY_POINTS = (
     "lmkv_store_layers_staged", "lmkv_retrieve_layers_staged",
     "lmkv_store_layers_staged_noalloc", "lmkv_decode_store_ranges",
     "lmkv_offload_init", "lmkv_offload_plan", "lmkv_offload_copied", "lmkv_offload_allocate",
-    "lmkv_offload_add_free",
+    "lmkv_offload_add_free", "lmkv_cachegen_default_bins", "lmkv_cachegen_layout",
+    "lmkv_cachegen_workspace_bytes", "lmkv_cachegen_encode", "lmkv_cachegen_decode",
 )
 
 
@@ -54,6 +60,13 @@ class OffloadState(ctypes.Structure):
 
     def as_tuple(self):
         return (self.start, self.current, self.end, self.limit, self.window)
+
+
+class CachegenLayout(ctypes.Structure):
+    """lmkv_cachegen_layout_t: byte offsets of one chunk's encoded blob."""
+    _fields_ = [("max1_offset", ctypes.c_uint64), ("cdf_offset", ctypes.c_uint64),
+                ("lengths_offset", ctypes.c_uint64), ("bytes_offset", ctypes.c_uint64),
+                ("max_bytes", ctypes.c_uint64)]
 
 
 class _PoolT(ctypes.Structure):
@@ -110,7 +123,14 @@ def load() -> ctypes.CDLL:
         fp8 = [pool_p, P, i32, P, P, i32, i32, i32, P, P, P, P]
         lib.lmkv_gather_chunks_fp8e4m3.argtypes = fp8
         lib.lmkv_scatter_chunks_fp8e4m3.argtypes = fp8
+        lib.lmkv_cachegen_default_bins.argtypes = [i32, P]
+        lib.lmkv_cachegen_layout.argtypes = [i32, i32, i32, P, ctypes.POINTER(CachegenLayout)]
+        lib.lmkv_cachegen_workspace_bytes.argtypes = [i32, i32, P, i32, P]
+        lib.lmkv_cachegen_encode.argtypes = [P, P, i32, i32, i32, P, P, P, P, ctypes.c_uint64, P, P]
+        lib.lmkv_cachegen_decode.argtypes = [P, P, P, i32, i32, i32, P, P, P, ctypes.c_uint64, P, P]
         for name in ("lmkv_count_chunks", "lmkv_enumerate_chunks", "lmkv_gather_chunks",
+                     "lmkv_cachegen_default_bins", "lmkv_cachegen_layout",
+                     "lmkv_cachegen_workspace_bytes", "lmkv_cachegen_encode", "lmkv_cachegen_decode",
                      "lmkv_decode_store_ranges", "lmkv_offload_init", "lmkv_offload_plan",
                      "lmkv_offload_copied", "lmkv_offload_allocate", "lmkv_offload_add_free",
                      "lmkv_scatter_chunks", "lmkv_gather_layer", "lmkv_scatter_layer",
@@ -405,6 +425,100 @@ def store_layers_staged_noalloc(pool, block_table, start, end, chunk_size, save_
     return load().lmkv_store_layers_staged_noalloc(*a, chunk_size, int(save_unfull), h,
                                                    int(layer_lo), int(layer_n), r, d,
                                                    _ptr(status), _stream_handle(stream))
+
+
+# ---- CacheGen codec ----
+
+def _i32_array(values) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(values).reshape(-1), dtype=np.int32)
+
+
+def cachegen_default_bins(num_layers: int) -> np.ndarray:
+    """int32 [2][num_layers] bins (row 0 K, row 1 V)."""
+    out = np.zeros(2 * num_layers, np.int32)
+    check(load().lmkv_cachegen_default_bins(num_layers, out.ctypes.data), "lmkv_cachegen_default_bins")
+    return out.reshape(2, num_layers)
+
+
+def cachegen_layout(num_layers: int, num_tokens: int, channels: int, bins) -> CachegenLayout:
+    b = _i32_array(bins)
+    out = CachegenLayout()
+    check(load().lmkv_cachegen_layout(num_layers, num_tokens, channels, b.ctypes.data,
+                                      ctypes.byref(out)), "lmkv_cachegen_layout")
+    return out
+
+
+def cachegen_workspace_bytes(num_layers: int, channels: int, num_tokens) -> int:
+    n = _i32_array(num_tokens)
+    out = ctypes.c_uint64(0)
+    check(load().lmkv_cachegen_workspace_bytes(num_layers, channels, n.ctypes.data, len(n),
+                                               ctypes.byref(out)), "lmkv_cachegen_workspace_bytes")
+    return out.value
+
+
+def cachegen_encode(chunk_ptrs, num_tokens, num_layers, channels, bins, blob_ptrs, sizes,
+                    workspace, status=None, stream=None) -> int:
+    """chunk_ptrs / blob_ptrs: DEVICE int64 pointer arrays; sizes: DEVICE uint64
+    (int64 tensor) [num_chunks]; workspace: a DEVICE uint8 tensor."""
+    n, b = _i32_array(num_tokens), _i32_array(bins)
+    return load().lmkv_cachegen_encode(_ptr(chunk_ptrs), n.ctypes.data, len(n), num_layers, channels,
+                                       b.ctypes.data, _ptr(blob_ptrs), _ptr(sizes), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _ptr(status),
+                                       _stream_handle(stream))
+
+
+def cachegen_decode(blob_ptrs, sizes, num_tokens, num_layers, channels, bins, chunk_ptrs,
+                    workspace, status=None, stream=None) -> int:
+    n, b = _i32_array(num_tokens), _i32_array(bins)
+    return load().lmkv_cachegen_decode(_ptr(blob_ptrs), _ptr(sizes), n.ctypes.data, len(n), num_layers,
+                                       channels, b.ctypes.data, _ptr(chunk_ptrs), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _ptr(status),
+                                       _stream_handle(stream))
+
+
+class CachegenCodec:
+    """Chunk buffers [2][L][n][H] bf16 <-> CacheGen blobs, through
+    lmkv_cachegen_encode / lmkv_cachegen_decode.  Holds the bins and a device
+    workspace that grows to the largest batch seen (PyTorch memory)."""
+
+    def __init__(self, num_layers: int, channels: int, bins=None, device="cuda"):
+        self.num_layers, self.channels = num_layers, channels
+        self.bins = _i32_array(cachegen_default_bins(num_layers) if bins is None else bins)
+        self.device = torch.device(device)
+        self.workspace = torch.empty(0, dtype=torch.uint8, device=self.device)
+
+    def layout(self, num_tokens: int) -> CachegenLayout:
+        return cachegen_layout(self.num_layers, num_tokens, self.channels, self.bins)
+
+    def _workspace(self, ntok):
+        need = cachegen_workspace_bytes(self.num_layers, self.channels, ntok)
+        if self.workspace.numel() < need:
+            self.workspace = torch.empty(need, dtype=torch.uint8, device=self.device)
+        return self.workspace
+
+    def encode(self, chunks, blobs=None, sizes=None, status=None, stream=None):
+        """Encode the chunk tensors; returns (blobs, sizes): device uint8 tensors
+        of each layout's max_bytes and a device int64 tensor of the sizes."""
+        ntok = [int(c.shape[2]) for c in chunks]
+        if blobs is None:
+            blobs = [torch.empty(self.layout(n).max_bytes, dtype=torch.uint8, device=self.device)
+                     for n in ntok]
+        if sizes is None:
+            sizes = torch.zeros(len(chunks), dtype=torch.int64, device=self.device)
+        ws = self._workspace(ntok)
+        check(cachegen_encode(pointer_array(chunks, self.device), ntok, self.num_layers, self.channels,
+                              self.bins, pointer_array(blobs, self.device), sizes, ws, status, stream),
+              "lmkv_cachegen_encode")
+        return blobs, sizes
+
+    def decode(self, blobs, sizes, chunks, status=None, stream=None):
+        """Decode into the chunk tensors (their token counts give n)."""
+        ntok = [int(c.shape[2]) for c in chunks]
+        ws = self._workspace(ntok)
+        check(cachegen_decode(pointer_array(blobs, self.device), sizes, ntok, self.num_layers,
+                              self.channels, self.bins, pointer_array(chunks, self.device), ws, status,
+                              stream), "lmkv_cachegen_decode")
+        return chunks
 
 
 def check(rc: int, what: str = "lmkv") -> None:

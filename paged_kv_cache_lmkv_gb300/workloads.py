@@ -195,3 +195,34 @@ def make_pool(w: Workload, device, seed: int | None, fill: str = "normal") -> li
             for kv in range(2):
                 apply_outliers_(t, kv, ch[kv, l])
     return layers
+
+
+# CacheGen codec inputs: the page's benchmark ("LMCache 中的 KV Cache 压缩：CacheGen
+# 编解码原理、配置方式与源码解析", section on verifying the compression) builds
+# synthetic bf16 KV of 32 layers x 8 KV heads x head_size 128 and sweeps the
+# chunk size over 64, 128, 256 and 768 tokens.
+CACHEGEN_LAYERS = 32
+CACHEGEN_CHANNELS = 8 * 128
+CACHEGEN_CHUNK_SIZES = (64, 128, 256, 768)
+
+
+def cachegen_chunks(num_layers: int, channels: int, ntoks, seed: int, device="cpu",
+                    outliers: bool = False, zero_rows: int = 0) -> list:
+    """Chunk buffers [2][L][n][H] bf16 ~ N(0, 1), one per entry of ntoks, drawn
+    on the CPU from a seeded generator (so every device sees the same values),
+    optionally with 1% of each (K/V, layer)'s channels scaled x20 and the
+    first `zero_rows` token rows of every slice set to zero."""
+    g = generator("cpu", seed)
+    out = []
+    for n in ntoks:
+        x = torch.randn((2, num_layers, n, channels), generator=g, dtype=torch.float32)
+        if outliers:
+            k = max(1, round(0.01 * channels))
+            for kv in range(2):
+                for l in range(num_layers):
+                    idx = torch.randperm(channels, generator=g)[:k]
+                    x[kv, l, :, idx] *= 20.0
+        if zero_rows:
+            x[:, :, :zero_rows] = 0
+        out.append(x.to(torch.bfloat16).to(device))
+    return out

@@ -34,7 +34,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_abi_version_and_status_strings(lib):
     assert lib.lmkv_abi_version() == 1
-    for code in range(8):
+    for code in range(10):
         assert lmkv.status_string(code) != "unknown status"
     assert lmkv.status_string(99) == "unknown status"
 
@@ -142,3 +142,54 @@ def test_staged_pipeline_host_validation(lib):
         assert args(0x70008, need) == lmkv.ERR_MISALIGNED              # misaligned staging
         assert args(0x70000, need, 3, 2) == lmkv.ERR_INVALID_ARG       # layers out of range
         assert args(0x70000, need, 1, 0) == lmkv.OK                    # nothing to do
+
+
+class FakeWorkspace(FakeTensor):
+    def __init__(self, nbytes, ptr=0x50000):
+        super().__init__(ptr)
+        self.nbytes = nbytes
+
+    def numel(self):
+        return self.nbytes
+
+    def element_size(self):
+        return 1
+
+
+def test_cachegen_layout_agrees_with_the_oracle(lib):
+    """Two independent implementations of the blob layout (the library's and
+    the oracle's) give the same offsets and bound, and the same bins rule."""
+    from oracle import cachegen as cg
+    for L in (1, 3, 9, 10, 11, 32, 80):
+        assert lmkv.cachegen_default_bins(L).tolist() == cg.default_bins(L).tolist()
+    for L, n, H in [(1, 1, 4), (2, 300, 40), (32, 256, 1024), (32, 768, 1024), (80, 4096, 2048)]:
+        bins = cg.default_bins(L)
+        a = lmkv.cachegen_layout(L, n, H, bins)
+        b = cg.layout(L, n, H, bins)
+        assert (a.max1_offset, a.cdf_offset, a.lengths_offset, a.bytes_offset, a.max_bytes) == \
+            (b["max1"], b["cdf"], b["lengths"], b["bytes"], b["bound"])
+
+
+def test_cachegen_host_validation(lib):
+    bins = lmkv.cachegen_default_bins(2)
+    for args in [(0, 10, 64, bins), (2, 0, 64, bins), (2, 4097, 64, bins), (2, 10, 66, bins),
+                 (2, 10, 4096, bins), (2, 10, 64, [2, 16, 16, 16]), (2, 10, 64, [16, 16, 16, 34])]:
+        with pytest.raises(lmkv.LmkvError):
+            lmkv.cachegen_layout(*args)
+    ws = lmkv.cachegen_workspace_bytes(2, 64, [10, 300])
+    assert ws > 2 * 2 * 310 * 64
+    before = lmkv.launch_count()
+    ptrs, sizes = FakeTensor(0x30000), FakeTensor(0x40000)
+    for fn in (lmkv.cachegen_encode, lmkv.cachegen_decode):
+        def go(ntok=(10, 300), L=2, H=64, b=bins, w=FakeWorkspace(ws)):
+            if fn is lmkv.cachegen_encode:
+                return fn(ptrs, list(ntok), L, H, b, ptrs, sizes, w, None, 0)
+            return fn(ptrs, sizes, list(ntok), L, H, b, ptrs, w, None, 0)
+        assert go(w=FakeWorkspace(ws - 1)) == lmkv.ERR_INVALID_ARG       # workspace too small
+        assert go(w=FakeWorkspace(ws, ptr=0x50008)) == lmkv.ERR_MISALIGNED
+        assert go(ntok=(10, 0)) == lmkv.ERR_INVALID_ARG                    # empty chunk
+        assert go(ntok=(5000,)) == lmkv.ERR_INVALID_ARG                    # beyond the token limit
+        assert go(H=62) == lmkv.ERR_INVALID_ARG
+        assert go(b=[16, 16, 16, 3]) == lmkv.ERR_INVALID_ARG
+        assert go(ntok=()) == lmkv.OK                                      # nothing to do
+    assert lmkv.launch_count() == before

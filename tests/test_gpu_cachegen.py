@@ -1,0 +1,143 @@
+"""GPU parity of the CacheGen codec ("LMCache 中的 KV Cache 压缩：CacheGen
+编解码原理、配置方式与源码解析", sections 1-5).
+
+The blob (per-token max1, the 2^16 CDFs, the stream lengths and the coded
+bytes) must equal the oracle's byte for byte: every symbol is an integer
+decided by fp32 arithmetic that both sides take in fp32 (MAX / max1 by IEEE
+division, x * factor and + MAX rounded separately, ties to even), the CDF
+is exact integer arithmetic and the coder is integer-only.  Decoding must give
+the oracle's bf16 rows bit for bit.  Shapes: the page's benchmark (32 layers
+x 8 KV heads x 128, chunk sizes 64 / 128 / 256 / 768), odd sizes that leave a
+ragged last batch and partial warps, the largest chunk and channel counts,
+outlier channels, all-zero rows, and more chunks than one launch takes.
+"""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_lmkv_gb300 as pkg
+from oracle import cachegen as cg
+from paged_kv_cache_lmkv_gb300 import workloads as wl
+from gpu_util import DEV, host_u16, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _gpu():
+    require_gpu()
+    yield
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def gpu_encode(codec, chunks):
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    blobs, sizes = codec.encode(chunks, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0, pkg.lmkv.status_string(status.item())
+    sz = sizes.cpu().tolist()
+    return [b[:s].cpu().numpy().tobytes() for b, s in zip(blobs, sz)], blobs, sizes
+
+
+def gpu_decode(codec, blobs_bytes, ntoks):
+    blobs = [torch.from_numpy(np.frombuffer(b, np.uint8).copy()).to(DEV) for b in blobs_bytes]
+    sizes = torch.tensor([len(b) for b in blobs_bytes], dtype=torch.int64, device=DEV)
+    outs = [torch.full((2, codec.num_layers, n, codec.channels), 7.0, dtype=torch.bfloat16, device=DEV)
+            for n in ntoks]
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    codec.decode(blobs, sizes, outs, status=status)
+    torch.cuda.synchronize()
+    return [host_u16(o) for o in outs], status.item()
+
+
+def check_against_oracle(L, H, ntoks, seed, bins=None, **kw):
+    bins = cg.default_bins(L) if bins is None else np.asarray(bins, np.int32).reshape(2, L)
+    chunks = wl.cachegen_chunks(L, H, ntoks, seed, **kw)
+    codec = pkg.CachegenCodec(L, H, bins, device=DEV)
+    got, _, _ = gpu_encode(codec, [c.to(DEV) for c in chunks])
+    expect = [cg.encode_chunk(c, bins) for c in chunks]
+    for g, (a, b) in enumerate(zip(got, expect)):
+        assert len(a) == len(b), f"chunk {g}: size {len(a)} != oracle {len(b)}"
+        if a != b:
+            diff = np.flatnonzero(np.frombuffer(a, np.uint8) != np.frombuffer(b, np.uint8))
+            lay = cg.layout(L, ntoks[g], H, bins)
+            raise AssertionError(f"chunk {g}: {diff.size} bytes differ, first at {diff[0]} (layout {lay})")
+    dec, st = gpu_decode(codec, expect, ntoks)
+    assert st == 0
+    for g, (c, d) in enumerate(zip(chunks, dec)):
+        assert np.array_equal(d, cg.decode_chunk(expect[g], L, ntoks[g], H, bins)), f"chunk {g}"
+    return expect
+
+
+@pytest.mark.parametrize("L,H,ntoks", [
+    (1, 4, [1]),                       # one token, one partial warp
+    (2, 40, [5, 256, 300]),            # ragged last batch, 10 of 32 lanes
+    (3, 128, [257, 513, 64]),          # three batches
+    (2, 96, [1000]),
+])
+def test_small_shapes_exact(L, H, ntoks):
+    bins = cg.default_bins(L)
+    bins[0, 0] = 8
+    bins[1, -1] = 4
+    check_against_oracle(L, H, ntoks, seed=L * 100 + H, bins=bins)
+
+
+@pytest.mark.parametrize("n", wl.CACHEGEN_CHUNK_SIZES)
+def test_benchmark_shape_exact(n):
+    """The page's benchmark shape with the 7B/8B default bins."""
+    check_against_oracle(wl.CACHEGEN_LAYERS, wl.CACHEGEN_CHANNELS, [n], seed=n)
+
+
+def test_outliers_and_zero_rows_exact():
+    check_against_oracle(4, 1024, [256, 100], seed=5, outliers=True, zero_rows=3)
+
+
+def test_largest_sizes_exact():
+    """The most channels per row and the most tokens per chunk."""
+    check_against_oracle(1, pkg.lmkv.CACHEGEN_MAX_CHANNELS, [300], seed=9)
+    check_against_oracle(1, 64, [pkg.lmkv.CACHEGEN_MAX_TOKENS], seed=10)
+
+
+def test_more_chunks_than_one_launch():
+    rng = np.random.default_rng(3)
+    ntoks = [int(v) for v in rng.integers(1, 400, 70)]
+    check_against_oracle(2, 32, ntoks, seed=11)
+
+
+def test_round_trip_error_bound_and_determinism():
+    """Two encodes give the same bytes; the decoded rows stay within half a
+    quantisation step (max1 / MAX) of the input plus the bf16 rounding."""
+    L, H, n = wl.CACHEGEN_LAYERS, wl.CACHEGEN_CHANNELS, 256
+    bins = cg.default_bins(L)
+    x = wl.cachegen_chunks(L, H, [n, n], seed=21, device=DEV)
+    codec = pkg.CachegenCodec(L, H, bins, device=DEV)
+    a, blobs, sizes = gpu_encode(codec, x)
+    b, _, _ = gpu_encode(codec, x)
+    assert a == b
+    out = [torch.empty_like(t) for t in x]
+    codec.decode(blobs, sizes, out)
+    torch.cuda.synchronize()
+    for xi, yi in zip(x, out):
+        xf, yf = xi.float(), yi.float()
+        max1 = xf.abs().amax(dim=3, keepdim=True)
+        MAX = torch.tensor(bins // 2 - 1, dtype=torch.float32, device=DEV)[:, :, None, None]
+        assert bool(((yf - xf).abs() <= max1 * (0.5 / MAX * (1 + 1e-5) + 2.0 ** -8)).all())
+    raw = sum(t.numel() * 2 for t in x)
+    assert raw / sum(len(v) for v in a) > 3.0
+
+
+def test_inconsistent_blob_is_rejected():
+    """A blob whose lengths do not add up to its size decodes to nothing and
+    reports BAD_DATA; the output keeps its contents."""
+    L, H, n = 2, 64, 300
+    bins = cg.default_bins(L)
+    x = wl.cachegen_chunks(L, H, [n], seed=4)
+    blob = bytearray(cg.encode_chunk(x[0], bins))
+    lay = cg.layout(L, n, H, bins)
+    first = int.from_bytes(blob[lay["lengths"]:lay["lengths"] + 4], "little")
+    blob[lay["lengths"]:lay["lengths"] + 4] = (first + 1).to_bytes(4, "little")
+    codec = pkg.CachegenCodec(L, H, bins, device=DEV)
+    dec, st = gpu_decode(codec, [bytes(blob)], [n])
+    assert st == pkg.lmkv.ERR_BAD_DATA
+    assert np.all(dec[0] == np.uint16(0x40E0))           # 7.0 in bf16, untouched
