@@ -59,6 +59,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cachegen", action="store_true",
+                    help="skip the CacheGen codec measurement")
     ap.add_argument("--no-pipeline", action="store_true",
                     help="skip the layer-wise pipeline measurement (host round trip per layer)")
     ap.add_argument("--case", choices=["llama8b", "profile-small"], default="llama8b",
@@ -510,6 +512,117 @@ def bench_decode_store(c: Ctx, reps: int = 50):
     return out
 
 
+def bench_cachegen(c: Ctx, clk_mhz, reps: int = 5):
+    """CacheGen codec ("LMCache 中的 KV Cache 压缩：CacheGen 编解码原理、配置方式与
+    源码解析", sections 1-5) on the chunks the 8B gather produced (40 x 256
+    tokens, 32 layers x 1024 channels, the page's benchmark shape, default
+    7B/8B bins), then the page's chunk-size sweep 64 / 128 / 256 / 768 on
+    10240-token sets of N(0,1) bf16.  Each encode / decode call covers the
+    whole set (>= 1.3 GB of bf16, far above L2); event-timed on one stream.
+    GB/s counts the raw bf16 bytes.  The ALU roofline compares warp
+    instructions issued per second (ncu's count per symbol, from the profile
+    summary, times the symbols) with the issue peak 152 SMs x 4 schedulers x
+    1 instruction per clock at the sampled SM clock."""
+    w = c.w
+    L, H = w.num_layers, w.row_elems
+    stream = torch.cuda.Stream(c.dev)
+    lib = pkg.lmkv
+    codec = pkg.CachegenCodec(L, H, device=c.dev)
+    inst = profiled_codec_instructions()
+
+    def measure(chunks):
+        ntok = [int(x.shape[2]) for x in chunks]
+        blobs = [torch.empty(codec.layout(n).max_bytes, dtype=torch.uint8, device=c.dev) for n in ntok]
+        outs = [torch.empty_like(x) for x in chunks]
+        sizes = torch.zeros(len(chunks), dtype=torch.int64, device=c.dev)
+        cptr, bptr, optr = (pkg.pointer_array(v, c.dev) for v in (chunks, blobs, outs))
+        ws = codec._workspace(ntok)
+        bins = codec.bins
+        torch.cuda.synchronize(c.dev)
+
+        def enc():
+            pkg.check(lib.cachegen_encode(cptr, ntok, L, H, bins, bptr, sizes, ws, c.status, stream))
+
+        def dec():
+            pkg.check(lib.cachegen_decode(bptr, sizes, ntok, L, H, bins, optr, ws, c.status, stream))
+
+        for _ in range(2):
+            enc()
+            dec()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ev[0].record(stream)
+        for _ in range(reps):
+            enc()
+        ev[1].record(stream)
+        for _ in range(reps):
+            dec()
+        ev[2].record(stream)
+        torch.cuda.synchronize(c.dev)
+        raw = sum(x.numel() * 2 for x in chunks)
+        comp = int(sizes.sum().item())
+        te, td = ev[0].elapsed_time(ev[1]) / reps, ev[1].elapsed_time(ev[2]) / reps
+        return {"chunks": len(chunks), "raw_MB": round(raw / 1e6, 1), "blob_MB": round(comp / 1e6, 1),
+                "ratio": round(raw / comp, 3), "encode_ms": round(te, 3), "decode_ms": round(td, 3),
+                "encode_GBps_raw": round(raw / (te * 1e-3) / 1e9, 1),
+                "decode_GBps_raw": round(raw / (td * 1e-3) / 1e9, 1),
+                "_symbols": raw // 2, "_te": te, "_td": td}
+
+    # the 8B store path: the chunks the gather wrote
+    pkg.check(pkg.gather_chunks(c.pool, c.bt, w.starts, w.ends, w.chunk_size, w.save_unfull, c.ptrs,
+                                c.status, stream))
+    torch.cuda.synchronize(c.dev)
+    main = measure(c.bufs)
+    out = {"workload": "CacheGen on the 8B gather output: 40 chunks x 256 tokens x 32 layers x "
+                       "1024 channels bf16 N(0,1), default bins (K 10x32 + 22x16, V 2x32 + 30x16)"}
+    out.update({k: v for k, v in main.items() if not k.startswith("_")})
+    if inst is not None and clk_mhz:
+        peak = 152 * 4 * clk_mhz * 1e6                     # warp instructions per second
+        roof = {}
+        for name, t_ms in (("encode", main["_te"]), ("decode", main["_td"])):
+            issued = inst[name] * main["_symbols"]
+            achieved = issued / (t_ms * 1e-3)
+            roof[name] = {"achieved_warp_inst_per_s": round(achieved / 1e9, 1),
+                          "warp_inst_per_symbol": inst[name]}
+            roof[name]["frac"] = round(achieved / peak, 4)
+        out["roofline"] = {"bound": "alu", "unit": "G warp-instructions/s",
+                           "peak": round(peak / 1e9, 1),
+                           "peak_source": "152 SMs x 4 schedulers x 1 issue/clock x sampled SM clock",
+                           **roof}
+    sweep = {}
+    for C in wl.CACHEGEN_CHUNK_SIZES:
+        ntoks = [C] * (10240 // C) + ([10240 % C] if 10240 % C else [])
+        chunks = wl.cachegen_chunks(L, H, ntoks, seed=C, device=c.dev)
+        r = measure(chunks)
+        sweep[str(C)] = {k: r[k] for k in ("chunks", "ratio", "encode_GBps_raw", "decode_GBps_raw")}
+        del chunks
+        torch.cuda.empty_cache()
+    out["chunk_size_sweep"] = sweep
+    return out
+
+
+def profiled_codec_instructions():
+    """Warp instructions per coded symbol of the encode and decode calls, from
+    the committed ncu summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "cachegen_codec_llama8b.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    vals = dict(re.findall(r"^(\w+):\s*([0-9a-f.]+)\s*$", text, flags=re.M))
+    if vals.get("codec_source_sha256_16") != codec_source_hash():
+        return None
+    try:
+        return {"encode": float(vals["encode_warp_inst_per_symbol"]),
+                "decode": float(vals["decode_warp_inst_per_symbol"])}
+    except KeyError:
+        return None
+
+
+def codec_source_hash() -> str:
+    src = os.path.join(ROOT, "paged_kv_cache_lmkv_gb300", "csrc", "lmkv_cachegen.cu")
+    return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle (baseline leg and --impl reference).
 
@@ -683,6 +796,7 @@ def main():
     e2e = bench_e2e(c, args, stream)
     pipeline = bench_layer_pipeline(c) if not args.no_pipeline else None
     decode = bench_decode_store(c) if not args.no_pipeline else None
+    cachegen = bench_cachegen(c, clk.get("sm_mhz") if clk else None) if not args.no_cachegen else None
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(c)
@@ -704,6 +818,7 @@ def main():
             "e2e": e2e,
             "layer_pipeline": pipeline,
             "decode_store": decode,
+            "cachegen": cachegen,
             "cpu_baseline": cpu,
             "gpu_launches": int(launches),
             "clocks": clk,

@@ -409,8 +409,9 @@ int lmkv_cachegen_default_bins(int32_t num_layers, int32_t* bins);
 
 /* Offsets of one chunk's blob.  INVALID_ARG unless 1 <= num_layers <=
  * LMKV_CACHEGEN_MAX_LAYERS, 1 <= num_tokens <= LMKV_CACHEGEN_MAX_TOKENS,
- * 4 <= channels <= LMKV_CACHEGEN_MAX_CHANNELS with channels % 4 == 0, and
- * every bins entry in 4..32.  Host only. */
+ * 4 <= channels <= LMKV_CACHEGEN_MAX_CHANNELS with channels % 4 == 0, every
+ * bins entry in 4..32, and max_bytes below 4 GiB - 256 (the kernels address
+ * a blob with 32-bit offsets).  Host only. */
 int lmkv_cachegen_layout(int32_t num_layers, int32_t num_tokens, int32_t channels,
                          const int32_t* bins, lmkv_cachegen_layout_t* out);
 
@@ -420,7 +421,7 @@ int lmkv_cachegen_workspace_bytes(int32_t num_layers, int32_t channels, const in
                                   int32_t num_chunks, uint64_t* bytes);
 
 /* Encode chunk g (DEVICE chunk_ptrs[g] -> [2][L][n_g][H] bf16, 16-byte
- * aligned) into DEVICE blob_ptrs[g] (at least max_bytes of its layout) and
+ * aligned) into DEVICE blob_ptrs[g] (4-byte aligned, at least max_bytes of its layout) and
  * store its size into DEVICE sizes[g] (uint64).  num_tokens and bins are
  * HOST arrays; workspace is DEVICE memory of lmkv_cachegen_workspace_bytes
  * bytes (16-byte aligned, contents irrelevant, not shared with calls in
@@ -434,7 +435,7 @@ int lmkv_cachegen_encode(void* const* chunk_ptrs, const int32_t* num_tokens, int
                          void* const* blob_ptrs, uint64_t* sizes, void* workspace,
                          uint64_t workspace_bytes, int32_t* d_status, void* stream);
 
-/* Decode blob g (DEVICE blob_ptrs[g], DEVICE sizes[g] bytes) into DEVICE
+/* Decode blob g (DEVICE blob_ptrs[g], 4-byte aligned, DEVICE sizes[g] bytes) into DEVICE
  * chunk_ptrs[g] ([2][L][n_g][H] bf16, 16-byte aligned).  Streams are found
  * through the prefix sums of the lengths (section 5).  A blob whose lengths
  * do not add up to its size, or a stream that would run past it, is not

@@ -38,6 +38,7 @@ constexpr int kMaxSlices = 2 * LMKV_CACHEGEN_MAX_LAYERS;
 constexpr int kStreams = 4;                    // channels (streams) per thread
 constexpr int kRows = 8;                       // rows per block-wide absmax round
 constexpr int kMaxThreads = LMKV_CACHEGEN_MAX_CHANNELS / kStreams;
+constexpr uint64_t kMaxBlobBytes = 0xFFFFFF00ull;   // blobs are addressed with 32-bit offsets
 constexpr uint32_t kHalf = 0x80000000u;
 constexpr uint32_t kQuarter = 0x40000000u;
 
@@ -81,13 +82,6 @@ __device__ __forceinline__ void set_status(int32_t* st, int code) {
     if (st != nullptr) atomicCAS(st, 0, code);
 }
 
-__device__ __forceinline__ uint2 ld_nc_v2(const void* p) {
-    uint2 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
-                 : "=r"(v.x), "=r"(v.y) : "l"(p));
-    return v;
-}
-
 // |x| of two packed bf16 as the larger fp32 bit pattern (non-negative floats
 // order like their bit patterns).
 __device__ __forceinline__ uint32_t abs_max_bits(uint32_t two_bf16) {
@@ -107,10 +101,18 @@ __device__ __forceinline__ uint32_t quantise(float x, float factor, float maxf, 
     return (uint32_t)q;
 }
 
+// Channel j (0..kStreams-1) of thread tid: the pairs (2*tid, 2*tid + 1) in
+// each half of the row.  Lanes then touch consecutive 32-bit words of every
+// [symbol][channel] uint16 table row, so table reads and histogram updates
+// are free of shared-memory bank conflicts whatever symbol each lane holds.
+__device__ __forceinline__ int chan(int tid, int j, int H) {
+    return 2 * tid + (j & 1) + (j >> 1) * (H >> 1);
+}
+
 // ---- arithmetic encoder state, one per stream ----
 struct Enc {
     uint32_t low, high, follow, nacc, words;
-    uint64_t acc;          // pending output bits, the last nacc valid
+    uint64_t acc;          // output bits not yet stored, the last nacc valid
 };
 
 __device__ __forceinline__ void enc_init(Enc& e) {
@@ -122,42 +124,46 @@ __device__ __forceinline__ void enc_init(Enc& e) {
     e.acc = 0;
 }
 
-// Append the c (0..32) low bits of v; full 32-bit words go to the slot,
-// most significant byte first.
+// Append the c (0..32) bits v (nothing above them set); a completed 32-bit
+// word goes to the slot, most significant byte first.
 __device__ __forceinline__ void put_bits(Enc& e, uint32_t v, uint32_t c, uint32_t* slot,
                                          uint32_t cap_words, bool& overflow) {
     e.acc = (e.acc << c) | v;
     e.nacc += c;
-    if (e.nacc >= 32) {
-        e.nacc -= 32;
-        const uint32_t w = (uint32_t)(e.acc >> e.nacc);
+    const bool full = e.nacc >= 32;
+    e.nacc -= full ? 32u : 0u;
+    const uint32_t w = (uint32_t)(e.acc >> e.nacc);
+    if (full) {
         if (e.words < cap_words) slot[e.words] = __byte_perm(w, 0, 0x0123);
         else overflow = true;
-        ++e.words;
     }
+    e.words += full ? 1u : 0u;
 }
 
-// The decided bit `bit`, then e.follow opposite bits, then the k-1 bits `rest`.
-__device__ __forceinline__ void emit(Enc& e, uint32_t bit, uint32_t k, uint32_t rest, uint32_t* slot,
-                                     uint32_t cap_words, bool& overflow) {
-    const uint32_t f = e.follow;
-    if (f + k <= 32) {
-        const uint32_t run = bit ? 0u : (f ? (0xFFFFFFFFu >> (32 - f)) : 0u);
-        const uint64_t v = ((uint64_t)bit << (f + k - 1)) | ((uint64_t)run << (k - 1)) | rest;
-        put_bits(e, (uint32_t)v, f + k, slot, cap_words, overflow);
-    } else {
-        put_bits(e, bit, 1, slot, cap_words, overflow);
-        for (uint32_t left = f; left > 0;) {
-            const uint32_t c = left < 32 ? left : 32;
-            put_bits(e, bit ? 0u : (0xFFFFFFFFu >> (32 - c)), c, slot, cap_words, overflow);
-            left -= c;
-        }
-        put_bits(e, rest, k - 1, slot, cap_words, overflow);
+// The rare case of more than 32 bits at once (a long run of held bits):
+// `bit`, then `f` opposite bits, then the k-1 bits `rest`.
+__device__ __forceinline__ void emit_long(Enc& e, uint32_t bit, uint32_t f, uint32_t k, uint32_t rest,
+                                      uint32_t* slot, uint32_t cap_words, bool& overflow) {
+    put_bits(e, bit, 1, slot, cap_words, overflow);
+    for (uint32_t left = f; left > 0;) {
+        const uint32_t c = left < 32 ? left : 32;
+        put_bits(e, bit ? 0u : (uint32_t)((1ull << c) - 1), c, slot, cap_words, overflow);
+        left -= c;
     }
-    e.follow = 0;
+    put_bits(e, rest, k - 1, slot, cap_words, overflow);
 }
 
-// Narrow [low, high] to the symbol's [lo, hi) out of 2^16 and renormalise.
+// Narrow [low, high] to the symbol's [lo, hi) out of 2^16, then renormalise.
+//
+// low and high are kept without the quarter subtraction of the middle-
+// straddling steps: such a step is a left shift followed by adding 2^31
+// modulo 2^32, and leaving the addition out changes only bit 31 of low and
+// high, both alike.  So low ^ high, high - low and every bit below bit 31 are
+// those of the textbook registers, and bit 31 of the true low is bit 31 of
+// this low flipped exactly when held bits are pending (follow > 0).  The
+// renormalisation is then one shift by k + m: the k leading bits where low
+// and high agree are decided (the first releases the held bits, as its
+// opposite), and the m steps after them that straddle the middle are held.
 __device__ __forceinline__ void enc_symbol(Enc& e, uint32_t lo, uint32_t hi, uint32_t* slot,
                                            uint32_t cap_words, bool& overflow) {
     const uint32_t rm1 = e.high - e.low;                       // range - 1
@@ -165,28 +171,40 @@ __device__ __forceinline__ void enc_symbol(Enc& e, uint32_t lo, uint32_t hi, uin
     const uint64_t bot = (uint64_t)rm1 * lo + lo;              // range * lo
     e.high = e.low + (uint32_t)(top >> 16) - 1;
     e.low = e.low + (uint32_t)(bot >> 16);
-    const uint32_t k = __clz(e.low ^ e.high);                  // leading agreed bits
-    if (k) {
-        const uint32_t rest = k > 1 ? (e.low << 1) >> (33 - k) : 0u;
-        emit(e, e.low >> 31, k, rest, slot, cap_words, overflow);
-        e.low <<= k;
-        e.high = (e.high << k) | ((1u << k) - 1);
+    const uint32_t k = __clz(e.low ^ e.high);                  // 0..18
+    const uint32_t f = e.follow;
+    // The k decided bits are the top k bits of the true low.  "b" followed by
+    // f copies of "not b" is the number 2^f - 1 + b, so the run is
+    // top_k(true low) + (2^f - 1) * 2^(k-1).
+    const uint32_t first = (uint32_t)((uint64_t)(f ? 1u : 0u) << k) >> 1;   // bit 31's place, or 0
+    const uint32_t topk = __funnelshift_rc(e.low, 0u, 32 - k) ^ first;     // 0 when k == 0
+    if (f + k <= 32) {
+        const uint32_t held = (uint32_t)((((1ull << f) - 1) << k) >> 1);
+        put_bits(e, k ? topk + held : 0u, k ? f + k : 0u, slot, cap_words, overflow);
+    } else if (k) {
+        emit_long(e, topk >> (k - 1), f, k, topk & ((1u << (k - 1)) - 1), slot, cap_words, overflow);
     }
-    const uint32_t a = __clz(~(e.low << 1)), b = __clz(e.high << 1);
+    const uint32_t a = __clz(~(e.low << (k + 1))), b = __clz(e.high << (k + 1));
     const uint32_t m = a < b ? a : b;                          // straddling steps
-    if (m) {
-        e.follow += m;
-        e.low = (e.low << m) & 0x7FFFFFFFu;
-        e.high = (e.high << m) | kHalf | ((1u << m) - 1);
-    }
+    const uint32_t c = k + m;
+    e.follow = (k ? 0u : f) + m;
+    e.low <<= c;
+    e.high = (e.high << c) | ((1u << c) - 1);
 }
 
 // Two final bits select a point inside the last interval; returns the
-// stream's length in bytes.
+// stream's length in bytes.  Bit 30 of the kept low is that of the true low.
 __device__ __forceinline__ uint32_t enc_finish(Enc& e, uint32_t* slot, uint32_t cap_words,
                                                bool& overflow) {
-    e.follow += 1;
-    emit(e, e.low >= kQuarter ? 1u : 0u, 1, 0, slot, cap_words, overflow);
+    const uint32_t bit = (e.low >> 30) & 1u;                   // true low >= 2^30
+    const uint32_t f = e.follow + 1;
+    if (f + 1 <= 32) {
+        const uint32_t run = bit ? 0u : (uint32_t)((1ull << f) - 1);
+        put_bits(e, (bit << f) | run, f + 1, slot, cap_words, overflow);
+    } else {
+        emit_long(e, bit, f, 1, 0, slot, cap_words, overflow);
+    }
+    e.follow = 0;
     const uint32_t bits = e.words * 32 + e.nacc;
     if (e.nacc) {
         const uint32_t w = (uint32_t)(e.acc << (32 - e.nacc));
@@ -197,60 +215,84 @@ __device__ __forceinline__ uint32_t enc_finish(Enc& e, uint32_t* slot, uint32_t 
 }
 
 // ---- arithmetic decoder state, one per stream ----
+// The reader does not stop at the stream's end: the bits after it are those
+// of the next stream (or of the blob's tail).  That cannot change a decoded
+// symbol, because the encoder's two final bits select a sub-interval of the
+// last interval that every continuation stays inside ([1/4, 1/2) or
+// [1/2, 3/4) of the renormalised window), and the decoder stops after n
+// symbols.  Reads stay inside the blob.  low, high and value are kept without
+// the quarter subtraction, as in the encoder: the decoder needs only
+// value - low, high - low and low ^ high, which that leaves unchanged.
 struct Dec {
-    uint32_t low, high, value, nbuf, left;
-    uint64_t buf;           // upcoming bits, most significant first; nbuf valid
-    const uint8_t* p;       // next unread byte; `left` bytes remain in the stream
+    uint32_t low, high, value, nbuf;
+    uint32_t q;              // blob offset of the next word to load
+    uint32_t next;           // the word at q - 4 as loaded, ahead of its use
+    uint64_t buf;            // upcoming bits, most significant first; nbuf valid
 };
 
-// Top the bit buffer up to more than 32 bits; past the stream's end the
-// stream reads as zeros.
-__device__ __forceinline__ void dec_refill(Dec& d) {
-    while (d.nbuf <= 32) {
-        uint32_t w = 0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) w = (w << 8) | (d.left > (uint32_t)i ? (uint32_t)__ldg(d.p + i) : 0u);
-        d.p += 4;
-        d.left = d.left > 4 ? d.left - 4 : 0;
-        d.buf |= (uint64_t)w << (32 - d.nbuf);
+// The aligned word at blob offset q as stored (little-endian load); bytes at
+// or past `size` read as zero.  The byte swap to stream order is left to the
+// consumer so that a load issued ahead is not waited for here.
+__device__ __forceinline__ uint32_t load_word(const uint8_t* blob, uint32_t q, uint32_t size) {
+    if (q + 4 <= size) return __ldg(reinterpret_cast<const uint32_t*>(blob + q));
+    uint32_t w = 0;
+    for (uint32_t i = 0; i < 4; ++i)
+        if (q + i < size) w |= (uint32_t)blob[q + i] << (8 * i);
+    return w;
+}
+
+// Keep more than 32 bits buffered; the word after the one consumed is
+// loaded now and used by the next refill.
+__device__ __forceinline__ void dec_refill(Dec& d, const uint8_t* blob, uint32_t size) {
+    if (d.nbuf <= 32) {
+        d.buf |= (uint64_t)__byte_perm(d.next, 0, 0x0123) << (32 - d.nbuf);
         d.nbuf += 32;
+        d.next = load_word(blob, d.q, size);
+        d.q += 4;
     }
 }
 
-__device__ __forceinline__ uint32_t dec_take(Dec& d, uint32_t c) {   // 1 <= c <= 32
-    const uint32_t r = (uint32_t)(d.buf >> (64 - c));
+// The next c (0..32) bits.
+__device__ __forceinline__ uint32_t dec_take(Dec& d, uint32_t c) {
+    const uint32_t r = __funnelshift_lc((uint32_t)(d.buf >> 32), 0u, c);
     d.buf <<= c;
     d.nbuf -= c;
     return r;
 }
 
-__device__ __forceinline__ void dec_init(Dec& d, const uint8_t* p, uint32_t len) {
+// The stream starting at blob offset `start` (the blob is 4-byte aligned and
+// `size` bytes long).
+__device__ __forceinline__ void dec_init(Dec& d, const uint8_t* blob, uint32_t start, uint32_t size) {
+    const uint32_t a = start & ~3u, sh = start - a;
+    d.buf = (uint64_t)(__byte_perm(load_word(blob, a, size), 0, 0x0123) << (8 * sh)) << 32;
+    d.nbuf = 32 - 8 * sh;
+    d.next = load_word(blob, a + 4, size);
+    d.q = a + 8;
+    dec_refill(d, blob, size);
+    d.value = dec_take(d, 32);
     d.low = 0;
     d.high = 0xFFFFFFFFu;
-    d.p = p;
-    d.left = len;
-    d.buf = 0;
-    d.nbuf = 0;
-    dec_refill(d);
-    d.value = dec_take(d, 32);
 }
 
 // One symbol.  table[k * H] holds C[k] of this stream's channel for k < nsym
-// (C[nsym] = 2^16).  The symbol is the largest k with
-// floor(range * C[k] / 2^16) <= value - low: the interval the encoder chose.
-__device__ __forceinline__ uint32_t dec_symbol(Dec& d, const uint16_t* table, int H, int nsym) {
-    if (d.nbuf < 32) dec_refill(d);
+// and 0xFFFF for nsym <= k < 2^kSteps (C[nsym] = 2^16).  The symbol is the
+// largest k with floor(range * C[k] / 2^16) <= value - low: the interval the
+// encoder chose.  A padding row can only be picked when value - low lies in
+// the top of the last symbol's interval, so the search result is clamped to
+// nsym - 1.
+template <int kSteps>
+__device__ __forceinline__ uint32_t dec_symbol(Dec& d, const uint16_t* table, int H, int nsym,
+                                               const uint8_t* blob, uint32_t size) {
+    dec_refill(d, blob, size);
     const uint32_t v = d.value - d.low;
     const uint32_t rm1 = d.high - d.low;
     int s = 0;
 #pragma unroll
-    for (int step = 16; step >= 1; step >>= 1) {
-        const int cand = s + step;
-        if (cand < nsym) {
-            const uint32_t C = table[cand * H];
-            if ((uint32_t)(((uint64_t)rm1 * C + C) >> 16) <= v) s = cand;
-        }
+    for (int step = 1 << (kSteps - 1); step >= 1; step >>= 1) {
+        const uint32_t C = table[(s + step) * H];
+        if ((uint32_t)(((uint64_t)rm1 * C + C) >> 16) <= v) s += step;
     }
+    s = s < nsym - 1 ? s : nsym - 1;
     const uint32_t lo = table[s * H];
     const uint32_t hi = s + 1 < nsym ? (uint32_t)table[(s + 1) * H] : 65536u;
     const uint64_t top = (uint64_t)rm1 * hi + hi;
@@ -258,18 +300,11 @@ __device__ __forceinline__ uint32_t dec_symbol(Dec& d, const uint16_t* table, in
     d.high = d.low + (uint32_t)(top >> 16) - 1;
     d.low = d.low + (uint32_t)(bot >> 16);
     const uint32_t k = __clz(d.low ^ d.high);
-    if (k) {
-        d.value = (d.value << k) | dec_take(d, k);
-        d.low <<= k;
-        d.high = (d.high << k) | ((1u << k) - 1);
-    }
-    const uint32_t a = __clz(~(d.low << 1)), b = __clz(d.high << 1);
-    const uint32_t m = a < b ? a : b;
-    if (m) {
-        d.value = (d.value & kHalf) | ((d.value << m) & 0x7FFFFFFFu) | dec_take(d, m);
-        d.low = (d.low << m) & 0x7FFFFFFFu;
-        d.high = (d.high << m) | kHalf | ((1u << m) - 1);
-    }
+    const uint32_t a = __clz(~(d.low << (k + 1))), b = __clz(d.high << (k + 1));
+    const uint32_t c = k + (a < b ? a : b);
+    d.low <<= c;
+    d.high = (d.high << c) | ((1u << c) - 1);
+    d.value = (d.value << c) | dec_take(d, c);
     return (uint32_t)s;
 }
 
@@ -286,8 +321,9 @@ __device__ __forceinline__ uint64_t block_sum(uint64_t v, uint64_t* red) {
     return t;
 }
 
-// Exclusive block-wide prefix sum of v (in thread order); `red` >= 32 words.
-__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* red) {
+// Exclusive block-wide prefix sum of v in thread order, and the block total.
+// `red` holds >= 32 words.
+__device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t* red, uint32_t* total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
     uint32_t x = v;
 #pragma unroll
@@ -298,15 +334,31 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* r
     __syncthreads();
     if (lane == 31) red[warp] = x;
     __syncthreads();
-    uint32_t before = 0;
-    for (int w = 0; w < warp; ++w) before += red[w];
-    (void)nw;
+    uint32_t before = 0, all = 0;
+    for (int w = 0; w < nw; ++w) {
+        before += w < warp ? red[w] : 0u;
+        all += red[w];
+    }
+    *total = all;
     return before + x - v;
 }
 
+// Byte offsets, in channel order, of this thread's kStreams streams within
+// their region, from the region's lengths.
+__device__ __forceinline__ void stream_offsets(const uint32_t (&l)[kStreams], uint32_t* red,
+                                               uint32_t (&off)[kStreams]) {
+    uint32_t total0, total1;
+    const uint32_t o0 = block_scan(l[0] + l[1], red, &total0);      // channels 0 .. H/2-1
+    const uint32_t o1 = block_scan(l[2] + l[3], red + 32, &total1); // channels H/2 .. H-1
+    off[0] = o0;
+    off[1] = o0 + l[0];
+    off[2] = total0 + o1;
+    off[3] = total0 + o1 + l[2];
+}
+
 // ---- encode 1: absmax, symbols, histogram, CDF ----
-// grid (2L, chunks), block = threads covering H / kStreams channel groups.
-// Shared memory: uint16 hist[kMaxSym][H].
+// grid (2L, chunks), block = H / kStreams threads rounded up to a warp.
+// Shared memory: uint16 hist[nsym_max][H].
 __global__ void __launch_bounds__(kMaxThreads) cg_cdf_kernel(const __grid_constant__ CgParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ uint32_t part[2][kRows][kMaxThreads / 32];
@@ -314,8 +366,7 @@ __global__ void __launch_bounds__(kMaxThreads) cg_cdf_kernel(const __grid_consta
     const int n = p.ntok[gi], H = p.H, L = p.L;
     const int bins = p.bins[s], MAX = bins / 2 - 1, nsym = 2 * MAX + 1;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = (blockDim.x + 31) >> 5;
-    const int c0 = tid * kStreams;
-    const bool active = c0 < H;
+    const bool active = tid < H / kStreams;
     uint16_t* hist = reinterpret_cast<uint16_t*>(smem);
 
     const uint8_t* chunk = p.chunk_ptrs[gi];
@@ -325,19 +376,28 @@ __global__ void __launch_bounds__(kMaxThreads) cg_cdf_kernel(const __grid_consta
         return;
     }
     if (active)
-        for (int k = 0; k < nsym; ++k)
-            *reinterpret_cast<uint2*>(hist + k * H + c0) = make_uint2(0, 0);
+        for (int k = 0; k < nsym; ++k) {
+            *reinterpret_cast<uint32_t*>(hist + k * H + chan(tid, 0, H)) = 0;
+            *reinterpret_cast<uint32_t*>(hist + k * H + chan(tid, 2, H)) = 0;
+        }
 
-    const uint8_t* x = chunk + ((uint64_t)s * n * H + c0) * 2;
-    uint32_t* sym = reinterpret_cast<uint32_t*>(p.ws + p.sym_off[gi] + (uint64_t)s * n * H + c0);
+    // this thread's two bf16 pairs of a row: channels (2t, 2t+1) and (H/2 + 2t, H/2 + 2t + 1)
+    const uint8_t* x = chunk + (uint64_t)s * n * H * 2 + 4 * tid;
+    uint32_t* sym = reinterpret_cast<uint32_t*>(p.ws + p.sym_off[gi] + (uint64_t)s * n * H) + tid;
     float* max1_out = reinterpret_cast<float*>(blob) + (uint64_t)s * n;
     const float maxf = (float)MAX;
 
     for (int t0 = 0, buf = 0; t0 < n; t0 += kRows, buf ^= 1) {
         uint2 v[kRows];
 #pragma unroll
-        for (int r = 0; r < kRows; ++r)
-            v[r] = (active && t0 + r < n) ? ld_nc_v2(x + (uint64_t)(t0 + r) * H * 2) : make_uint2(0, 0);
+        for (int r = 0; r < kRows; ++r) {
+            v[r] = make_uint2(0, 0);
+            if (active && t0 + r < n) {
+                const uint8_t* row = x + (uint64_t)(t0 + r) * H * 2;
+                v[r].x = __ldg(reinterpret_cast<const uint32_t*>(row));
+                v[r].y = __ldg(reinterpret_cast<const uint32_t*>(row + H));
+            }
+        }
 #pragma unroll
         for (int r = 0; r < kRows; ++r) {
             const uint32_t a = abs_max_bits(v[r].x), b = abs_max_bits(v[r].y);
@@ -354,61 +414,60 @@ __global__ void __launch_bounds__(kMaxThreads) cg_cdf_kernel(const __grid_consta
             const float m = __uint_as_float(mb);
             if (tid == r) max1_out[t] = m;
             if (!active) continue;
-            uint32_t q0, q1, q2, q3;
+            uint32_t q[kStreams];
             if (m == 0.0f) {
-                q0 = q1 = q2 = q3 = (uint32_t)MAX;
+                q[0] = q[1] = q[2] = q[3] = (uint32_t)MAX;
             } else {
                 const float factor = __fdiv_rn(maxf, m);
-                q0 = quantise(bf16_lo(v[r].x), factor, maxf, 2 * MAX);
-                q1 = quantise(bf16_hi(v[r].x), factor, maxf, 2 * MAX);
-                q2 = quantise(bf16_lo(v[r].y), factor, maxf, 2 * MAX);
-                q3 = quantise(bf16_hi(v[r].y), factor, maxf, 2 * MAX);
+                q[0] = quantise(bf16_lo(v[r].x), factor, maxf, 2 * MAX);
+                q[1] = quantise(bf16_hi(v[r].x), factor, maxf, 2 * MAX);
+                q[2] = quantise(bf16_lo(v[r].y), factor, maxf, 2 * MAX);
+                q[3] = quantise(bf16_hi(v[r].y), factor, maxf, 2 * MAX);
             }
-            sym[(uint64_t)t * (H / 4)] = q0 | (q1 << 8) | (q2 << 16) | (q3 << 24);
-            hist[q0 * H + c0 + 0] += 1;
-            hist[q1 * H + c0 + 1] += 1;
-            hist[q2 * H + c0 + 2] += 1;
-            hist[q3 * H + c0 + 3] += 1;
+            sym[(uint64_t)t * (H / 4)] = q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24);
+#pragma unroll
+            for (int j = 0; j < kStreams; ++j) hist[q[j] * H + chan(tid, j, H)] += 1;
         }
     }
     if (!active) return;
     // C[k] = round(cum[k] * (2^16 - (Lp - 1)) / n) + k, ties to even; the
     // blob keeps C[1..nsym-1] per channel.
     const uint32_t M = 65536u - (uint32_t)nsym;
-    uint16_t* cdf = reinterpret_cast<uint16_t*>(blob + cdf_offset(L, n)) + p.cdf_prefix[s] +
-                    (uint64_t)c0 * (nsym - 1);
+    uint16_t* cdf = reinterpret_cast<uint16_t*>(blob + cdf_offset(L, n)) + p.cdf_prefix[s];
 #pragma unroll
     for (int j = 0; j < kStreams; ++j) {
+        const int c = chan(tid, j, H);
+        uint16_t* dst = cdf + (uint64_t)c * (nsym - 1);
         uint32_t cum = 0;
         for (int k = 0; k < nsym; ++k) {
             const uint32_t num = cum * M;
             uint32_t q = num / (uint32_t)n;
             const uint32_t r = num - q * (uint32_t)n;
             if (2 * r > (uint32_t)n || (2 * r == (uint32_t)n && (q & 1))) ++q;
-            if (k > 0) cdf[j * (nsym - 1) + k - 1] = (uint16_t)(q + k);
-            cum += hist[k * H + c0 + j];
+            if (k > 0) dst[k - 1] = (uint16_t)(q + k);
+            cum += hist[k * H + c];
         }
     }
 }
 
 // Load one slice's CDF table from the blob into shared memory:
-// table[k * H + c] = C[k] for k < nsym (C[0] = 0).
+// table[k * H + c] = C[k] for k < nsym (C[0] = 0), this thread's channels.
 __device__ __forceinline__ void load_table(uint16_t* table, const uint8_t* blob, const CgParams& p,
-                                           int s, int n, int nsym, int c0, bool active) {
-    if (!active) return;
+                                           int s, int n, int nsym, int tid) {
     const int H = p.H;
-    const uint16_t* src = reinterpret_cast<const uint16_t*>(blob + cdf_offset(p.L, n)) +
-                          p.cdf_prefix[s] + (uint64_t)c0 * (nsym - 1);
+    const uint16_t* src = reinterpret_cast<const uint16_t*>(blob + cdf_offset(p.L, n)) + p.cdf_prefix[s];
 #pragma unroll
     for (int j = 0; j < kStreams; ++j) {
-        table[c0 + j] = 0;
-        for (int k = 1; k < nsym; ++k) table[k * H + c0 + j] = src[j * (nsym - 1) + k - 1];
+        const int c = chan(tid, j, H);
+        const uint16_t* sc = src + (uint64_t)c * (nsym - 1);
+        table[c] = 0;
+        for (int k = 1; k < nsym; ++k) table[k * H + c] = sc[k - 1];
     }
 }
 
 // ---- encode 2: one CTA per (chunk, batch, kv, layer) region ----
-// grid (nb_max * 2L, chunks).  Shared memory: uint16 table[kMaxSym][H].
-__global__ void __launch_bounds__(kMaxThreads) cg_code_kernel(const __grid_constant__ CgParams p) {
+// grid (nb_max * 2L, chunks).  Shared memory: uint16 table[nsym_max][H].
+__global__ void __launch_bounds__(kMaxThreads, 1) cg_code_kernel(const __grid_constant__ CgParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ uint64_t red[32];
     const int gi = blockIdx.y, n = p.ntok[gi], H = p.H, L = p.L;
@@ -416,12 +475,12 @@ __global__ void __launch_bounds__(kMaxThreads) cg_code_kernel(const __grid_const
     if (b >= batches_of(n)) return;
     const int nsym = nsym_of(p.bins[s]);
     const int t0 = b * kBatch, nt = n - t0 < kBatch ? n - t0 : kBatch;
-    const int tid = threadIdx.x, c0 = tid * kStreams;
-    const bool active = c0 < H;
+    const int tid = threadIdx.x;
+    const bool active = tid < H / kStreams;
     uint8_t* blob = p.blob_ptrs[gi];
     if (p.chunk_ptrs[gi] == nullptr || blob == nullptr) return;   // reported by the CDF kernel
     uint16_t* table = reinterpret_cast<uint16_t*>(smem);
-    load_table(table, blob, p, s, n, nsym, c0, active);
+    if (active) load_table(table, blob, p, s, n, nsym, tid);
     __syncthreads();
 
     const uint64_t stride = slot_stride(n);
@@ -430,15 +489,17 @@ __global__ void __launch_bounds__(kMaxThreads) cg_code_kernel(const __grid_const
     bool overflow = false;
     if (active) {
         uint32_t* slot[kStreams];
+        const uint16_t* tab[kStreams];
         Enc e[kStreams];
 #pragma unroll
         for (int j = 0; j < kStreams; ++j) {
-            slot[j] = reinterpret_cast<uint32_t*>(p.ws + p.slot_off[gi] +
-                                                  ((uint64_t)region * H + c0 + j) * stride);
+            const int c = chan(tid, j, H);
+            slot[j] = reinterpret_cast<uint32_t*>(p.ws + p.slot_off[gi] + ((uint64_t)region * H + c) * stride);
+            tab[j] = table + c;
             enc_init(e[j]);
         }
         const uint32_t* sym = reinterpret_cast<const uint32_t*>(p.ws + p.sym_off[gi] +
-                                                                ((uint64_t)s * n + t0) * H + c0);
+                                                                ((uint64_t)s * n + t0) * H) + tid;
         const int hw = H / 4;
         uint32_t w_next = sym[0];
         for (int t = 0; t < nt; ++t) {
@@ -447,21 +508,20 @@ __global__ void __launch_bounds__(kMaxThreads) cg_code_kernel(const __grid_const
 #pragma unroll
             for (int j = 0; j < kStreams; ++j) {
                 const uint32_t q = (w >> (8 * j)) & 0xFFu;
-                const uint32_t lo = table[q * H + c0 + j];
-                const uint32_t hi = (int)q + 1 < nsym ? (uint32_t)table[(q + 1) * H + c0 + j] : 65536u;
+                const uint32_t lo = tab[j][q * H];
+                const uint32_t hi = (int)q + 1 < nsym ? (uint32_t)tab[j][(q + 1) * H] : 65536u;
                 enc_symbol(e[j], lo, hi, slot[j], cap_words, overflow);
             }
         }
+        uint32_t* lengths = reinterpret_cast<uint32_t*>(blob + lengths_offset(L, n, p.cdf_entries)) +
+                            (uint64_t)region * H;
 #pragma unroll
         for (int j = 0; j < kStreams; ++j) {
             len[j] = enc_finish(e[j], slot[j], cap_words, overflow);
             // never past the slot (excluded by the bound; keeps the blob in bounds)
             len[j] = len[j] < cap_words * 4 ? len[j] : cap_words * 4;
+            lengths[chan(tid, j, H)] = len[j];
         }
-        uint32_t* lengths = reinterpret_cast<uint32_t*>(blob + lengths_offset(L, n, p.cdf_entries)) +
-                            (uint64_t)region * H + c0;
-#pragma unroll
-        for (int j = 0; j < kStreams; ++j) lengths[j] = len[j];
     }
     if (overflow) set_status(p.status, LMKV_ERR_SCRATCH_LIMIT);   // excluded by the bound
     const uint64_t total = block_sum((uint64_t)len[0] + len[1] + len[2] + len[3], red);
@@ -484,40 +544,40 @@ __device__ __forceinline__ void region_base(const uint32_t* totals, int region, 
 }
 
 // ---- encode 3: place every stream at its prefix-sum offset ----
-// grid (nb_max * 2L, chunks), block as the coder.
+// grid (nb_max * 2L, chunks), block as the coder.  Shared memory: uint32
+// off[H], len[H].
 __global__ void __launch_bounds__(kMaxThreads) cg_compact_kernel(const __grid_constant__ CgParams p) {
     __shared__ uint64_t red[32];
-    __shared__ uint32_t sred[32];
+    __shared__ uint32_t sred[64];
     extern __shared__ __align__(16) uint8_t smem[];
-    uint32_t* off = reinterpret_cast<uint32_t*>(smem);           // [H] offset within the region
-    uint32_t* lens = off + p.H;                                   // [H]
+    uint32_t* off = reinterpret_cast<uint32_t*>(smem);
+    uint32_t* lens = off + p.H;
     const int gi = blockIdx.y, n = p.ntok[gi], H = p.H, L = p.L;
     const int region = blockIdx.x, b = region / (2 * L);
     const int nb = batches_of(n), nregions = nb * 2 * L;
     if (b >= nb) return;
     uint8_t* blob = p.blob_ptrs[gi];
     if (p.chunk_ptrs[gi] == nullptr || blob == nullptr) return;
-    const int tid = threadIdx.x, c0 = tid * kStreams;
-    const bool active = c0 < H;
-    const uint32_t* totals = reinterpret_cast<const uint32_t*>(p.ws + p.tot_off[gi]);
+    const int tid = threadIdx.x;
+    const bool active = tid < H / kStreams;
     uint64_t before, all;
-    region_base(totals, region, nregions, red, &before, &all);
+    region_base(reinterpret_cast<const uint32_t*>(p.ws + p.tot_off[gi]), region, nregions, red,
+                &before, &all);
     const uint64_t bytes0 = bytes_offset(L, n, H, p.cdf_entries);
     if (region == 0 && tid == 0) p.sizes[gi] = bytes0 + all;
 
     const uint32_t* lengths = reinterpret_cast<const uint32_t*>(blob + lengths_offset(L, n, p.cdf_entries)) +
                               (uint64_t)region * H;
-    uint32_t l[kStreams] = {0, 0, 0, 0};
+    uint32_t l[kStreams] = {0, 0, 0, 0}, o[kStreams];
     if (active)
 #pragma unroll
-        for (int j = 0; j < kStreams; ++j) l[j] = lengths[c0 + j];
-    uint32_t o = block_exclusive_scan(l[0] + l[1] + l[2] + l[3], sred);
+        for (int j = 0; j < kStreams; ++j) l[j] = lengths[chan(tid, j, H)];
+    stream_offsets(l, sred, o);
     if (active)
 #pragma unroll
         for (int j = 0; j < kStreams; ++j) {
-            off[c0 + j] = o;
-            lens[c0 + j] = l[j];
-            o += l[j];
+            off[chan(tid, j, H)] = o[j];
+            lens[chan(tid, j, H)] = l[j];
         }
     __syncthreads();
     // one warp per stream, lanes on consecutive bytes
@@ -558,12 +618,53 @@ __global__ void __launch_bounds__(256) cg_total_kernel(const __grid_constant__ C
     }
 }
 
+// The decoder's table: C[k] for k < nsym, then 0xFFFF up to the next power of
+// two rows (see dec_symbol).
+__device__ __forceinline__ void load_search_table(uint16_t* table, const uint8_t* blob,
+                                                  const CgParams& p, int s, int n, int nsym, int tid) {
+    const int H = p.H, rows = nsym > 16 ? 32 : 16;
+    const uint16_t* src = reinterpret_cast<const uint16_t*>(blob + cdf_offset(p.L, n)) + p.cdf_prefix[s];
+#pragma unroll
+    for (int j = 0; j < kStreams; ++j) {
+        const int c = chan(tid, j, H);
+        const uint16_t* sc = src + (uint64_t)c * (nsym - 1);
+        table[c] = 0;
+        for (int k = 1; k < rows; ++k) table[k * H + c] = k < nsym ? sc[k - 1] : (uint16_t)0xFFFF;
+    }
+}
+
+// Decode this thread's kStreams streams over the batch's nt tokens and write
+// the dequantised rows.
+template <int kSteps>
+__device__ __forceinline__ void decode_rows(const uint8_t* blob, uint32_t size, uint32_t start,
+                                            const uint32_t (&o)[kStreams], const uint16_t* table, int tid,
+                                            int H, int nsym, const float* deq, const float* max1s, int nt,
+                                            uint8_t* out) {
+    Dec d[kStreams];
+    const uint16_t* tab[kStreams];
+#pragma unroll
+    for (int j = 0; j < kStreams; ++j) {
+        dec_init(d[j], blob, start + o[j], size);
+        tab[j] = table + chan(tid, j, H);
+    }
+    for (int t = 0; t < nt; ++t) {
+        const float m = max1s[t];
+        float y[kStreams];
+#pragma unroll
+        for (int j = 0; j < kStreams; ++j)
+            y[j] = __fmul_rn(deq[dec_symbol<kSteps>(d[j], tab[j], H, nsym, blob, size)], m);
+        uint8_t* row = out + (uint64_t)t * H * 2;
+        *reinterpret_cast<__nv_bfloat162*>(row) = __floats2bfloat162_rn(y[0], y[1]);
+        *reinterpret_cast<__nv_bfloat162*>(row + H) = __floats2bfloat162_rn(y[2], y[3]);
+    }
+}
+
 // ---- decode 2: one CTA per (chunk, batch, kv, layer) region ----
-// grid (nb_max * 2L, chunks).  Shared memory: uint16 table[kMaxSym][H].
-__global__ void __launch_bounds__(kMaxThreads) cg_decode_kernel(const __grid_constant__ CgParams p) {
+// grid (nb_max * 2L, chunks).  Shared memory: uint16 table[nsym_max][H].
+__global__ void __launch_bounds__(kMaxThreads, 1) cg_decode_kernel(const __grid_constant__ CgParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ uint64_t red[32];
-    __shared__ uint32_t sred[32];
+    __shared__ uint32_t sred[64];
     __shared__ float deq[32];
     __shared__ float max1s[kBatch];
     const int gi = blockIdx.y, n = p.ntok[gi], H = p.H, L = p.L;
@@ -573,8 +674,8 @@ __global__ void __launch_bounds__(kMaxThreads) cg_decode_kernel(const __grid_con
     const uint8_t* blob = p.blob_ptrs[gi];
     uint8_t* chunk = const_cast<uint8_t*>(p.chunk_ptrs[gi]);
     if (blob == nullptr || chunk == nullptr) return;   // reported by the totals kernel
-    const int tid = threadIdx.x, c0 = tid * kStreams;
-    const bool active = c0 < H;
+    const int tid = threadIdx.x;
+    const bool active = tid < H / kStreams;
     const int bins = p.bins[s], MAX = bins / 2 - 1, nsym = 2 * MAX + 1;
     const int t0 = b * kBatch, nt = n - t0 < kBatch ? n - t0 : kBatch;
 
@@ -582,24 +683,24 @@ __global__ void __launch_bounds__(kMaxThreads) cg_decode_kernel(const __grid_con
     region_base(reinterpret_cast<const uint32_t*>(p.ws + p.tot_off[gi]), region, nregions, red,
                 &before, &all);
     const uint64_t bytes0 = bytes_offset(L, n, H, p.cdf_entries);
-    if (bytes0 + all != p.sizes[gi]) {          // the lengths do not add up to the blob
+    const uint64_t size = p.sizes[gi];
+    if (bytes0 + all != size) {          // the lengths do not add up to the blob
         if (tid == 0) set_status(p.status, LMKV_ERR_BAD_DATA);
         return;
     }
     uint16_t* table = reinterpret_cast<uint16_t*>(smem);
-    load_table(table, blob, p, s, n, nsym, c0, active);
+    if (active) load_search_table(table, blob, p, s, n, nsym, tid);
     if (tid < nsym) deq[tid] = __fdiv_rn((float)(tid - MAX), (float)MAX);
     const float* max1 = reinterpret_cast<const float*>(blob) + (uint64_t)s * n + t0;
     for (int t = tid; t < nt; t += blockDim.x) max1s[t] = max1[t];
 
     const uint32_t* lengths = reinterpret_cast<const uint32_t*>(blob + lengths_offset(L, n, p.cdf_entries)) +
                               (uint64_t)region * H;
-    uint32_t l[kStreams] = {0, 0, 0, 0};
+    uint32_t l[kStreams] = {0, 0, 0, 0}, o[kStreams];
     if (active)
 #pragma unroll
-        for (int j = 0; j < kStreams; ++j) l[j] = lengths[c0 + j];
-    const uint32_t o = block_exclusive_scan(l[0] + l[1] + l[2] + l[3], sred);   // syncs the block
-    __syncthreads();
+        for (int j = 0; j < kStreams; ++j) l[j] = lengths[chan(tid, j, H)];
+    stream_offsets(l, sred, o);          // also orders the shared-memory writes above
     if (!active) return;
     const uint64_t bound = stream_bound(nt);
     bool bad = false;
@@ -609,29 +710,12 @@ __global__ void __launch_bounds__(kMaxThreads) cg_decode_kernel(const __grid_con
         set_status(p.status, LMKV_ERR_BAD_DATA);
         return;
     }
-    Dec d[kStreams];
-    const uint8_t* src = blob + bytes0 + before + o;
-#pragma unroll
-    for (int j = 0; j < kStreams; ++j) {
-        dec_init(d[j], src, l[j]);
-        src += l[j];
-    }
-    uint8_t* out = chunk + (((uint64_t)s * n + t0) * H + c0) * 2;
-    for (int t = 0; t < nt; ++t) {
-        const float m = max1s[t];
-        float y[kStreams];
-#pragma unroll
-        for (int j = 0; j < kStreams; ++j) {
-            const uint32_t q = dec_symbol(d[j], table + c0 + j, H, nsym);
-            y[j] = __fmul_rn(deq[q], m);
-        }
-        const __nv_bfloat162 a = __floats2bfloat162_rn(y[0], y[1]);
-        const __nv_bfloat162 c = __floats2bfloat162_rn(y[2], y[3]);
-        uint2 v;
-        v.x = *reinterpret_cast<const uint32_t*>(&a);
-        v.y = *reinterpret_cast<const uint32_t*>(&c);
-        *reinterpret_cast<uint2*>(out + (uint64_t)t * H * 2) = v;
-    }
+    const uint32_t start = (uint32_t)(bytes0 + before);
+    uint8_t* out = chunk + ((uint64_t)s * n + t0) * H * 2 + 4 * tid;
+    if (nsym > 16)
+        decode_rows<5>(blob, (uint32_t)size, start, o, table, tid, H, nsym, deq, max1s, nt, out);
+    else
+        decode_rows<4>(blob, (uint32_t)size, start, o, table, tid, H, nsym, deq, max1s, nt, out);
 }
 
 // ---- host side ----
@@ -707,6 +791,11 @@ int run(Dir dir, void* const* chunk_ptrs, void* const* blob_ptrs, uint64_t* size
     uint64_t need = 0;
     rc = workspace_size(L, H, ntok, num_chunks, &need);
     if (rc != LMKV_OK) return rc;
+    for (int32_t g = 0; g < num_chunks; ++g) {
+        lmkv_cachegen_layout_t lay;
+        rc = lmkv_cachegen_layout(L, ntok[g], H, bins, &lay);
+        if (rc != LMKV_OK) return rc;
+    }
     if (need > workspace_bytes) return LMKV_ERR_INVALID_ARG;
     for (int s = 0; s < 2 * L; ++s) p.bins[s] = (uint8_t)bins[s];
     p.L = L;
@@ -715,12 +804,13 @@ int run(Dir dir, void* const* chunk_ptrs, void* const* blob_ptrs, uint64_t* size
     p.ws = static_cast<uint8_t*>(workspace);
     const int threads = threads_for(H);
     const size_t table_bytes = (size_t)max_nsym * H * 2;
+    const size_t search_bytes = (size_t)(max_nsym > 16 ? 32 : 16) * H * 2;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (dir == Dir::kEncode) {
         if (set_smem((const void*)cg_cdf_kernel, table_bytes) != LMKV_OK ||
             set_smem((const void*)cg_code_kernel, table_bytes) != LMKV_OK)
             return LMKV_ERR_CUDA;
-    } else if (set_smem((const void*)cg_decode_kernel, table_bytes) != LMKV_OK) {
+    } else if (set_smem((const void*)cg_decode_kernel, search_bytes) != LMKV_OK) {
         return LMKV_ERR_CUDA;
     }
     uint64_t at = 0;
@@ -749,7 +839,7 @@ int run(Dir dir, void* const* chunk_ptrs, void* const* blob_ptrs, uint64_t* size
             lmkv_internal_add_launches(3);
         } else {
             cg_total_kernel<<<regions, 256, 0, st>>>(p);
-            cg_decode_kernel<<<regions, threads, table_bytes, st>>>(p);
+            cg_decode_kernel<<<regions, threads, search_bytes, st>>>(p);
             lmkv_internal_add_launches(2);
         }
         if (cudaGetLastError() != cudaSuccess) return LMKV_ERR_CUDA;
@@ -787,7 +877,8 @@ int lmkv_cachegen_layout(int32_t num_layers, int32_t num_tokens, int32_t channel
         bound += 2ull * num_layers * channels * stream_bound(nt);
     }
     out->max_bytes = bound;
-    return LMKV_OK;
+    // the kernels address a blob with 32-bit offsets
+    return bound <= kMaxBlobBytes ? LMKV_OK : LMKV_ERR_INVALID_ARG;
 }
 
 int lmkv_cachegen_workspace_bytes(int32_t num_layers, int32_t channels, const int32_t* num_tokens,

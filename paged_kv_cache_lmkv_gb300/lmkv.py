@@ -506,18 +506,31 @@ class CachegenCodec:
         if sizes is None:
             sizes = torch.zeros(len(chunks), dtype=torch.int64, device=self.device)
         ws = self._workspace(ntok)
-        check(cachegen_encode(pointer_array(chunks, self.device), ntok, self.num_layers, self.channels,
-                              self.bins, pointer_array(blobs, self.device), sizes, ws, status, stream),
-              "lmkv_cachegen_encode")
+        cptr, bptr = pointer_array(chunks, self.device), pointer_array(blobs, self.device)
+        self._order(stream, cptr, bptr)
+        check(cachegen_encode(cptr, ntok, self.num_layers, self.channels, self.bins, bptr, sizes, ws,
+                              status, stream), "lmkv_cachegen_encode")
         return blobs, sizes
+
+    def _order(self, stream, *arrays):
+        """The pointer arrays are written on the current stream: a different
+        `stream` waits for them and keeps them alive until it has read them."""
+        if stream is None:
+            return
+        cur = torch.cuda.current_stream(self.device)
+        if isinstance(stream, torch.cuda.Stream) and stream != cur:
+            stream.wait_stream(cur)
+            for a in arrays:
+                a.record_stream(stream)
 
     def decode(self, blobs, sizes, chunks, status=None, stream=None):
         """Decode into the chunk tensors (their token counts give n)."""
         ntok = [int(c.shape[2]) for c in chunks]
         ws = self._workspace(ntok)
-        check(cachegen_decode(pointer_array(blobs, self.device), sizes, ntok, self.num_layers,
-                              self.channels, self.bins, pointer_array(chunks, self.device), ws, status,
-                              stream), "lmkv_cachegen_decode")
+        bptr, cptr = pointer_array(blobs, self.device), pointer_array(chunks, self.device)
+        self._order(stream, bptr, cptr)
+        check(cachegen_decode(bptr, sizes, ntok, self.num_layers, self.channels, self.bins, cptr, ws,
+                              status, stream), "lmkv_cachegen_decode")
         return chunks
 
 
