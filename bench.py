@@ -63,7 +63,9 @@ def parse_args():
                     help="skip the CacheGen codec measurement")
     ap.add_argument("--no-pipeline", action="store_true",
                     help="skip the layer-wise pipeline measurement (host round trip per layer)")
-    ap.add_argument("--case", choices=["llama8b", "profile-small"], default="llama8b",
+    ap.add_argument("--codec-chunks", type=int, default=40,
+                    help="--case codec: number of 256-token chunks")
+    ap.add_argument("--case", choices=["llama8b", "profile-small", "codec"], default="llama8b",
                     help="profile-small: the 8B shape with a 1024-block pool and a 4096-token "
                          "request (16 chunks), for ncu captures only")
     return ap.parse_args()
@@ -600,6 +602,41 @@ def bench_cachegen(c: Ctx, clk_mhz, reps: int = 5):
     return out
 
 
+def bench_codec_only(args):
+    """--case codec: the codec alone on --codec-chunks chunks of 256 tokens of
+    the 8B shape (N(0,1) bf16 drawn on the device from a seeded generator),
+    warm-up + --steps rounds of encode then decode; one JSON line.  This is the
+    command the codec's ncu summaries are taken with."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    pkg.lmkv.load()
+    w = wl.LLAMA8B
+    L, H = w.num_layers, w.row_elems
+    chunks = [wl.fill_normal_(torch.empty((2, L, 256, H), dtype=torch.bfloat16, device=dev), 100 + g)
+              for g in range(args.codec_chunks)]
+    codec = pkg.CachegenCodec(L, H, device=dev)
+    blobs, sizes = codec.encode(chunks)
+    outs = [torch.empty_like(x) for x in chunks]
+    for _ in range(args.warmup):
+        codec.encode(chunks, blobs, sizes)
+        codec.decode(blobs, sizes, outs)
+    torch.cuda.synchronize(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    ev[0].record()
+    for _ in range(args.steps):
+        codec.encode(chunks, blobs, sizes)
+    ev[1].record()
+    for _ in range(args.steps):
+        codec.decode(blobs, sizes, outs)
+    ev[2].record()
+    torch.cuda.synchronize(dev)
+    raw = sum(x.numel() * 2 for x in chunks)
+    print(json.dumps({"case": "codec", "chunks": args.codec_chunks,
+                      "encode_ms": round(ev[0].elapsed_time(ev[1]) / max(1, args.steps), 4),
+                      "decode_ms": round(ev[1].elapsed_time(ev[2]) / max(1, args.steps), 4),
+                      "ratio": round(raw / int(sizes.sum().item()), 4)}), flush=True)
+
+
 def profiled_codec_instructions():
     """Warp instructions per coded symbol of the encode and decode calls, from
     the committed ncu summary, if it was taken on the current kernel source."""
@@ -764,6 +801,9 @@ def main():
     args = parse_args()
     if args.impl == "reference":
         bench_reference(args)
+        return
+    if args.case == "codec":
+        bench_codec_only(args)
         return
     rank, world, local = dist_env()
     if world > 1:
