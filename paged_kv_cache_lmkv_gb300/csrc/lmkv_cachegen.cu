@@ -39,8 +39,6 @@ constexpr int kStreams = 4;                    // channels (streams) per thread
 constexpr int kRows = 8;                       // rows per block-wide absmax round
 constexpr int kMaxThreads = LMKV_CACHEGEN_MAX_CHANNELS / kStreams;
 constexpr uint64_t kMaxBlobBytes = 0xFFFFFF00ull;   // blobs are addressed with 32-bit offsets
-constexpr uint32_t kHalf = 0x80000000u;
-constexpr uint32_t kQuarter = 0x40000000u;
 
 struct CgParams {
     const uint8_t* const* chunk_ptrs;   // DEVICE array of chunk buffers
@@ -467,7 +465,11 @@ __device__ __forceinline__ void load_table(uint16_t* table, const uint8_t* blob,
 
 // ---- encode 2: one CTA per (chunk, batch, kv, layer) region ----
 // grid (nb_max * 2L, chunks).  Shared memory: uint16 table[nsym_max][H].
-__global__ void __launch_bounds__(kMaxThreads, 1) cg_code_kernel(const __grid_constant__ CgParams p) {
+// kThreads = 256 (up to 1024 channels) lets three CTAs share an SM's
+// registers; 512 covers up to 2048 channels.
+template <int kThreads>
+__global__ void __launch_bounds__(kThreads, kThreads == 256 ? 3 : 1)
+cg_code_kernel(const __grid_constant__ CgParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ uint64_t red[32];
     const int gi = blockIdx.y, n = p.ntok[gi], H = p.H, L = p.L;
@@ -661,7 +663,9 @@ __device__ __forceinline__ void decode_rows(const uint8_t* blob, uint32_t size, 
 
 // ---- decode 2: one CTA per (chunk, batch, kv, layer) region ----
 // grid (nb_max * 2L, chunks).  Shared memory: uint16 table[nsym_max][H].
-__global__ void __launch_bounds__(kMaxThreads, 1) cg_decode_kernel(const __grid_constant__ CgParams p) {
+template <int kThreads>
+__global__ void __launch_bounds__(kThreads, kThreads == 256 ? 3 : 1)
+cg_decode_kernel(const __grid_constant__ CgParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ uint64_t red[32];
     __shared__ uint32_t sred[64];
@@ -767,10 +771,14 @@ int workspace_size(int32_t L, int32_t H, const int32_t* ntok, int32_t num_chunks
 
 int threads_for(int H) { return ((H / kStreams + 31) / 32) * 32; }
 
+// Allow `bytes` of dynamic shared memory and ask for the largest shared
+// memory carve-out, so that as many CTAs fit per SM as their tables allow.
 int set_smem(const void* fn, size_t bytes) {
-    if (bytes <= 48 * 1024) return LMKV_OK;
-    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) == cudaSuccess
-               ? LMKV_OK : LMKV_ERR_CUDA;
+    if (bytes > 48 * 1024 &&
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
+        return LMKV_ERR_CUDA;
+    return cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                cudaSharedmemCarveoutMaxShared) == cudaSuccess ? LMKV_OK : LMKV_ERR_CUDA;
 }
 
 enum class Dir { kEncode, kDecode };
@@ -803,14 +811,17 @@ int run(Dir dir, void* const* chunk_ptrs, void* const* blob_ptrs, uint64_t* size
     p.status = d_status;
     p.ws = static_cast<uint8_t*>(workspace);
     const int threads = threads_for(H);
+    const bool wide = threads > 256;
     const size_t table_bytes = (size_t)max_nsym * H * 2;
     const size_t search_bytes = (size_t)(max_nsym > 16 ? 32 : 16) * H * 2;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (dir == Dir::kEncode) {
         if (set_smem((const void*)cg_cdf_kernel, table_bytes) != LMKV_OK ||
-            set_smem((const void*)cg_code_kernel, table_bytes) != LMKV_OK)
+            set_smem(wide ? (const void*)cg_code_kernel<512> : (const void*)cg_code_kernel<256>,
+                     table_bytes) != LMKV_OK)
             return LMKV_ERR_CUDA;
-    } else if (set_smem((const void*)cg_decode_kernel, search_bytes) != LMKV_OK) {
+    } else if (set_smem(wide ? (const void*)cg_decode_kernel<512> : (const void*)cg_decode_kernel<256>,
+                        search_bytes) != LMKV_OK) {
         return LMKV_ERR_CUDA;
     }
     uint64_t at = 0;
@@ -834,12 +845,14 @@ int run(Dir dir, void* const* chunk_ptrs, void* const* blob_ptrs, uint64_t* size
         const dim3 slices(2 * L, cnt), regions(nb_max * 2 * L, cnt);
         if (dir == Dir::kEncode) {
             cg_cdf_kernel<<<slices, threads, table_bytes, st>>>(p);
-            cg_code_kernel<<<regions, threads, table_bytes, st>>>(p);
+            if (wide) cg_code_kernel<512><<<regions, threads, table_bytes, st>>>(p);
+            else cg_code_kernel<256><<<regions, threads, table_bytes, st>>>(p);
             cg_compact_kernel<<<regions, threads, (size_t)H * 8, st>>>(p);
             lmkv_internal_add_launches(3);
         } else {
             cg_total_kernel<<<regions, 256, 0, st>>>(p);
-            cg_decode_kernel<<<regions, threads, search_bytes, st>>>(p);
+            if (wide) cg_decode_kernel<512><<<regions, threads, search_bytes, st>>>(p);
+            else cg_decode_kernel<256><<<regions, threads, search_bytes, st>>>(p);
             lmkv_internal_add_launches(2);
         }
         if (cudaGetLastError() != cudaSuccess) return LMKV_ERR_CUDA;
