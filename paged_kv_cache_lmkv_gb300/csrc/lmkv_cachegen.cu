@@ -108,9 +108,11 @@ __device__ __forceinline__ int chan(int tid, int j, int H) {
 }
 
 // ---- arithmetic encoder state, one per stream ----
+// Bit strings are moved with the funnel shifts of two 32-bit words (a shift
+// by a variable amount of a 64-bit integer is not one instruction).
 struct Enc {
     uint32_t low, high, follow, nacc, words;
-    uint64_t acc;          // output bits not yet stored, the last nacc valid
+    uint32_t acc_hi, acc_lo;   // output bits not yet stored: the last nacc of acc_hi:acc_lo
 };
 
 __device__ __forceinline__ void enc_init(Enc& e) {
@@ -119,24 +121,29 @@ __device__ __forceinline__ void enc_init(Enc& e) {
     e.follow = 0;
     e.nacc = 0;
     e.words = 0;
-    e.acc = 0;
+    e.acc_hi = 0;
+    e.acc_lo = 0;
 }
 
 // Append the c (0..32) bits v (nothing above them set); a completed 32-bit
 // word goes to the slot, most significant byte first.
 __device__ __forceinline__ void put_bits(Enc& e, uint32_t v, uint32_t c, uint32_t* slot,
                                          uint32_t cap_words, bool& overflow) {
-    e.acc = (e.acc << c) | v;
+    e.acc_hi = __funnelshift_lc(e.acc_lo, e.acc_hi, c);
+    e.acc_lo = __funnelshift_lc(0u, e.acc_lo, c) | v;
     e.nacc += c;
     const bool full = e.nacc >= 32;
     e.nacc -= full ? 32u : 0u;
-    const uint32_t w = (uint32_t)(e.acc >> e.nacc);
+    const uint32_t w = __funnelshift_rc(e.acc_lo, e.acc_hi, e.nacc);
     if (full) {
         if (e.words < cap_words) slot[e.words] = __byte_perm(w, 0, 0x0123);
         else overflow = true;
     }
     e.words += full ? 1u : 0u;
 }
+
+// 2^f - 1 for 0 <= f <= 32.
+__device__ __forceinline__ uint32_t ones(uint32_t f) { return __funnelshift_rc(0xFFFFFFFFu, 0u, 32 - f); }
 
 // The rare case of more than 32 bits at once (a long run of held bits):
 // `bit`, then `f` opposite bits, then the k-1 bits `rest`.
@@ -145,7 +152,7 @@ __device__ __forceinline__ void emit_long(Enc& e, uint32_t bit, uint32_t f, uint
     put_bits(e, bit, 1, slot, cap_words, overflow);
     for (uint32_t left = f; left > 0;) {
         const uint32_t c = left < 32 ? left : 32;
-        put_bits(e, bit ? 0u : (uint32_t)((1ull << c) - 1), c, slot, cap_words, overflow);
+        put_bits(e, bit ? 0u : ones(c), c, slot, cap_words, overflow);
         left -= c;
     }
     put_bits(e, rest, k - 1, slot, cap_words, overflow);
@@ -174,11 +181,10 @@ __device__ __forceinline__ void enc_symbol(Enc& e, uint32_t lo, uint32_t hi, uin
     // The k decided bits are the top k bits of the true low.  "b" followed by
     // f copies of "not b" is the number 2^f - 1 + b, so the run is
     // top_k(true low) + (2^f - 1) * 2^(k-1).
-    const uint32_t first = (uint32_t)((uint64_t)(f ? 1u : 0u) << k) >> 1;   // bit 31's place, or 0
-    const uint32_t topk = __funnelshift_rc(e.low, 0u, 32 - k) ^ first;     // 0 when k == 0
+    const uint32_t topk = __funnelshift_rc(e.low ^ (f ? 0x80000000u : 0u), 0u, 32 - k);  // 0 if k == 0
     if (f + k <= 32) {
-        const uint32_t held = (uint32_t)((((1ull << f) - 1) << k) >> 1);
-        put_bits(e, k ? topk + held : 0u, k ? f + k : 0u, slot, cap_words, overflow);
+        const uint32_t held = k ? ones(f) << (k - 1) : 0u;
+        put_bits(e, topk + held, k ? f + k : 0u, slot, cap_words, overflow);
     } else if (k) {
         emit_long(e, topk >> (k - 1), f, k, topk & ((1u << (k - 1)) - 1), slot, cap_words, overflow);
     }
@@ -197,7 +203,7 @@ __device__ __forceinline__ uint32_t enc_finish(Enc& e, uint32_t* slot, uint32_t 
     const uint32_t bit = (e.low >> 30) & 1u;                   // true low >= 2^30
     const uint32_t f = e.follow + 1;
     if (f + 1 <= 32) {
-        const uint32_t run = bit ? 0u : (uint32_t)((1ull << f) - 1);
+        const uint32_t run = bit ? 0u : ones(f);
         put_bits(e, (bit << f) | run, f + 1, slot, cap_words, overflow);
     } else {
         emit_long(e, bit, f, 1, 0, slot, cap_words, overflow);
@@ -205,7 +211,7 @@ __device__ __forceinline__ uint32_t enc_finish(Enc& e, uint32_t* slot, uint32_t 
     e.follow = 0;
     const uint32_t bits = e.words * 32 + e.nacc;
     if (e.nacc) {
-        const uint32_t w = (uint32_t)(e.acc << (32 - e.nacc));
+        const uint32_t w = e.acc_lo << (32 - e.nacc);
         if (e.words < cap_words) slot[e.words] = __byte_perm(w, 0, 0x0123);
         else overflow = true;
     }
@@ -225,7 +231,7 @@ struct Dec {
     uint32_t low, high, value, nbuf;
     uint32_t q;              // blob offset of the next word to load
     uint32_t next;           // the word at q - 4 as loaded, ahead of its use
-    uint64_t buf;            // upcoming bits, most significant first; nbuf valid
+    uint32_t buf_hi, buf_lo; // upcoming bits, most significant first; nbuf valid
 };
 
 // The aligned word at blob offset q as stored (little-endian load); bytes at
@@ -243,7 +249,9 @@ __device__ __forceinline__ uint32_t load_word(const uint8_t* blob, uint32_t q, u
 // loaded now and used by the next refill.
 __device__ __forceinline__ void dec_refill(Dec& d, const uint8_t* blob, uint32_t size) {
     if (d.nbuf <= 32) {
-        d.buf |= (uint64_t)__byte_perm(d.next, 0, 0x0123) << (32 - d.nbuf);
+        const uint32_t w = __byte_perm(d.next, 0, 0x0123);     // placed at bit 64 - nbuf - 32
+        d.buf_hi |= __funnelshift_rc(w, 0u, d.nbuf);
+        d.buf_lo |= __funnelshift_lc(0u, w, 32 - d.nbuf);
         d.nbuf += 32;
         d.next = load_word(blob, d.q, size);
         d.q += 4;
@@ -252,8 +260,9 @@ __device__ __forceinline__ void dec_refill(Dec& d, const uint8_t* blob, uint32_t
 
 // The next c (0..32) bits.
 __device__ __forceinline__ uint32_t dec_take(Dec& d, uint32_t c) {
-    const uint32_t r = __funnelshift_lc((uint32_t)(d.buf >> 32), 0u, c);
-    d.buf <<= c;
+    const uint32_t r = __funnelshift_lc(d.buf_hi, 0u, c);
+    d.buf_hi = __funnelshift_lc(d.buf_lo, d.buf_hi, c);
+    d.buf_lo = __funnelshift_lc(0u, d.buf_lo, c);
     d.nbuf -= c;
     return r;
 }
@@ -262,7 +271,8 @@ __device__ __forceinline__ uint32_t dec_take(Dec& d, uint32_t c) {
 // `size` bytes long).
 __device__ __forceinline__ void dec_init(Dec& d, const uint8_t* blob, uint32_t start, uint32_t size) {
     const uint32_t a = start & ~3u, sh = start - a;
-    d.buf = (uint64_t)(__byte_perm(load_word(blob, a, size), 0, 0x0123) << (8 * sh)) << 32;
+    d.buf_hi = __byte_perm(load_word(blob, a, size), 0, 0x0123) << (8 * sh);
+    d.buf_lo = 0;
     d.nbuf = 32 - 8 * sh;
     d.next = load_word(blob, a + 4, size);
     d.q = a + 8;
@@ -403,25 +413,26 @@ __global__ void __launch_bounds__(kMaxThreads) cg_cdf_kernel(const __grid_consta
             if (lane == 0) part[buf][r][warp] = m;
         }
         __syncthreads();
+        // lane r of every warp finishes row r: the max over the warps' partial
+        // maxima and factor = MAX / max1 (IEEE division; 0 for an all-zero row,
+        // which then quantises to MAX everywhere); the other lanes get them by
+        // shuffles
+        uint32_t mb = 0;
+        if (lane < kRows)
+            for (int w = 0; w < nw; ++w) mb = mb > part[buf][lane][w] ? mb : part[buf][lane][w];
+        const float mrow = __uint_as_float(mb);
+        const float frow = mb ? __fdiv_rn(maxf, mrow) : 0.0f;
+        if (warp == 0 && lane < kRows && t0 + lane < n) max1_out[t0 + lane] = mrow;
 #pragma unroll
         for (int r = 0; r < kRows; ++r) {
             const int t = t0 + r;
-            if (t >= n) break;
-            uint32_t mb = 0;
-            for (int w = 0; w < nw; ++w) mb = mb > part[buf][r][w] ? mb : part[buf][r][w];
-            const float m = __uint_as_float(mb);
-            if (tid == r) max1_out[t] = m;
-            if (!active) continue;
+            const float factor = __shfl_sync(0xFFFFFFFFu, frow, r);
+            if (t >= n || !active) continue;
             uint32_t q[kStreams];
-            if (m == 0.0f) {
-                q[0] = q[1] = q[2] = q[3] = (uint32_t)MAX;
-            } else {
-                const float factor = __fdiv_rn(maxf, m);
-                q[0] = quantise(bf16_lo(v[r].x), factor, maxf, 2 * MAX);
-                q[1] = quantise(bf16_hi(v[r].x), factor, maxf, 2 * MAX);
-                q[2] = quantise(bf16_lo(v[r].y), factor, maxf, 2 * MAX);
-                q[3] = quantise(bf16_hi(v[r].y), factor, maxf, 2 * MAX);
-            }
+            q[0] = quantise(bf16_lo(v[r].x), factor, maxf, 2 * MAX);
+            q[1] = quantise(bf16_hi(v[r].x), factor, maxf, 2 * MAX);
+            q[2] = quantise(bf16_lo(v[r].y), factor, maxf, 2 * MAX);
+            q[3] = quantise(bf16_hi(v[r].y), factor, maxf, 2 * MAX);
             sym[(uint64_t)t * (H / 4)] = q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24);
 #pragma unroll
             for (int j = 0; j < kStreams; ++j) hist[q[j] * H + chan(tid, j, H)] += 1;
