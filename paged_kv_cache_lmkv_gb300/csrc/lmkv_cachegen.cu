@@ -70,10 +70,11 @@ __host__ __device__ inline uint64_t bytes_offset(int L, int n, int H, int cdf_en
 // 2^14 of at most 2^32 and each emitted or pending bit doubles it, so at most
 // 18 bits per symbol, plus the two final bits.
 __host__ __device__ inline uint64_t stream_bound(int nt) { return (18ull * nt + 2 + 7) / 8; }
-// Slot stride in the workspace: the bound rounded up to 16 bytes.
+// Slot stride in the workspace: the bound plus 4 bytes (the compaction reads
+// one word past a stream), rounded up to 16 bytes.
 __host__ __device__ inline uint64_t slot_stride(int n) {
     const int nt = n < kBatch ? n : kBatch;
-    return (stream_bound(nt) + 15) & ~15ull;
+    return (stream_bound(nt) + 4 + 15) & ~15ull;
 }
 
 __device__ __forceinline__ void set_status(int32_t* st, int code) {
@@ -497,7 +498,7 @@ cg_code_kernel(const __grid_constant__ CgParams p) {
     __syncthreads();
 
     const uint64_t stride = slot_stride(n);
-    const uint32_t cap_words = (uint32_t)(stride / 4);
+    const uint32_t cap_words = (uint32_t)((stride - 4) / 4);     // keep the slack word free
     uint32_t len[kStreams] = {0, 0, 0, 0};
     bool overflow = false;
     if (active) {
@@ -593,16 +594,31 @@ __global__ void __launch_bounds__(kMaxThreads) cg_compact_kernel(const __grid_co
             lens[chan(tid, j, H)] = l[j];
         }
     __syncthreads();
-    // one warp per stream, lanes on consecutive bytes
+    // One warp per stream.  The destination is byte-aligned: the bytes before
+    // its first 4-byte boundary and after its last are copied one by one
+    // (those words are shared with the neighbouring streams), the words in
+    // between whole, each assembled from two aligned words of the slot.
     const int lane = tid & 31, warp = tid >> 5, nw = (blockDim.x + 31) >> 5;
     const uint64_t stride = slot_stride(n);
     uint8_t* dst0 = blob + bytes0 + before;
     const uint8_t* src0 = p.ws + p.slot_off[gi] + (uint64_t)region * H * stride;
     for (int c = warp; c < H; c += nw) {
-        const uint32_t nbytes = lens[c];
-        const uint8_t* src = src0 + (uint64_t)c * stride;
+        const uint32_t len = lens[c];
+        const uint8_t* src = src0 + (uint64_t)c * stride;          // 16-byte aligned
         uint8_t* dst = dst0 + off[c];
-        for (uint32_t i = lane; i < nbytes; i += 32) dst[i] = src[i];
+        uint32_t head = (uint32_t)(-reinterpret_cast<uintptr_t>(dst)) & 3u;
+        head = head < len ? head : len;
+        const uint32_t words = (len - head) >> 2;
+        const uint32_t body = head + 4 * words, tail = len - body;
+        if ((uint32_t)lane < head) dst[lane] = src[lane];
+        if ((uint32_t)lane < tail) dst[body + lane] = src[body + lane];
+        const uint32_t sh = head;                                 // source misalignment
+        const uint32_t* sw = reinterpret_cast<const uint32_t*>(src);
+        uint32_t* dw = reinterpret_cast<uint32_t*>(dst + head);
+        for (uint32_t i = lane; i < words; i += 32) {
+            const uint32_t lo = sw[i], hi = sw[i + 1];           // i + 1 stays in the slot's slack
+            dw[i] = sh ? __funnelshift_r(lo, hi, 8 * sh) : lo;
+        }
     }
 }
 
