@@ -590,6 +590,41 @@ def bench_cachegen(c: Ctx, clk_mhz, reps: int = 5):
                            "peak": round(peak / 1e9, 1),
                            "peak_source": "152 SMs x 4 schedulers x 1 issue/clock x sampled SM clock",
                            **roof}
+    # the fused store / retrieve: pool pages <-> blobs in one pass, against the
+    # two-step path (gather then encode, decode then scatter) on the same batch
+    a = (w.starts, w.ends, w.chunk_size, w.save_unfull)
+    ntok = [n for _, _, n in c.chunks]
+    blobs = [torch.empty(codec.layout(n).max_bytes, dtype=torch.uint8, device=c.dev) for n in ntok]
+    bptr = pkg.pointer_array(blobs, c.dev)
+    sizes = torch.zeros(len(ntok), dtype=torch.int64, device=c.dev)
+    ws = codec._workspace(ntok)
+    torch.cuda.synchronize(c.dev)
+    calls = {
+        "store_fused": lambda: pkg.check(lib.cachegen_store_chunks(c.pool, c.bt, *a, codec.bins, bptr, sizes, ws,
+                                                                   c.status, stream)),
+        "retrieve_fused": lambda: pkg.check(lib.cachegen_retrieve_chunks(c.pool2, c.bt2, *a, codec.bins, bptr,
+                                                                         sizes, ws, c.status, stream)),
+        "gather": lambda: pkg.check(pkg.gather_chunks(c.pool, c.bt, *a, c.ptrs, c.status, stream)),
+        "scatter": lambda: pkg.check(pkg.scatter_chunks(c.pool2, c.bt2, *a, c.ptrs, c.status, stream)),
+    }
+    times = {}
+    for name in ("store_fused", "retrieve_fused", "gather", "scatter"):
+        for _ in range(2):
+            calls[name]()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            calls[name]()
+        e1.record(stream)
+        torch.cuda.synchronize(c.dev)
+        times[name] = e0.elapsed_time(e1) / reps
+    raw = main["_symbols"] * 2
+    out["store_fused_ms"] = round(times["store_fused"], 3)
+    out["store_two_step_ms"] = round(times["gather"] + main["_te"], 3)
+    out["retrieve_fused_ms"] = round(times["retrieve_fused"], 3)
+    out["retrieve_two_step_ms"] = round(main["_td"] + times["scatter"], 3)
+    out["store_fused_GBps_raw"] = round(raw / (times["store_fused"] * 1e-3) / 1e9, 1)
+    out["retrieve_fused_GBps_raw"] = round(raw / (times["retrieve_fused"] * 1e-3) / 1e9, 1)
     sweep = {}
     for C in wl.CACHEGEN_CHUNK_SIZES:
         ntoks = [C] * (10240 // C) + ([10240 % C] if 10240 % C else [])

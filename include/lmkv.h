@@ -447,6 +447,35 @@ int lmkv_cachegen_decode(void* const* blob_ptrs, const uint64_t* sizes, const in
                          const int32_t* bins, void* const* chunk_ptrs, void* workspace,
                          uint64_t workspace_bytes, int32_t* d_status, void* stream);
 
+/* Store with CacheGen: the chunks of a store call (enumerated and validated
+ * exactly as lmkv_gather_chunks does; same pool, block_table, max_blocks,
+ * start, end, num_req, chunk_size, save_unfull_chunk) are encoded straight
+ * from the pool's pages into DEVICE blob_ptrs[g] / sizes[g], without a chunk
+ * buffer in between: the quantise pass reads each token row from its page.
+ * The result equals lmkv_gather_chunks followed by lmkv_cachegen_encode.
+ * bf16 pools only (UNSUPPORTED otherwise); H = num_kv_heads * head_dim and
+ * chunk_size within the codec's limits; the workspace as
+ * lmkv_cachegen_workspace_bytes for the chunks' token counts.  A row in a
+ * block with an id outside [0, num_blocks) is coded as zeros and sets
+ * *d_status to BAD_BLOCK. */
+int lmkv_cachegen_store_chunks(const lmkv_pool_t* pool, const int32_t* block_table, int32_t max_blocks,
+                               const int64_t* start, const int64_t* end, int32_t num_req,
+                               int32_t chunk_size, int32_t save_unfull_chunk, const int32_t* bins,
+                               void* const* blob_ptrs, uint64_t* sizes, void* workspace,
+                               uint64_t workspace_bytes, int32_t* d_status, void* stream);
+
+/* Retrieve with CacheGen: decode blob g straight into the pages of chunk g
+ * of the call (the inverse of lmkv_cachegen_store_chunks; equal to
+ * lmkv_cachegen_decode followed by lmkv_scatter_chunks).  Rows in a block with
+ * a bad id are not written and set BAD_BLOCK; an inconsistent blob is not
+ * decoded and sets BAD_DATA. */
+int lmkv_cachegen_retrieve_chunks(const lmkv_pool_t* pool, const int32_t* block_table,
+                                  int32_t max_blocks, const int64_t* start, const int64_t* end,
+                                  int32_t num_req, int32_t chunk_size, int32_t save_unfull_chunk,
+                                  const int32_t* bins, void* const* blob_ptrs, const uint64_t* sizes,
+                                  void* workspace, uint64_t workspace_bytes, int32_t* d_status,
+                                  void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* lmkv_status_string(int status);
 

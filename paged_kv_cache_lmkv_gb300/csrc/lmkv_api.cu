@@ -528,6 +528,27 @@ void* noalloc_staging_address() {
 
 void lmkv_internal_add_launches(int64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
+int lmkv_internal_list_chunks(const lmkv_pool_t* pool, const int32_t* block_table, int32_t max_blocks,
+                              const int64_t* start, const int64_t* end, int32_t num_req,
+                              int32_t chunk_size, int32_t save_unfull, std::vector<LmkvChunkRef>* out) {
+    Call c{pool, block_table, max_blocks, start, end, num_req, chunk_size, save_unfull,
+           nullptr, nullptr, 0, pool ? pool->num_layers : 1, 1, 0, 0, nullptr};
+    static void* const kAny = nullptr;
+    c.chunk_ptrs = &kAny;                 // the codec passes its blobs separately
+    const int rc = validate(c);
+    if (rc != LMKV_OK) return rc;
+    out->clear();
+    for (int32_t r = 0; r < num_req; ++r) {
+        const int64_t nch = request_chunks(start[r], end[r], chunk_size, save_unfull);
+        for (int64_t j = 0; j < nch; ++j) {
+            const int64_t t0 = start[r] + j * chunk_size;
+            const int64_t n = end[r] - t0 < chunk_size ? end[r] - t0 : chunk_size;
+            out->push_back(LmkvChunkRef{r, t0, (int32_t)n});
+        }
+    }
+    return LMKV_OK;
+}
+
 extern "C" {
 
 int lmkv_count_chunks(const int64_t* start, const int64_t* end, int32_t num_req,

@@ -29,6 +29,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <vector>
 
 namespace {
 
@@ -41,7 +42,7 @@ constexpr int kMaxThreads = LMKV_CACHEGEN_MAX_CHANNELS / kStreams;
 constexpr uint64_t kMaxBlobBytes = 0xFFFFFF00ull;   // blobs are addressed with 32-bit offsets
 
 struct CgParams {
-    const uint8_t* const* chunk_ptrs;   // DEVICE array of chunk buffers
+    const uint8_t* const* chunk_ptrs;   // DEVICE array of chunk buffers (chunk form), else null
     uint8_t* const* blob_ptrs;          // DEVICE array of blobs
     uint64_t* sizes;                    // DEVICE blob sizes (encode writes, decode reads)
     int32_t* status;
@@ -53,7 +54,76 @@ struct CgParams {
     uint64_t slot_off[kMaxChunks];
     int32_t cdf_prefix[kMaxSlices];     // cdf entries before slice s
     uint8_t bins[kMaxSlices];
+    // Pool form (layer_base != null): chunk gi is tokens [chunk_tok0, chunk_tok0 +
+    // ntok) of block-table row chunk_req, rows read from / written to the pages.
+    const uint8_t* const* layer_base;   // DEVICE array of per-layer pool bases
+    const int32_t* block_table;
+    int64_t num_blocks;
+    int32_t bt_stride, block_size;
+    int32_t chunk_req[kMaxChunks];
+    int64_t chunk_tok0[kMaxChunks];
 };
+
+// The token rows of one (chunk, K/V, layer) slice, walked in token order:
+// consecutive rows of the chunk buffer, or the rows of the chunk's pages in
+// the pool (one block-table entry per block; an id outside [0, num_blocks)
+// gives null rows).
+struct Rows {
+    const uint8_t* cur;        // chunk form: this row; pool form: the current block's first row
+    const uint8_t* layer;      // pool form: K or V half of the layer
+    const int32_t* bt;         // pool form: the request's block-table row
+    uint32_t row_bytes;
+    int32_t col, slot, B;
+    int64_t nb;
+    bool pool;
+};
+
+__device__ __forceinline__ const uint8_t* block_rows(const Rows& R, int32_t blk) {
+    return (blk >= 0 && blk < R.nb) ? R.layer + (uint64_t)blk * R.B * R.row_bytes : nullptr;
+}
+
+// Rows of slice s of chunk gi from token t (chunk-relative) on.
+__device__ __forceinline__ void rows_init(Rows& R, const CgParams& p, int gi, int s, int n, int t) {
+    R.row_bytes = (uint32_t)p.H * 2;
+    R.pool = p.layer_base != nullptr;
+    if (!R.pool) {
+        R.cur = p.chunk_ptrs[gi] + ((uint64_t)s * n + t) * R.row_bytes;
+        return;
+    }
+    const int kv = s / p.L, l = s % p.L;
+    R.B = p.block_size;
+    R.nb = p.num_blocks;
+    R.layer = p.layer_base[l] + (uint64_t)kv * p.num_blocks * p.block_size * R.row_bytes;
+    R.bt = p.block_table + (uint64_t)p.chunk_req[gi] * p.bt_stride;
+    const int64_t tok = p.chunk_tok0[gi] + t;
+    R.col = (int32_t)(tok / R.B);
+    R.slot = (int32_t)(tok % R.B);
+    R.cur = block_rows(R, R.bt[R.col]);
+}
+
+__device__ __forceinline__ const uint8_t* rows_ptr(const Rows& R) {
+    if (!R.pool) return R.cur;
+    return R.cur ? R.cur + (uint64_t)R.slot * R.row_bytes : nullptr;
+}
+
+// Step to the next row; `more` says whether it exists (so no block-table entry
+// past the request's last block is read).
+__device__ __forceinline__ void rows_next(Rows& R, bool more) {
+    if (!R.pool) {
+        R.cur += R.row_bytes;
+        return;
+    }
+    if (++R.slot == R.B) {
+        R.slot = 0;
+        ++R.col;
+        if (more) R.cur = block_rows(R, R.bt[R.col]);
+    }
+}
+
+// The chunk's rows are there to be read or written.
+__device__ __forceinline__ bool has_rows(const CgParams& p, int gi) {
+    return p.layer_base != nullptr || p.chunk_ptrs[gi] != nullptr;
+}
 
 __host__ __device__ inline int nsym_of(int bins) { return 2 * (bins / 2 - 1) + 1; }
 __host__ __device__ inline int batches_of(int n) { return (n + kBatch - 1) / kBatch; }
@@ -378,9 +448,8 @@ __global__ void __launch_bounds__(kMaxThreads) cg_cdf_kernel(const __grid_consta
     const bool active = tid < H / kStreams;
     uint16_t* hist = reinterpret_cast<uint16_t*>(smem);
 
-    const uint8_t* chunk = p.chunk_ptrs[gi];
     uint8_t* blob = p.blob_ptrs[gi];
-    if (chunk == nullptr || blob == nullptr) {
+    if (!has_rows(p, gi) || blob == nullptr) {
         if (tid == 0) set_status(p.status, LMKV_ERR_BAD_POINTER);
         return;
     }
@@ -391,7 +460,9 @@ __global__ void __launch_bounds__(kMaxThreads) cg_cdf_kernel(const __grid_consta
         }
 
     // this thread's two bf16 pairs of a row: channels (2t, 2t+1) and (H/2 + 2t, H/2 + 2t + 1)
-    const uint8_t* x = chunk + (uint64_t)s * n * H * 2 + 4 * tid;
+    Rows rows;
+    rows_init(rows, p, gi, s, n, 0);
+    bool bad_row = false;
     uint32_t* sym = reinterpret_cast<uint32_t*>(p.ws + p.sym_off[gi] + (uint64_t)s * n * H) + tid;
     float* max1_out = reinterpret_cast<float*>(blob) + (uint64_t)s * n;
     const float maxf = (float)MAX;
@@ -401,10 +472,15 @@ __global__ void __launch_bounds__(kMaxThreads) cg_cdf_kernel(const __grid_consta
 #pragma unroll
         for (int r = 0; r < kRows; ++r) {
             v[r] = make_uint2(0, 0);
-            if (active && t0 + r < n) {
-                const uint8_t* row = x + (uint64_t)(t0 + r) * H * 2;
-                v[r].x = __ldg(reinterpret_cast<const uint32_t*>(row));
-                v[r].y = __ldg(reinterpret_cast<const uint32_t*>(row + H));
+            if (t0 + r < n) {
+                const uint8_t* row = rows_ptr(rows);
+                if (row == nullptr) {
+                    bad_row = true;                     // a bad block id: the row reads as zeros
+                } else if (active) {
+                    v[r].x = __ldg(reinterpret_cast<const uint32_t*>(row + 4 * tid));
+                    v[r].y = __ldg(reinterpret_cast<const uint32_t*>(row + H + 4 * tid));
+                }
+                rows_next(rows, t0 + r + 1 < n);
             }
         }
 #pragma unroll
@@ -439,6 +515,7 @@ __global__ void __launch_bounds__(kMaxThreads) cg_cdf_kernel(const __grid_consta
             for (int j = 0; j < kStreams; ++j) hist[q[j] * H + chan(tid, j, H)] += 1;
         }
     }
+    if (bad_row && tid == 0) set_status(p.status, LMKV_ERR_BAD_BLOCK);
     if (!active) return;
     // C[k] = round(cum[k] * (2^16 - (Lp - 1)) / n) + k, ties to even; the
     // blob keeps C[1..nsym-1] per channel.
@@ -492,7 +569,7 @@ cg_code_kernel(const __grid_constant__ CgParams p) {
     const int tid = threadIdx.x;
     const bool active = tid < H / kStreams;
     uint8_t* blob = p.blob_ptrs[gi];
-    if (p.chunk_ptrs[gi] == nullptr || blob == nullptr) return;   // reported by the CDF kernel
+    if (!has_rows(p, gi) || blob == nullptr) return;   // reported by the CDF kernel
     uint16_t* table = reinterpret_cast<uint16_t*>(smem);
     if (active) load_table(table, blob, p, s, n, nsym, tid);
     __syncthreads();
@@ -571,7 +648,7 @@ __global__ void __launch_bounds__(kMaxThreads) cg_compact_kernel(const __grid_co
     const int nb = batches_of(n), nregions = nb * 2 * L;
     if (b >= nb) return;
     uint8_t* blob = p.blob_ptrs[gi];
-    if (p.chunk_ptrs[gi] == nullptr || blob == nullptr) return;
+    if (!has_rows(p, gi) || blob == nullptr) return;
     const int tid = threadIdx.x;
     const bool active = tid < H / kStreams;
     uint64_t before, all;
@@ -630,7 +707,7 @@ __global__ void __launch_bounds__(256) cg_total_kernel(const __grid_constant__ C
     const int region = blockIdx.x;
     if (region / (2 * L) >= batches_of(n)) return;
     const uint8_t* blob = p.blob_ptrs[gi];
-    if (blob == nullptr || p.chunk_ptrs[gi] == nullptr) {
+    if (blob == nullptr || !has_rows(p, gi)) {
         if (region == 0 && threadIdx.x == 0) set_status(p.status, LMKV_ERR_BAD_POINTER);
         return;
     }
@@ -668,7 +745,7 @@ template <int kSteps>
 __device__ __forceinline__ void decode_rows(const uint8_t* blob, uint32_t size, uint32_t start,
                                             const uint32_t (&o)[kStreams], const uint16_t* table, int tid,
                                             int H, int nsym, const float* deq, const float* max1s, int nt,
-                                            uint8_t* out) {
+                                            Rows& rows, bool& bad_row) {
     Dec d[kStreams];
     const uint16_t* tab[kStreams];
 #pragma unroll
@@ -682,9 +759,14 @@ __device__ __forceinline__ void decode_rows(const uint8_t* blob, uint32_t size, 
 #pragma unroll
         for (int j = 0; j < kStreams; ++j)
             y[j] = __fmul_rn(deq[dec_symbol<kSteps>(d[j], tab[j], H, nsym, blob, size)], m);
-        uint8_t* row = out + (uint64_t)t * H * 2;
-        *reinterpret_cast<__nv_bfloat162*>(row) = __floats2bfloat162_rn(y[0], y[1]);
-        *reinterpret_cast<__nv_bfloat162*>(row + H) = __floats2bfloat162_rn(y[2], y[3]);
+        uint8_t* row = const_cast<uint8_t*>(rows_ptr(rows));
+        if (row != nullptr) {
+            *reinterpret_cast<__nv_bfloat162*>(row + 4 * tid) = __floats2bfloat162_rn(y[0], y[1]);
+            *reinterpret_cast<__nv_bfloat162*>(row + H + 4 * tid) = __floats2bfloat162_rn(y[2], y[3]);
+        } else {
+            bad_row = true;                        // a bad block id: the row is not written
+        }
+        rows_next(rows, t + 1 < nt);
     }
 }
 
@@ -703,8 +785,7 @@ cg_decode_kernel(const __grid_constant__ CgParams p) {
     const int nb = batches_of(n), nregions = nb * 2 * L;
     if (b >= nb) return;
     const uint8_t* blob = p.blob_ptrs[gi];
-    uint8_t* chunk = const_cast<uint8_t*>(p.chunk_ptrs[gi]);
-    if (blob == nullptr || chunk == nullptr) return;   // reported by the totals kernel
+    if (blob == nullptr || !has_rows(p, gi)) return;   // reported by the totals kernel
     const int tid = threadIdx.x;
     const bool active = tid < H / kStreams;
     const int bins = p.bins[s], MAX = bins / 2 - 1, nsym = 2 * MAX + 1;
@@ -742,11 +823,14 @@ cg_decode_kernel(const __grid_constant__ CgParams p) {
         return;
     }
     const uint32_t start = (uint32_t)(bytes0 + before);
-    uint8_t* out = chunk + ((uint64_t)s * n + t0) * H * 2 + 4 * tid;
+    Rows rows;
+    rows_init(rows, p, gi, s, n, t0);
+    bool bad_row = false;
     if (nsym > 16)
-        decode_rows<5>(blob, (uint32_t)size, start, o, table, tid, H, nsym, deq, max1s, nt, out);
+        decode_rows<5>(blob, (uint32_t)size, start, o, table, tid, H, nsym, deq, max1s, nt, rows, bad_row);
     else
-        decode_rows<4>(blob, (uint32_t)size, start, o, table, tid, H, nsym, deq, max1s, nt, out);
+        decode_rows<4>(blob, (uint32_t)size, start, o, table, tid, H, nsym, deq, max1s, nt, rows, bad_row);
+    if (bad_row && tid == 0) set_status(p.status, LMKV_ERR_BAD_BLOCK);
 }
 
 // ---- host side ----
@@ -810,17 +894,25 @@ int set_smem(const void* fn, size_t bytes) {
 
 enum class Dir { kEncode, kDecode };
 
+// The pool form of a call: rows come from / go to the pages of the listed chunks.
+struct PoolForm {
+    const lmkv_pool_t* pool;
+    const int32_t* block_table;
+    int32_t max_blocks;
+    const std::vector<LmkvChunkRef>* chunks;
+};
+
 int run(Dir dir, void* const* chunk_ptrs, void* const* blob_ptrs, uint64_t* sizes, const int32_t* ntok,
         int32_t num_chunks, int32_t L, int32_t H, const int32_t* bins, void* workspace,
-        uint64_t workspace_bytes, int32_t* d_status, void* stream) {
+        uint64_t workspace_bytes, int32_t* d_status, void* stream, const PoolForm* pf = nullptr) {
     CgParams p{};
     int max_nsym = 0;
     int rc = check_shape(L, H, bins, p.cdf_prefix, &p.cdf_entries, &max_nsym);
     if (rc != LMKV_OK) return rc;
     if (num_chunks < 0) return LMKV_ERR_INVALID_ARG;
     if (num_chunks == 0) return LMKV_OK;
-    if (chunk_ptrs == nullptr || blob_ptrs == nullptr || sizes == nullptr || ntok == nullptr ||
-        workspace == nullptr)
+    if ((chunk_ptrs == nullptr && pf == nullptr) || blob_ptrs == nullptr || sizes == nullptr ||
+        ntok == nullptr || workspace == nullptr)
         return LMKV_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return LMKV_ERR_MISALIGNED;
     uint64_t need = 0;
@@ -837,6 +929,13 @@ int run(Dir dir, void* const* chunk_ptrs, void* const* blob_ptrs, uint64_t* size
     p.H = H;
     p.status = d_status;
     p.ws = static_cast<uint8_t*>(workspace);
+    if (pf != nullptr) {
+        p.layer_base = reinterpret_cast<const uint8_t* const*>(pf->pool->layer_base);
+        p.block_table = pf->block_table;
+        p.num_blocks = pf->pool->num_blocks;
+        p.bt_stride = pf->max_blocks;
+        p.block_size = pf->pool->block_size;
+    }
     const int threads = threads_for(H);
     const bool wide = threads > 256;
     const size_t table_bytes = (size_t)max_nsym * H * 2;
@@ -862,11 +961,15 @@ int run(Dir dir, void* const* chunk_ptrs, void* const* blob_ptrs, uint64_t* size
             p.tot_off[i] = w.tot;
             p.sym_off[i] = w.sym;
             p.slot_off[i] = w.slot;
+            if (pf != nullptr) {
+                p.chunk_req[i] = (*pf->chunks)[g0 + i].req;
+                p.chunk_tok0[i] = (*pf->chunks)[g0 + i].tok0;
+            }
             at = w.end;
             nb_max = batches_of(n) > nb_max ? batches_of(n) : nb_max;
         }
         p.nchunks = cnt;
-        p.chunk_ptrs = reinterpret_cast<const uint8_t* const*>(chunk_ptrs) + g0;
+        p.chunk_ptrs = chunk_ptrs ? reinterpret_cast<const uint8_t* const*>(chunk_ptrs) + g0 : nullptr;
         p.blob_ptrs = reinterpret_cast<uint8_t* const*>(blob_ptrs) + g0;
         p.sizes = sizes + g0;
         const dim3 slices(2 * L, cnt), regions(nb_max * 2 * L, cnt);
@@ -943,6 +1046,44 @@ int lmkv_cachegen_decode(void* const* blob_ptrs, const uint64_t* sizes, const in
                          uint64_t workspace_bytes, int32_t* d_status, void* stream) {
     return run(Dir::kDecode, chunk_ptrs, blob_ptrs, const_cast<uint64_t*>(sizes), num_tokens, num_chunks,
                num_layers, channels, bins, workspace, workspace_bytes, d_status, stream);
+}
+
+// The pool forms: the chunks of a store / retrieve call, enumerated and
+// validated as lmkv_gather_chunks does.
+static int pool_entry(Dir dir, const lmkv_pool_t* pool, const int32_t* block_table, int32_t max_blocks,
+                      const int64_t* start, const int64_t* end, int32_t num_req, int32_t chunk_size,
+                      int32_t save_unfull_chunk, const int32_t* bins, void* const* blob_ptrs,
+                      uint64_t* sizes, void* workspace, uint64_t workspace_bytes, int32_t* d_status,
+                      void* stream) {
+    std::vector<LmkvChunkRef> chunks;
+    const int rc = lmkv_internal_list_chunks(pool, block_table, max_blocks, start, end, num_req, chunk_size,
+                                             save_unfull_chunk, &chunks);
+    if (rc != LMKV_OK) return rc;
+    if (pool->elem_bytes != 2) return LMKV_ERR_UNSUPPORTED;
+    std::vector<int32_t> ntok(chunks.size());
+    for (size_t g = 0; g < chunks.size(); ++g) ntok[g] = chunks[g].n;
+    const PoolForm pf{pool, block_table, max_blocks, &chunks};
+    return run(dir, nullptr, blob_ptrs, sizes, ntok.data(), (int32_t)chunks.size(), pool->num_layers,
+               pool->num_kv_heads * pool->head_dim, bins, workspace, workspace_bytes, d_status, stream, &pf);
+}
+
+int lmkv_cachegen_store_chunks(const lmkv_pool_t* pool, const int32_t* block_table, int32_t max_blocks,
+                               const int64_t* start, const int64_t* end, int32_t num_req, int32_t chunk_size,
+                               int32_t save_unfull_chunk, const int32_t* bins, void* const* blob_ptrs,
+                               uint64_t* sizes, void* workspace, uint64_t workspace_bytes, int32_t* d_status,
+                               void* stream) {
+    return pool_entry(Dir::kEncode, pool, block_table, max_blocks, start, end, num_req, chunk_size,
+                      save_unfull_chunk, bins, blob_ptrs, sizes, workspace, workspace_bytes, d_status, stream);
+}
+
+int lmkv_cachegen_retrieve_chunks(const lmkv_pool_t* pool, const int32_t* block_table, int32_t max_blocks,
+                                  const int64_t* start, const int64_t* end, int32_t num_req,
+                                  int32_t chunk_size, int32_t save_unfull_chunk, const int32_t* bins,
+                                  void* const* blob_ptrs, const uint64_t* sizes, void* workspace,
+                                  uint64_t workspace_bytes, int32_t* d_status, void* stream) {
+    return pool_entry(Dir::kDecode, pool, block_table, max_blocks, start, end, num_req, chunk_size,
+                      save_unfull_chunk, bins, blob_ptrs, const_cast<uint64_t*>(sizes), workspace,
+                      workspace_bytes, d_status, stream);
 }
 
 }  // extern "C"

@@ -44,6 +44,7 @@ ENTRY_POINTS = (
     "lmkv_offload_init", "lmkv_offload_plan", "lmkv_offload_copied", "lmkv_offload_allocate",
     "lmkv_offload_add_free", "lmkv_cachegen_default_bins", "lmkv_cachegen_layout",
     "lmkv_cachegen_workspace_bytes", "lmkv_cachegen_encode", "lmkv_cachegen_decode",
+    "lmkv_cachegen_store_chunks", "lmkv_cachegen_retrieve_chunks",
 )
 
 
@@ -128,9 +129,13 @@ def load() -> ctypes.CDLL:
         lib.lmkv_cachegen_workspace_bytes.argtypes = [i32, i32, P, i32, P]
         lib.lmkv_cachegen_encode.argtypes = [P, P, i32, i32, i32, P, P, P, P, ctypes.c_uint64, P, P]
         lib.lmkv_cachegen_decode.argtypes = [P, P, P, i32, i32, i32, P, P, P, ctypes.c_uint64, P, P]
+        cg_pool = [pool_p, P, i32, P, P, i32, i32, i32, P, P, P, P, ctypes.c_uint64, P, P]
+        lib.lmkv_cachegen_store_chunks.argtypes = cg_pool
+        lib.lmkv_cachegen_retrieve_chunks.argtypes = cg_pool
         for name in ("lmkv_count_chunks", "lmkv_enumerate_chunks", "lmkv_gather_chunks",
                      "lmkv_cachegen_default_bins", "lmkv_cachegen_layout",
                      "lmkv_cachegen_workspace_bytes", "lmkv_cachegen_encode", "lmkv_cachegen_decode",
+                     "lmkv_cachegen_store_chunks", "lmkv_cachegen_retrieve_chunks",
                      "lmkv_decode_store_ranges", "lmkv_offload_init", "lmkv_offload_plan",
                      "lmkv_offload_copied", "lmkv_offload_allocate", "lmkv_offload_add_free",
                      "lmkv_scatter_chunks", "lmkv_gather_layer", "lmkv_scatter_layer",
@@ -476,6 +481,28 @@ def cachegen_decode(blob_ptrs, sizes, num_tokens, num_layers, channels, bins, ch
                                        _stream_handle(stream))
 
 
+def cachegen_store_chunks(pool, block_table, start, end, chunk_size, save_unfull, bins, blob_ptrs,
+                          sizes, workspace, status=None, stream=None) -> int:
+    """Encode a store call's chunks straight from the pool's pages."""
+    a, _keep = _common(pool, block_table, start, end)
+    b = _i32_array(bins)
+    return load().lmkv_cachegen_store_chunks(*a, chunk_size, int(save_unfull), b.ctypes.data,
+                                             _ptr(blob_ptrs), _ptr(sizes), _ptr(workspace),
+                                             workspace.numel() * workspace.element_size(), _ptr(status),
+                                             _stream_handle(stream))
+
+
+def cachegen_retrieve_chunks(pool, block_table, start, end, chunk_size, save_unfull, bins, blob_ptrs,
+                             sizes, workspace, status=None, stream=None) -> int:
+    """Decode blobs straight into the pages of a retrieve call's chunks."""
+    a, _keep = _common(pool, block_table, start, end)
+    b = _i32_array(bins)
+    return load().lmkv_cachegen_retrieve_chunks(*a, chunk_size, int(save_unfull), b.ctypes.data,
+                                                _ptr(blob_ptrs), _ptr(sizes), _ptr(workspace),
+                                                workspace.numel() * workspace.element_size(),
+                                                _ptr(status), _stream_handle(stream))
+
+
 class CachegenCodec:
     """Chunk buffers [2][L][n][H] bf16 <-> CacheGen blobs, through
     lmkv_cachegen_encode / lmkv_cachegen_decode.  Holds the bins and a device
@@ -522,6 +549,32 @@ class CachegenCodec:
             stream.wait_stream(cur)
             for a in arrays:
                 a.record_stream(stream)
+
+    def store(self, pool, block_table, start, end, chunk_size, save_unfull, blobs=None, sizes=None,
+              status=None, stream=None):
+        """Encode a store call's chunks straight from the pool; returns (blobs, sizes)."""
+        ntok = [n for _, _, n in enumerate_chunks(start, end, chunk_size, save_unfull)]
+        if blobs is None:
+            blobs = [torch.empty(self.layout(n).max_bytes, dtype=torch.uint8, device=self.device)
+                     for n in ntok]
+        if sizes is None:
+            sizes = torch.zeros(len(ntok), dtype=torch.int64, device=self.device)
+        ws = self._workspace(ntok)
+        bptr = pointer_array(blobs, self.device)
+        self._order(stream, bptr)
+        check(cachegen_store_chunks(pool, block_table, start, end, chunk_size, save_unfull, self.bins,
+                                    bptr, sizes, ws, status, stream), "lmkv_cachegen_store_chunks")
+        return blobs, sizes
+
+    def retrieve(self, pool, block_table, start, end, chunk_size, save_unfull, blobs, sizes,
+                 status=None, stream=None):
+        """Decode blobs straight into the pool's pages of a retrieve call's chunks."""
+        ntok = [n for _, _, n in enumerate_chunks(start, end, chunk_size, save_unfull)]
+        ws = self._workspace(ntok)
+        bptr = pointer_array(blobs, self.device)
+        self._order(stream, bptr)
+        check(cachegen_retrieve_chunks(pool, block_table, start, end, chunk_size, save_unfull, self.bins,
+                                       bptr, sizes, ws, status, stream), "lmkv_cachegen_retrieve_chunks")
 
     def decode(self, blobs, sizes, chunks, status=None, stream=None):
         """Decode into the chunk tensors (their token counts give n)."""

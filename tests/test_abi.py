@@ -193,3 +193,17 @@ def test_cachegen_host_validation(lib):
         assert go(b=[16, 16, 16, 3]) == lmkv.ERR_INVALID_ARG
         assert go(ntok=()) == lmkv.OK                                      # nothing to do
     assert lmkv.launch_count() == before
+
+
+def test_cachegen_pool_forms_host_validation(lib):
+    """The fused store / retrieve validate like the gather and need bf16."""
+    bins = lmkv.cachegen_default_bins(2)
+    ws = FakeWorkspace(1 << 30)
+    bt = FakeTensor(shape=(1, 64))
+    for fn in (lmkv.cachegen_store_chunks, lmkv.cachegen_retrieve_chunks):
+        args = (FakeTensor(0x30000), FakeTensor(0x40000), ws, None, 0)
+        assert fn(fake_pool(), bt, [17], [300], 256, True, bins, *args) == lmkv.ERR_INVALID_ARG
+        assert fn(fake_pool(), bt, [0], [4096], 256, True, bins, *args) == lmkv.ERR_INVALID_ARG
+        assert fn(fake_pool(elem=4), bt, [0], [512], 256, True, bins, *args) == lmkv.ERR_UNSUPPORTED
+        assert fn(fake_pool(), bt, [0], [512], 256, True, [16, 16, 16, 2], *args) == lmkv.ERR_INVALID_ARG
+        assert fn(fake_pool(), bt, [0], [100], 256, False, bins, *args) == lmkv.OK   # no chunk

@@ -141,3 +141,122 @@ def test_inconsistent_blob_is_rejected():
     dec, st = gpu_decode(codec, [bytes(blob)], [n])
     assert st == pkg.lmkv.ERR_BAD_DATA
     assert np.all(dec[0] == np.uint16(0x40E0))           # 7.0 in bf16, untouched
+
+
+# ---- the pool forms: store = gather then encode, retrieve = decode then scatter ----
+
+import oracle  # noqa: E402
+from gpu_util import device_pool, host_bytes  # noqa: E402
+
+
+def _oracle_gather(w, layers_dev, table, chunks):
+    hp = oracle.HostPool([host_bytes(t) for t in layers_dev], w.block_size)
+    out = [np.zeros((2, w.num_layers, n, w.row_bytes), np.uint8) for _, _, n in chunks]
+    rc = oracle.gather(hp, table, w.starts, w.ends, w.chunk_size, w.save_unfull, out)
+    return [o.view(np.uint16) for o in out], rc
+
+
+@pytest.mark.parametrize("w", [
+    wl.Workload("cg-small", 3, 2, 64, 16, 96, (300, 700), chunk_size=256),
+    wl.Workload("cg-ragged", 2, 1, 32, 32, 80, (100, 64, 900), req_start=(0, 0, 256), chunk_size=128),
+    wl.Workload("cg-no-tail", 2, 2, 64, 16, 64, (700,), chunk_size=256, save_unfull=False),
+], ids=lambda w: w.name)
+def test_pool_store_and_retrieve_exact(w):
+    """lmkv_cachegen_store_chunks gives the oracle's blobs of the oracle's
+    gather; lmkv_cachegen_retrieve_chunks writes the oracle's decode of those
+    blobs into exactly the chunks' rows (the other rows keep the sentinel)."""
+    pool = device_pool(w, seed=3)
+    table = wl.block_table(w, 5)
+    bt = torch.from_numpy(table).to(DEV)
+    chunks = pkg.enumerate_chunks(w.starts, w.ends, w.chunk_size, w.save_unfull)
+    bins = cg.default_bins(w.num_layers)
+    bins[1, 0] = 8
+    codec = pkg.CachegenCodec(w.num_layers, w.row_elems, bins, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    blobs, sizes = codec.store(pool, bt, w.starts, w.ends, w.chunk_size, w.save_unfull, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    xs, rc = _oracle_gather(w, pool.layers, table, chunks)
+    assert rc == 0
+    expect = [cg.encode_chunk(x, bins) for x in xs]
+    got = [b[:s].cpu().numpy().tobytes() for b, s in zip(blobs, sizes.cpu().tolist())]
+    assert got == expect
+
+    # retrieve into a sentinel pool under another table
+    pool2 = device_pool(w, seed=None, fill="sentinel")
+    table2 = wl.block_table(w, 6)
+    bt2 = torch.from_numpy(table2).to(DEV)
+    codec.retrieve(pool2, bt2, w.starts, w.ends, w.chunk_size, w.save_unfull, blobs, sizes, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    hp = oracle.HostPool([host_bytes(t) for t in wl.make_pool(w, "cpu", None, fill="sentinel")],
+                         w.block_size)
+    dec = [cg.decode_chunk(e, w.num_layers, n, w.row_elems, bins).view(np.uint8).reshape(2, w.num_layers, n, -1)
+           for e, (_, _, n) in zip(expect, chunks)]
+    assert oracle.scatter(hp, table2, w.starts, w.ends, w.chunk_size, w.save_unfull, dec) == 0
+    for l in range(w.num_layers):
+        assert np.array_equal(host_bytes(pool2.layers[l]), hp.layers[l]), f"layer {l}"
+
+
+def test_pool_forms_equal_the_two_step_path_at_the_8b_shape():
+    """The 8B batch (40 chunks): the fused store equals gather + encode and
+    the fused retrieve equals decode + scatter, byte for byte; one chunk is
+    also checked against the oracle."""
+    w = wl.LLAMA8B.with_(num_blocks=1024)
+    pool = device_pool(w, seed=0)
+    table = wl.block_table(w, 1)
+    bt = torch.from_numpy(table).to(DEV)
+    chunks = pkg.enumerate_chunks(w.starts, w.ends, w.chunk_size, w.save_unfull)
+    codec = pkg.CachegenCodec(w.num_layers, w.row_elems, device=DEV)
+    blobs, sizes = codec.store(pool, bt, w.starts, w.ends, w.chunk_size, w.save_unfull)
+    bufs = [torch.empty((2, w.num_layers, n, w.row_elems), dtype=torch.bfloat16, device=DEV) for _, _, n in chunks]
+    pkg.check(pkg.gather_chunks(pool, bt, w.starts, w.ends, w.chunk_size, w.save_unfull,
+                                pkg.pointer_array(bufs, DEV), None, None))
+    blobs2, sizes2 = codec.encode(bufs)
+    torch.cuda.synchronize()
+    assert torch.equal(sizes, sizes2)
+    for a, b, s in zip(blobs, blobs2, sizes.cpu().tolist()):
+        assert torch.equal(a[:s], b[:s])
+    g = 17
+    assert blobs[g][:sizes[g]].cpu().numpy().tobytes() == cg.encode_chunk(bufs[g].cpu(), codec.bins)
+
+    pool2 = device_pool(w, seed=None, fill="sentinel")
+    pool3 = device_pool(w, seed=None, fill="sentinel")
+    table2 = wl.block_table(w, 2)
+    bt2 = torch.from_numpy(table2).to(DEV)
+    codec.retrieve(pool2, bt2, w.starts, w.ends, w.chunk_size, w.save_unfull, blobs, sizes)
+    outs = [torch.empty_like(b) for b in bufs]
+    codec.decode(blobs, sizes, outs)
+    pkg.check(pkg.scatter_chunks(pool3, bt2, w.starts, w.ends, w.chunk_size, w.save_unfull,
+                                 pkg.pointer_array(outs, DEV), None, None))
+    torch.cuda.synchronize()
+    for a, b in zip(pool2.layers, pool3.layers):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_pool_store_bad_block_reads_zeros():
+    """A block id outside the pool: its rows are coded as zeros (the oracle's
+    gather leaves them zero too) and the call reports BAD_BLOCK; the retrieve
+    leaves those rows unwritten."""
+    w = wl.Workload("cg-bad", 2, 2, 64, 16, 64, (512,), chunk_size=256)
+    pool = device_pool(w, seed=4)
+    table = wl.block_table(w, 7)
+    table[0, 3] = 1000
+    bt = torch.from_numpy(table).to(DEV)
+    chunks = pkg.enumerate_chunks(w.starts, w.ends, w.chunk_size, w.save_unfull)
+    bins = cg.default_bins(w.num_layers)
+    codec = pkg.CachegenCodec(w.num_layers, w.row_elems, bins, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    blobs, sizes = codec.store(pool, bt, w.starts, w.ends, w.chunk_size, w.save_unfull, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == pkg.lmkv.ERR_BAD_BLOCK
+    xs, rc = _oracle_gather(w, pool.layers, table, chunks)
+    assert rc == oracle.BAD_BLOCK
+    got = [b[:s].cpu().numpy().tobytes() for b, s in zip(blobs, sizes.cpu().tolist())]
+    assert got == [cg.encode_chunk(x, bins) for x in xs]
+    pool2 = device_pool(w, seed=None, fill="sentinel")
+    status.zero_()
+    codec.retrieve(pool2, bt, w.starts, w.ends, w.chunk_size, w.save_unfull, blobs, sizes, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == pkg.lmkv.ERR_BAD_BLOCK
+    assert int((pool2.layers[0].view(torch.uint8) != wl.SENTINEL_BYTE).any(dim=-1).sum()) == 2 * (512 - 16)
