@@ -65,7 +65,7 @@ def parse_args():
                     help="skip the layer-wise pipeline measurement (host round trip per layer)")
     ap.add_argument("--codec-chunks", type=int, default=40,
                     help="--case codec: number of 256-token chunks")
-    ap.add_argument("--case", choices=["llama8b", "profile-small", "codec"], default="llama8b",
+    ap.add_argument("--case", choices=["llama8b", "profile-small", "codec", "llama70b"], default="llama8b",
                     help="profile-small: the 8B shape with a 1024-block pool and a 4096-token "
                          "request (16 chunks), for ncu captures only")
     return ap.parse_args()
@@ -821,9 +821,15 @@ def bench_reference(args):
 
 
 def config_dict(w, c):
-    return {"workload": "llama3.1-8b KV batch: 32 layers x 8 KV heads x head_dim 128 bf16, "
-                        "16-token pages (8192-block pool/layer), one 10240-token request "
-                        "= 40 chunks of 256",
+    if w.name == "llama3.1-70b":
+        what = ("llama3.1-70b KV batch: 80 layers x 8 KV heads x head_dim 128 bf16, 16-token "
+                "pages (4608-block pool/layer), requests of 4096 / 9000 / 20000 / 32768 tokens "
+                f"= {len(c.chunks)} chunks (partial last chunks kept), interleaved block tables")
+    else:
+        what = (f"{w.name} KV batch: {w.num_layers} layers x {w.num_kv_heads} KV heads x head_dim "
+                f"{w.head_dim} bf16, {w.block_size}-token pages ({w.num_blocks}-block pool/layer), "
+                f"{int(w.ends.sum())} tokens = {len(c.chunks)} chunks of {w.chunk_size}")
+    return {"workload": what,
             "steps_include": list(PHASES),
             "per_layer_calls": w.num_layers,
             "bytes_per_step": int(sum(c.phase_bytes.values())),
@@ -850,6 +856,13 @@ def main():
     w = wl.LLAMA8B
     if args.case == "profile-small":
         w = w.with_(num_blocks=1024, req_tokens=(4096,))
+    if args.case == "llama70b":
+        # the 70B batch (4096 / 9000 / 20000 / 32768 tokens, partial last chunks,
+        # interleaved tables); the pool holds 4608 blocks per layer (the batch
+        # needs 4117), so that both pools and the chunk buffers fit beside
+        # each other; device phases only
+        w = wl.LLAMA70B.with_(num_blocks=4608)
+        args.no_pipeline = args.no_cachegen = args.no_cpu_baseline = True
     c = setup(dev, w)
     stream = torch.cuda.Stream(dev)
     per_phase, launches, clk, wall = bench_device(c, args, stream, rank, world, local)
@@ -868,7 +881,7 @@ def main():
                         "frac_of_peak": round(gbs / peak, 4)}
     breakdown["gather_layer"]["us_per_call"] = round(phase_ms["gather_layer"] * 1e3 / w.num_layers, 2)
     breakdown["scatter_layer"]["us_per_call"] = round(phase_ms["scatter_layer"] * 1e3 / w.num_layers, 2)
-    e2e = bench_e2e(c, args, stream)
+    e2e = bench_e2e(c, args, stream) if args.case != "llama70b" else None
     pipeline = bench_layer_pipeline(c) if not args.no_pipeline else None
     decode = bench_decode_store(c) if not args.no_pipeline else None
     cachegen = bench_cachegen(c, clk.get("sm_mhz") if clk else None) if not args.no_cachegen else None
@@ -887,7 +900,7 @@ def main():
             "roofline": {"bound": "hbm", "kernel": "lmkv gather_chunks (move_lsu_kernel<gather>)",
                          "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} hbm_gbs",
-                         "traffic": profiled_traffic(),
+                         "traffic": profiled_traffic() if args.case == "llama8b" else None,
                          "algorithmic_bytes_per_launch": int(c.phase_bytes["gather"])},
             "breakdown": breakdown,
             "e2e": e2e,
