@@ -29,6 +29,9 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
+#include <set>
+#include <utility>
 #include <vector>
 
 namespace {
@@ -884,12 +887,24 @@ int threads_for(int H) { return ((H / kStreams + 31) / 32) * 32; }
 
 // Allow `bytes` of dynamic shared memory and ask for the largest shared
 // memory carve-out, so that as many CTAs fit per SM as their tables allow.
+// Done once per (device, kernel) with the largest size any codec call can
+// need, so that later calls (and calls inside a stream capture) make no
+// attribute call at all.
 int set_smem(const void* fn, size_t bytes) {
-    if (bytes > 48 * 1024 &&
-        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
+    static std::mutex mu;
+    static std::set<std::pair<int, const void*>> done;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return LMKV_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done.count({dev, fn})) return LMKV_OK;
+    const size_t most = (size_t)32 * LMKV_CACHEGEN_MAX_CHANNELS * 2;    // 32 table rows of 2-byte entries
+    (void)bytes;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most) != cudaSuccess ||
+        cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess)
         return LMKV_ERR_CUDA;
-    return cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                cudaSharedmemCarveoutMaxShared) == cudaSuccess ? LMKV_OK : LMKV_ERR_CUDA;
+    done.insert({dev, fn});
+    return LMKV_OK;
 }
 
 enum class Dir { kEncode, kDecode };

@@ -505,8 +505,11 @@ def cachegen_retrieve_chunks(pool, block_table, start, end, chunk_size, save_unf
 
 class CachegenCodec:
     """Chunk buffers [2][L][n][H] bf16 <-> CacheGen blobs, through
-    lmkv_cachegen_encode / lmkv_cachegen_decode.  Holds the bins and a device
-    workspace that grows to the largest batch seen (PyTorch memory)."""
+    lmkv_cachegen_encode / lmkv_cachegen_decode, and pool pages <-> blobs
+    through the fused store / retrieve.  Holds the bins and a device workspace
+    that grows to the largest batch seen (PyTorch memory); calls that share
+    one codec object must be ordered on one stream (they share the
+    workspace)."""
 
     def __init__(self, num_layers: int, channels: int, bins=None, device="cuda"):
         self.num_layers, self.channels = num_layers, channels

@@ -260,3 +260,33 @@ def test_pool_store_bad_block_reads_zeros():
     torch.cuda.synchronize()
     assert status.item() == pkg.lmkv.ERR_BAD_BLOCK
     assert int((pool2.layers[0].view(torch.uint8) != wl.SENTINEL_BYTE).any(dim=-1).sum()) == 2 * (512 - 16)
+
+
+def test_codec_calls_capture_in_a_cuda_graph():
+    """After a first call on the device, encode and decode can be captured in
+    a CUDA graph; a replay reproduces the eager results."""
+    L, H, ntoks = 4, 256, [256, 100]
+    lib = pkg.lmkv
+    codec = pkg.CachegenCodec(L, H, device=DEV)
+    x = wl.cachegen_chunks(L, H, ntoks, seed=31, device=DEV)
+    blobs, sizes = codec.encode(x)
+    outs = [torch.empty_like(t) for t in x]
+    codec.decode(blobs, sizes, outs)
+    torch.cuda.synchronize()
+    blobs2 = [torch.zeros_like(b) for b in blobs]
+    sizes2 = torch.zeros_like(sizes)
+    outs2 = [torch.zeros_like(t) for t in x]
+    cptr, bptr, optr = (pkg.pointer_array(v, DEV) for v in (x, blobs2, outs2))
+    ws = codec._workspace(ntoks)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        pkg.check(lib.cachegen_encode(cptr, ntoks, L, H, codec.bins, bptr, sizes2, ws, None, None))
+        pkg.check(lib.cachegen_decode(bptr, sizes2, ntoks, L, H, codec.bins, optr, ws, None, None))
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(sizes, sizes2)
+    for a, b, s in zip(blobs, blobs2, sizes.cpu().tolist()):
+        assert torch.equal(a[:s], b[:s])
+    for a, b in zip(outs, outs2):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
