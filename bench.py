@@ -783,6 +783,35 @@ def cpu_baseline(c: Ctx, budget_s: float = 20.0):
             "kind": "oracle", "sample": smp.describe(t_all)}
 
 
+def cpu_baseline_all_cores(c: Ctx, rounds: int = 3):
+    """The same oracle on every host core at once: one thread per core, each
+    running every phase of the step on its own 256-token chunk (its own host
+    copy of the batch's first chunk).  The oracle is plain C called through
+    ctypes, which releases the interpreter lock, so the threads run in
+    parallel; the oracle itself is unchanged."""
+    n = len(os.sched_getaffinity(0))
+    smps = [OracleSample(c, c.w.chunk_size) for _ in range(n)]
+    per = sum(smps[0].bytes.values())
+
+    def work(s):
+        for name in PHASES:
+            s.run(name)
+
+    vals = []
+    for _ in range(rounds):
+        threads = [threading.Thread(target=work, args=(s,)) for s in smps]
+        t0 = time.perf_counter()
+        for t in threads:
+            t.start()
+        for t in threads:
+            t.join()
+        vals.append(n * per / (time.perf_counter() - t0) / 1e9)
+    return {"value": round(statistics.median(vals), 3), "unit": UNIT, "cores": n, "kind": "oracle",
+            "sample": f"{n} threads, each every phase of the step on one 256-token chunk of the batch "
+                      f"(all {c.w.num_layers} layers), {rounds} rounds, median; the phase mix is the "
+                      f"step's, so the rate stands for the full step"}
+
+
 def bench_reference(args):
     rank, world, local = dist_env()
     if rank != 0:
@@ -865,7 +894,17 @@ def main():
         args.no_pipeline = args.no_cachegen = args.no_cpu_baseline = True
     c = setup(dev, w)
     stream = torch.cuda.Stream(dev)
-    per_phase, launches, clk, wall = bench_device(c, args, stream, rank, world, local)
+    try:
+        per_phase, launches, clk, wall = bench_device(c, args, stream, rank, world, local)
+    except pkg.LmkvError as exc:
+        # report what the device says (a sticky fault shows up here) before failing
+        try:
+            torch.cuda.synchronize(dev)
+            dev_state = "device synchronises cleanly"
+        except RuntimeError as sync_exc:
+            dev_state = f"device synchronise raised: {sync_exc}"
+        print(f"bench: {exc}; {dev_state}", file=sys.stderr, flush=True)
+        raise
     phase_ms = {n: statistics.mean(v) for n, v in per_phase.items()}
     step_ms = sum(phase_ms.values())
     total_ms = max_over_ranks(step_ms * args.steps, world)
@@ -885,9 +924,10 @@ def main():
     pipeline = bench_layer_pipeline(c) if not args.no_pipeline else None
     decode = bench_decode_store(c) if not args.no_pipeline else None
     cachegen = bench_cachegen(c, clk.get("sm_mhz") if clk else None) if not args.no_cachegen else None
-    cpu = None
+    cpu = cpu_all = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(c)
+        cpu_all = cpu_baseline_all_cores(c)
     if rank == 0:
         out = {
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -908,6 +948,7 @@ def main():
             "decode_store": decode,
             "cachegen": cachegen,
             "cpu_baseline": cpu,
+            "cpu_baseline_all_cores": cpu_all,
             "gpu_launches": int(launches),
             "clocks": clk,
             "wall_s_timed_region": round(wall, 3),

@@ -486,6 +486,13 @@ int lmkv_abi_version(void);
  * points, all streams); a host-side counter for accounting, not a sync. */
 int64_t lmkv_launch_count(void);
 
+/* The cudaError_t (as int) of the most recent CUDA runtime call that made an
+ * entry point return LMKV_ERR_CUDA, 0 if none; a launch can report an error
+ * left by an earlier asynchronous fault.  lmkv_cuda_error_name gives its name
+ * (static storage). */
+int lmkv_last_cuda_error(void);
+const char* lmkv_cuda_error_name(int err);
+
 #ifdef __cplusplus
 }
 #endif

@@ -16,6 +16,14 @@
 namespace {
 
 std::atomic<int64_t> g_launches{0};
+std::atomic<int> g_last_cuda_error{0};
+
+// Keep the code of a failed CUDA runtime call for lmkv_last_cuda_error().
+inline int cuda_status(cudaError_t err) {
+    if (err == cudaSuccess) return LMKV_OK;
+    g_last_cuda_error.store((int)err, std::memory_order_relaxed);
+    return LMKV_ERR_CUDA;
+}
 
 // Copy engine configuration (chosen by measurement on GB300: a sweep of the
 // LSU and TMA bulk engines over threads, unroll, grid shape and stages found
@@ -187,7 +195,7 @@ int launch_pdl(Kernel kernel, int64_t grid, int threads, cudaStream_t stream, Ar
     cfg.numAttrs = 1;
     const cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, args...);
     g_launches.fetch_add(1, std::memory_order_relaxed);
-    return err == cudaSuccess ? LMKV_OK : LMKV_ERR_CUDA;
+    return cuda_status(err);
 }
 
 template <class Kernel, class... Args>
@@ -207,7 +215,7 @@ int launch_pdl_smem(Kernel kernel, int64_t grid, int threads, int64_t smem, cuda
     cfg.numAttrs = 1;
     const cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, args...);
     g_launches.fetch_add(1, std::memory_order_relaxed);
-    return err == cudaSuccess ? LMKV_OK : LMKV_ERR_CUDA;
+    return cuda_status(err);
 }
 
 // Number of CTAs the LSU engine launches for `items` items (one per item).
@@ -276,13 +284,13 @@ int layers_entry(bool gather, const lmkv_pool_t* pool, const int32_t* block_tabl
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     for (int32_t i = 0; i < layer_n; ++i) {
         if (ready != nullptr && ready[i] != nullptr &&
-            cudaStreamWaitEvent(s, reinterpret_cast<cudaEvent_t>(ready[i]), 0) != cudaSuccess)
+            cuda_status(cudaStreamWaitEvent(s, reinterpret_cast<cudaEvent_t>(ready[i]), 0)) != LMKV_OK)
             return LMKV_ERR_CUDA;
         rc = move_entry(gather, pool, block_table, max_blocks, start, end, num_req, chunk_size,
                         save_unfull, chunk_ptrs, layer_lo + i, d_status, stream);
         if (rc != LMKV_OK) return rc;
         if (done != nullptr && done[i] != nullptr &&
-            cudaEventRecord(reinterpret_cast<cudaEvent_t>(done[i]), s) != cudaSuccess)
+            cuda_status(cudaEventRecord(reinterpret_cast<cudaEvent_t>(done[i]), s)) != LMKV_OK)
             return LMKV_ERR_CUDA;
     }
     return LMKV_OK;
@@ -347,7 +355,7 @@ int staged_entry(bool store, const lmkv_pool_t* pool, const int32_t* block_table
         }
         const int64_t chunk_bytes = 2 * L * n * rb;
         for (int64_t k = 0; k < count; ++k) {
-            if (copy_2d(host + k * chunk_bytes, stage + k * 2 * n * rb, n) != cudaSuccess)
+            if (cuda_status(copy_2d(host + k * chunk_bytes, stage + k * 2 * n * rb, n)) != LMKV_OK)
                 return LMKV_ERR_CUDA;
         }
         return LMKV_OK;
@@ -388,7 +396,7 @@ int staged_entry(bool store, const lmkv_pool_t* pool, const int32_t* block_table
     for (int32_t i = 0; i < layer_n; ++i) {
         const int32_t l = layer_lo + i;
         if (ready != nullptr && ready[i] != nullptr &&
-            cudaStreamWaitEvent(s, reinterpret_cast<cudaEvent_t>(ready[i]), 0) != cudaSuccess)
+            cuda_status(cudaStreamWaitEvent(s, reinterpret_cast<cudaEvent_t>(ready[i]), 0)) != LMKV_OK)
             return LMKV_ERR_CUDA;
         if (store) {
             rc = move_entry(true, pool, block_table, max_blocks, start, end, num_req, chunk_size,
@@ -402,7 +410,7 @@ int staged_entry(bool store, const lmkv_pool_t* pool, const int32_t* block_table
         }
         if (rc != LMKV_OK) return rc;
         if (done != nullptr && done[i] != nullptr &&
-            cudaEventRecord(reinterpret_cast<cudaEvent_t>(done[i]), s) != cudaSuccess)
+            cuda_status(cudaEventRecord(reinterpret_cast<cudaEvent_t>(done[i]), s)) != LMKV_OK)
             return LMKV_ERR_CUDA;
     }
     return LMKV_OK;
@@ -423,13 +431,13 @@ bool ensure_smem(Kernel kernel, int64_t bytes, std::atomic<int>* cache) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
     if (cache[dev].load(std::memory_order_relaxed) >= bytes) return true;
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
-        cudaSuccess) {
+    if (cuda_status(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes)) !=
+        LMKV_OK) {
         (void)cudaGetLastError();
         return false;
     }
     if (kQuantCluster > 8 &&
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+        cuda_status(cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != LMKV_OK) {
         (void)cudaGetLastError();
         return false;
     }
@@ -527,6 +535,8 @@ void* noalloc_staging_address() {
 }  // namespace
 
 void lmkv_internal_add_launches(int64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+int lmkv_internal_cuda_status(cudaError_t err) { return cuda_status(err); }
 
 int lmkv_internal_list_chunks(const lmkv_pool_t* pool, const int32_t* block_table, int32_t max_blocks,
                               const int64_t* start, const int64_t* end, int32_t num_req,
@@ -805,5 +815,9 @@ int lmkv_store_layers_staged_noalloc(const lmkv_pool_t* pool, const int32_t* blo
 int lmkv_abi_version(void) { return LMKV_ABI_VERSION; }
 
 int64_t lmkv_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int lmkv_last_cuda_error(void) { return g_last_cuda_error.load(std::memory_order_relaxed); }
+
+const char* lmkv_cuda_error_name(int err) { return cudaGetErrorName((cudaError_t)err); }
 
 }  // extern "C"

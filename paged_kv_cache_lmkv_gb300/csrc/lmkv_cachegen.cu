@@ -894,14 +894,15 @@ int set_smem(const void* fn, size_t bytes) {
     static std::mutex mu;
     static std::set<std::pair<int, const void*>> done;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return LMKV_ERR_CUDA;
+    if (lmkv_internal_cuda_status(cudaGetDevice(&dev)) != LMKV_OK) return LMKV_ERR_CUDA;
     std::lock_guard<std::mutex> lock(mu);
     if (done.count({dev, fn})) return LMKV_OK;
     const size_t most = (size_t)32 * LMKV_CACHEGEN_MAX_CHANNELS * 2;    // 32 table rows of 2-byte entries
     (void)bytes;
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most) != cudaSuccess ||
-        cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+    if (lmkv_internal_cuda_status(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                      (int)most)) != LMKV_OK ||
+        lmkv_internal_cuda_status(cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                                      cudaSharedmemCarveoutMaxShared)) != LMKV_OK)
         return LMKV_ERR_CUDA;
     done.insert({dev, fn});
     return LMKV_OK;
@@ -1000,7 +1001,7 @@ int run(Dir dir, void* const* chunk_ptrs, void* const* blob_ptrs, uint64_t* size
             else cg_decode_kernel<256><<<regions, threads, search_bytes, st>>>(p);
             lmkv_internal_add_launches(2);
         }
-        if (cudaGetLastError() != cudaSuccess) return LMKV_ERR_CUDA;
+        if (lmkv_internal_cuda_status(cudaGetLastError()) != LMKV_OK) return LMKV_ERR_CUDA;
     }
     return LMKV_OK;
 }

@@ -2,6 +2,8 @@
 // (not part of the C ABI).
 #pragma once
 
+#include <cuda_runtime.h>
+
 #include <cstdint>
 #include <vector>
 
@@ -9,6 +11,10 @@
 
 // Adds n to the counter lmkv_launch_count() reports.
 void lmkv_internal_add_launches(int64_t n);
+
+// LMKV_OK for cudaSuccess; otherwise records err for lmkv_last_cuda_error()
+// and returns LMKV_ERR_CUDA.
+int lmkv_internal_cuda_status(cudaError_t err);
 
 // One chunk of a store / retrieve call: request row, first token, tokens.
 struct LmkvChunkRef {

@@ -45,13 +45,18 @@ ENTRY_POINTS = (
     "lmkv_offload_add_free", "lmkv_cachegen_default_bins", "lmkv_cachegen_layout",
     "lmkv_cachegen_workspace_bytes", "lmkv_cachegen_encode", "lmkv_cachegen_decode",
     "lmkv_cachegen_store_chunks", "lmkv_cachegen_retrieve_chunks",
+    "lmkv_last_cuda_error", "lmkv_cuda_error_name",
 )
 
 
 class LmkvError(RuntimeError):
     def __init__(self, code: int, what: str = ""):
         self.code = code
-        super().__init__(f"{what}: lmkv status {code} ({status_string(code)})")
+        msg = f"{what}: lmkv status {code} ({status_string(code)})"
+        if code == ERR_CUDA:
+            err = last_cuda_error()
+            msg += f"; last CUDA error {err} ({cuda_error_name(err)})"
+        super().__init__(msg)
 
 
 class OffloadState(ctypes.Structure):
@@ -148,6 +153,10 @@ def load() -> ctypes.CDLL:
         lib.lmkv_status_string.restype = ctypes.c_char_p
         lib.lmkv_launch_count.argtypes = []
         lib.lmkv_launch_count.restype = ctypes.c_int64
+        lib.lmkv_last_cuda_error.argtypes = []
+        lib.lmkv_last_cuda_error.restype = ctypes.c_int
+        lib.lmkv_cuda_error_name.argtypes = [ctypes.c_int]
+        lib.lmkv_cuda_error_name.restype = ctypes.c_char_p
         _lib = lib
         return lib
 
@@ -158,6 +167,14 @@ def status_string(code: int) -> str:
 
 def launch_count() -> int:
     return int(load().lmkv_launch_count())
+
+
+def last_cuda_error() -> int:
+    return int(load().lmkv_last_cuda_error())
+
+
+def cuda_error_name(err: int) -> str:
+    return load().lmkv_cuda_error_name(int(err)).decode()
 
 
 def _i64_array(values) -> np.ndarray:
