@@ -123,9 +123,20 @@ __device__ __forceinline__ void rows_next(Rows& R, bool more) {
     }
 }
 
-// The chunk's rows are there to be read or written.
-__device__ __forceinline__ bool has_rows(const CgParams& p, int gi) {
-    return p.layer_base != nullptr || p.chunk_ptrs[gi] != nullptr;
+// The chunk's blob and rows are there and 4-byte aligned (the kernels move
+// 32-bit words); otherwise the chunk is skipped and BAD_POINTER reported.
+__device__ __forceinline__ bool aligned4(const void* q) {
+    return q != nullptr && (reinterpret_cast<uintptr_t>(q) & 3) == 0;
+}
+// Every kernel of a call takes the same whole-chunk decision, so a chunk is
+// either processed by all of them or by none (no kernel reads what a skipped
+// one did not write).
+__device__ __forceinline__ bool chunk_ok(const CgParams& p, int gi) {
+    if (!aligned4(p.blob_ptrs[gi])) return false;
+    if (p.layer_base == nullptr) return aligned4(p.chunk_ptrs[gi]);
+    bool ok = true;
+    for (int l = 0; l < p.L; ++l) ok &= aligned4(p.layer_base[l]);
+    return ok;
 }
 
 __host__ __device__ inline int nsym_of(int bins) { return 2 * (bins / 2 - 1) + 1; }
@@ -452,7 +463,7 @@ __global__ void __launch_bounds__(kMaxThreads) cg_cdf_kernel(const __grid_consta
     uint16_t* hist = reinterpret_cast<uint16_t*>(smem);
 
     uint8_t* blob = p.blob_ptrs[gi];
-    if (!has_rows(p, gi) || blob == nullptr) {
+    if (!chunk_ok(p, gi)) {
         if (tid == 0) set_status(p.status, LMKV_ERR_BAD_POINTER);
         return;
     }
@@ -572,7 +583,7 @@ cg_code_kernel(const __grid_constant__ CgParams p) {
     const int tid = threadIdx.x;
     const bool active = tid < H / kStreams;
     uint8_t* blob = p.blob_ptrs[gi];
-    if (!has_rows(p, gi) || blob == nullptr) return;   // reported by the CDF kernel
+    if (!chunk_ok(p, gi)) return;   // reported by the CDF kernel
     uint16_t* table = reinterpret_cast<uint16_t*>(smem);
     if (active) load_table(table, blob, p, s, n, nsym, tid);
     __syncthreads();
@@ -651,7 +662,10 @@ __global__ void __launch_bounds__(kMaxThreads) cg_compact_kernel(const __grid_co
     const int nb = batches_of(n), nregions = nb * 2 * L;
     if (b >= nb) return;
     uint8_t* blob = p.blob_ptrs[gi];
-    if (!has_rows(p, gi) || blob == nullptr) return;
+    if (!chunk_ok(p, gi)) {
+        if (region == 0 && threadIdx.x == 0) p.sizes[gi] = 0;     // nothing was encoded
+        return;
+    }
     const int tid = threadIdx.x;
     const bool active = tid < H / kStreams;
     uint64_t before, all;
@@ -710,8 +724,8 @@ __global__ void __launch_bounds__(256) cg_total_kernel(const __grid_constant__ C
     const int region = blockIdx.x;
     if (region / (2 * L) >= batches_of(n)) return;
     const uint8_t* blob = p.blob_ptrs[gi];
-    if (blob == nullptr || !has_rows(p, gi)) {
-        if (region == 0 && threadIdx.x == 0) set_status(p.status, LMKV_ERR_BAD_POINTER);
+    if (!chunk_ok(p, gi)) {
+        if (threadIdx.x == 0) set_status(p.status, LMKV_ERR_BAD_POINTER);
         return;
     }
     const uint32_t* lengths = reinterpret_cast<const uint32_t*>(blob + lengths_offset(L, n, p.cdf_entries)) +
@@ -788,7 +802,7 @@ cg_decode_kernel(const __grid_constant__ CgParams p) {
     const int nb = batches_of(n), nregions = nb * 2 * L;
     if (b >= nb) return;
     const uint8_t* blob = p.blob_ptrs[gi];
-    if (blob == nullptr || !has_rows(p, gi)) return;   // reported by the totals kernel
+    if (!chunk_ok(p, gi)) return;   // reported by the totals kernel
     const int tid = threadIdx.x;
     const bool active = tid < H / kStreams;
     const int bins = p.bins[s], MAX = bins / 2 - 1, nsym = 2 * MAX + 1;

@@ -290,3 +290,41 @@ def test_codec_calls_capture_in_a_cuda_graph():
         assert torch.equal(a[:s], b[:s])
     for a, b in zip(outs, outs2):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_bad_pointers_skip_the_chunk():
+    """A null or misaligned blob, a misaligned chunk buffer: that chunk is
+    skipped by every kernel (size 0, nothing written) and the call reports
+    BAD_POINTER; the other chunks are coded as usual."""
+    L, H, ntoks = 2, 64, [256, 100, 300]
+    bins = cg.default_bins(L)
+    x = [t.to(DEV) for t in wl.cachegen_chunks(L, H, ntoks, seed=41)]
+    codec = pkg.CachegenCodec(L, H, bins, device=DEV)
+    lib = pkg.lmkv
+    raw = torch.empty(codec.layout(300).max_bytes + 64, dtype=torch.uint8, device=DEV)
+    odd = torch.empty(2 * L * 100 * H + 8, dtype=torch.bfloat16, device=DEV)[1:1 + 2 * L * 100 * H]
+    odd = odd.view(2, L, 100, H)                                  # 2-byte aligned chunk buffer
+    odd.copy_(x[1])
+    blobs = [torch.full((codec.layout(n).max_bytes,), 0x5A, dtype=torch.uint8, device=DEV) for n in ntoks]
+    cases = [
+        ("null blob", [x[0], x[1], x[2]], [blobs[0].data_ptr(), 0, blobs[2].data_ptr()]),
+        ("misaligned blob", [x[0], x[1], x[2]], [blobs[0].data_ptr(), raw.data_ptr() + 2, blobs[2].data_ptr()]),
+        ("misaligned chunk", [x[0], odd, x[2]], [blobs[0].data_ptr(), blobs[1].data_ptr(), blobs[2].data_ptr()]),
+    ]
+    for what, chunks, bptrs in cases:
+        for b in blobs:
+            b.fill_(0x5A)
+        sizes = torch.full((3,), 7, dtype=torch.int64, device=DEV)
+        status = torch.zeros(1, dtype=torch.int32, device=DEV)
+        bptr = torch.tensor(bptrs, dtype=torch.int64, device=DEV)
+        ws = codec._workspace(ntoks)
+        pkg.check(lib.cachegen_encode(pkg.pointer_array(chunks, DEV), ntoks, L, H, bins, bptr, sizes, ws,
+                                      status, None))
+        torch.cuda.synchronize()
+        assert status.item() == lib.ERR_BAD_POINTER, what
+        assert sizes[1].item() == 0, what
+        if what == "misaligned chunk":
+            assert bool((blobs[1] == 0x5A).all()), what
+        for g in (0, 2):
+            s = int(sizes[g].item())
+            assert blobs[g][:s].cpu().numpy().tobytes() == cg.encode_chunk(x[g].cpu(), bins), what
