@@ -35,7 +35,15 @@ constexpr int kLsuUnroll = 8;
 constexpr int kQuantThreads = 256;        // staged quantiser
 constexpr int kQuantRegThreads = 512;     // register-staged fallback (slices beyond shared memory)
 constexpr int kQuantVPT = 8;
-constexpr int kQuantCluster = 8;
+// Cluster sizes of the staged quantiser: 4 CTAs per (chunk, K/V, layer) tile
+// where a CTA's quarter of the tile fits the staging limit (every 8B / 70B /
+// Qwen tile: 64 rows = 8 in registers + 56 in 112 KiB of shared memory), else
+// 8 (longer chunks; also the register-staged fallback).  Measured on the 8B
+// batch (median of 30 event-timed calls): clusters of 4 0.371 ms, of 8
+// 0.398 ms; 4 with 6 register vectors 0.374, with 2 (120 KiB of shared
+// memory, one CTA per SM) 0.584; 512-thread CTAs 0.40-0.50.
+constexpr int kQuantCluster = 4;
+constexpr int kQuantClusterWide = 8;
 constexpr int kQuantHybridVPT = 4;        // register vectors per thread of the staged quantiser
 constexpr int kDequantThreads = 256;
 
@@ -421,7 +429,7 @@ int check_fp8_pool(const lmkv_pool_t* pool, int32_t chunk_size) {
     if (rc != LMKV_OK) return rc;
     if (pool->elem_bytes != 2) return LMKV_ERR_UNSUPPORTED;
     if (((int64_t)pool->num_kv_heads * pool->head_dim) % 16 != 0) return LMKV_ERR_UNSUPPORTED;
-    if (chunk_size > kQuantCluster * lmkv::kQuantMaxRows) return LMKV_ERR_UNSUPPORTED;
+    if (chunk_size > kQuantClusterWide * lmkv::kQuantMaxRows) return LMKV_ERR_UNSUPPORTED;
     return LMKV_OK;
 }
 
@@ -436,7 +444,7 @@ bool ensure_smem(Kernel kernel, int64_t bytes, std::atomic<int>* cache) {
         (void)cudaGetLastError();
         return false;
     }
-    if (kQuantCluster > 8 &&
+    if (kQuantClusterWide > 8 &&
         cuda_status(cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != LMKV_OK) {
         (void)cudaGetLastError();
         return false;
@@ -449,30 +457,39 @@ constexpr int64_t kQuantSmemMax = 200 * 1024;
 
 // Shared-memory bytes of the hybrid quantiser: the slice rows beyond those
 // its registers hold.
-int64_t quant_hybrid_smem_bytes(const Call& c) {
+// Shared memory of one CTA of the staged quantiser with `cluster` CTAs per
+// tile: the rows of its slice beyond those its registers hold.
+int64_t quant_hybrid_smem_bytes(const Call& c, int cluster) {
     const int64_t row = (int64_t)c.pool->num_kv_heads * c.pool->head_dim * c.pool->elem_bytes;
-    const int64_t rows = (c.chunk_size + kQuantCluster - 1) / kQuantCluster;
+    const int64_t rows = (c.chunk_size + cluster - 1) / cluster;
     const int64_t reg_rows = (int64_t)kQuantThreads * kQuantHybridVPT * 16 / row;
     return (rows > reg_rows ? rows - reg_rows : 0) * row;
 }
 
+template <class B, int kCluster>
+int launch_hybrid(const Call& c, float* scales, cudaStream_t stream, int64_t hsmem) {
+    auto hyb = lmkv::quant_gather_hybrid_kernel<B, kQuantThreads, kQuantHybridVPT, kCluster>;
+    static std::atomic<int> hyb_cache[64];
+    const int64_t bytes = hsmem > 16 ? hsmem : 16;
+    if (!ensure_smem(hyb, bytes, hyb_cache)) return LMKV_ERR_CUDA;
+    return for_each_block<B>(c, scales, [&](const B& b) {
+        const int64_t ctas = (int64_t)b.num_chunks * 2 * b.layer_n * kCluster;
+        return launch_pdl_smem(hyb, ctas, kQuantThreads, bytes, stream, b);
+    });
+}
+
 template <class B>
 int launch_quant(const Call& c, float* scales, cudaStream_t stream) {
-    const int64_t hsmem = quant_hybrid_smem_bytes(c);
-    if (hsmem <= kQuantSmemMax) {
-        auto hyb = lmkv::quant_gather_hybrid_kernel<B, kQuantThreads, kQuantHybridVPT, kQuantCluster>;
-        static std::atomic<int> hyb_cache[64];
-        const int64_t bytes = hsmem > 16 ? hsmem : 16;
-        if (!ensure_smem(hyb, bytes, hyb_cache)) return LMKV_ERR_CUDA;
-        return for_each_block<B>(c, scales, [&](const B& b) {
-            const int64_t ctas = (int64_t)b.num_chunks * 2 * b.layer_n * kQuantCluster;
-            return launch_pdl_smem(hyb, ctas, kQuantThreads, bytes, stream, b);
-        });
+    if (c.chunk_size <= kQuantCluster * lmkv::kQuantMaxRows) {
+        const int64_t h = quant_hybrid_smem_bytes(c, kQuantCluster);
+        if (h <= kQuantSmemMax) return launch_hybrid<B, kQuantCluster>(c, scales, stream, h);
     }
+    const int64_t h = quant_hybrid_smem_bytes(c, kQuantClusterWide);
+    if (h <= kQuantSmemMax) return launch_hybrid<B, kQuantClusterWide>(c, scales, stream, h);
     // rows beyond shared memory: register-staged kernel, re-reading what does not fit
     return for_each_block<B>(c, scales, [&](const B& b) {
-        const int64_t ctas = (int64_t)b.num_chunks * 2 * b.layer_n * kQuantCluster;
-        return launch_pdl(lmkv::quant_gather_kernel<B, kQuantRegThreads, kQuantVPT, kQuantCluster>,
+        const int64_t ctas = (int64_t)b.num_chunks * 2 * b.layer_n * kQuantClusterWide;
+        return launch_pdl(lmkv::quant_gather_kernel<B, kQuantRegThreads, kQuantVPT, kQuantClusterWide>,
                           ctas, kQuantRegThreads, stream, b);
     });
 }

@@ -615,9 +615,11 @@ __device__ __forceinline__ uint32_t absmax_smem_slice(const uint8_t* slice, uint
 // together.  The CTA takes the absmax over registers and shared memory, the
 // cluster exchanges CTA maxima through distributed shared memory (one split
 // cluster barrier; lane r reads CTA r's maximum), and every CTA quantises its
-// rows.  Measured on the 8B batch: 4 register vectors per thread (16 KiB of
-// registers + 48 KiB of shared memory per CTA) beat staging everything in
-// shared memory (0.394 vs 0.406 ms) and 8 or 12 register vectors.
+// rows.  Measured on the 8B batch with clusters of 8: 4 register vectors per
+// thread (16 KiB of registers + 48 KiB of shared memory per CTA) beat staging
+// everything in shared memory (0.394 vs 0.406 ms) and 8 or 12 register
+// vectors; clusters of 4 (16 KiB + 112 KiB per CTA, two CTAs per SM) are
+// faster again (0.371 ms): half as many CTAs meet at each cluster barrier.
 template <class B, int kThreads, int kVPT, int kCluster>
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
 quant_gather_hybrid_kernel(const __grid_constant__ B p) {
