@@ -320,8 +320,8 @@ def bench_e2e(c: Ctx, args, stream):
     step does them: the batch's KV is stored to pinned host memory while an
     earlier stored batch of the same shape is retrieved into the second pool
     (independent data, so the two run at once on two streams, one per transfer
-    direction).  Both use the staged layer-wise pipeline (kernel <-> one-layer
-    device staging buffer, copy engine <-> host).  Per step: H2D of the block
+    direction).  Both use the overlapped layer-wise pipeline (kernel <-> two
+    one-layer device staging halves, copy engine <-> host on a copy stream).  Per step: H2D of the block
     tables, the store and the retrieve of every layer, D2H of the status word;
     timed with events, copies included."""
     w = c.w
@@ -332,14 +332,15 @@ def bench_e2e(c: Ctx, args, stream):
     stored = pinned_arena(c.bufs)
     earlier = pinned_arena(c.bufs)
     nst = pkg.staging_bytes(c.pool, *a)
-    stage_s = torch.empty(nst, dtype=torch.uint8, device=c.dev)
-    stage_r = torch.empty(nst, dtype=torch.uint8, device=c.dev)
+    stage_s = torch.empty(2 * nst, dtype=torch.uint8, device=c.dev)     # two layers each
+    stage_r = torch.empty(2 * nst, dtype=torch.uint8, device=c.dev)
     host_status = torch.zeros(1, dtype=torch.int32, pin_memory=True)
-    other = torch.cuda.Stream(c.dev)
+    other, xfer_s, xfer_r = (torch.cuda.Stream(c.dev) for _ in range(3))
+    sync_s, sync_r = pkg.overlap_events(stream), pkg.overlap_events(other)
     fork, join = torch.cuda.Event(), torch.cuda.Event()
     # the earlier batch: store it once (untimed)
-    pkg.check(pkg.store_layers_staged(c.pool, c.bt, *a, earlier, stage_s, 0, L, None, None,
-                                      c.status, stream))
+    pkg.check(pkg.store_layers_overlapped(c.pool, c.bt, *a, earlier, stage_s, 0, L, sync_s, None, None,
+                                          c.status, stream, xfer_s))
     torch.cuda.synchronize(c.dev)
     chunk_bytes = sum(h.numel() * h.element_size() for h in stored)
     h2d = host_bt.numel() * 4 + host_bt2.numel() * 4 + chunk_bytes
@@ -351,10 +352,10 @@ def bench_e2e(c: Ctx, args, stream):
             c.bt2.copy_(host_bt2, non_blocking=True)
             fork.record(stream)
             other.wait_event(fork)
-            pkg.check(pkg.store_layers_staged(c.pool, c.bt, *a, stored, stage_s, 0, L, None, None,
-                                              c.status, stream))
-            pkg.check(pkg.retrieve_layers_staged(c.pool2, c.bt2, *a, earlier, stage_r, 0, L, None,
-                                                 None, c.status, other))
+            pkg.check(pkg.store_layers_overlapped(c.pool, c.bt, *a, stored, stage_s, 0, L, sync_s, None,
+                                                  None, c.status, stream, xfer_s))
+            pkg.check(pkg.retrieve_layers_overlapped(c.pool2, c.bt2, *a, earlier, stage_r, 0, L, sync_r,
+                                                     None, None, c.status, other, xfer_r))
             join.record(other)
             stream.wait_event(join)
             host_status.copy_(c.status, non_blocking=True)
@@ -375,9 +376,10 @@ def bench_e2e(c: Ctx, args, stream):
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "ms_per_step": round(ms, 4),
             "what": "store of the batch to pinned host memory concurrent with the retrieve of an "
-                    "earlier stored batch, both through the staged layer-wise pipeline (kernel + "
-                    "copy engine), H2D block tables and D2H status included; bytes counted as "
-                    "the gather's and the scatter's (read + write)"}
+                    "earlier stored batch, both through the overlapped layer-wise pipeline (kernel "
+                    "<-> two device staging halves, copy engine <-> host on a copy stream), H2D "
+                    "block tables and D2H status included; bytes counted as the gather's and the "
+                    "scatter's (read + write)"}
 
 
 def bench_layer_pipeline(c: Ctx, reps: int = 5):
@@ -399,7 +401,10 @@ def bench_layer_pipeline(c: Ctx, reps: int = 5):
     nst = pkg.staging_bytes(c.pool, *a)
     stage = torch.empty(nst, dtype=torch.uint8, device=c.dev)
     stage2 = torch.empty(nst, dtype=torch.uint8, device=c.dev)
-    compute, copy, copy2 = (torch.cuda.Stream(c.dev) for _ in range(3))
+    stage_x = torch.empty(2 * nst, dtype=torch.uint8, device=c.dev)      # two halves
+    stage_x2 = torch.empty(2 * nst, dtype=torch.uint8, device=c.dev)
+    compute, copy, copy2, xfer, xfer2 = (torch.cuda.Stream(c.dev) for _ in range(5))
+    sync, sync2 = pkg.overlap_events(copy), pkg.overlap_events(copy2)
     ready = [torch.cuda.Event() for _ in range(L)]
     done = [torch.cuda.Event() for _ in range(L)]
     for e in ready + done:
@@ -426,6 +431,10 @@ def bench_layer_pipeline(c: Ctx, reps: int = 5):
             c.pool, c.bt, *a, host, stage, 0, L, r, d, c.status, copy)),
         "staged_retrieve": lambda r=None, d=None: pkg.check(pkg.retrieve_layers_staged(
             c.pool2, c.bt2, *a, host, stage, 0, L, r, d, c.status, copy)),
+        "overlapped_store": lambda r=None, d=None: pkg.check(pkg.store_layers_overlapped(
+            c.pool, c.bt, *a, host, stage_x, 0, L, sync, r, d, c.status, copy, xfer)),
+        "overlapped_retrieve": lambda r=None, d=None: pkg.check(pkg.retrieve_layers_overlapped(
+            c.pool2, c.bt2, *a, host, stage_x, 0, L, sync, r, d, c.status, copy, xfer)),
     }
     t_move = {k: timed(f) for k, f in moves.items()}
     # compute stand-in: square bf16 GEMM whose duration is about one layer's transfer
@@ -471,7 +480,17 @@ def bench_layer_pipeline(c: Ctx, reps: int = 5):
     t_dup = timed(duplex)
     out["staged_store_and_retrieve_concurrent"] = {
         "ms": round(t_dup, 3), "GBps_both_directions": round(2 * payload / (t_dup * 1e-3) / 1e9, 1)}
-    out["retrieve_from_host_Gbps"] = round(8 * payload / (t_move["staged_retrieve"] * 1e-3) / 1e9)
+
+    def duplex_x():
+        pkg.check(pkg.store_layers_overlapped(c.pool, c.bt, *a, host2, stage_x2, 0, L, sync2, None, None,
+                                              c.status, copy2, xfer2))
+        pkg.check(pkg.retrieve_layers_overlapped(c.pool2, c.bt2, *a, host, stage_x, 0, L, sync, None,
+                                                 None, c.status, copy, xfer))
+    t_dupx = timed(duplex_x)
+    out["overlapped_store_and_retrieve_concurrent"] = {
+        "ms": round(t_dupx, 3), "GBps_both_directions": round(2 * payload / (t_dupx * 1e-3) / 1e9, 1)}
+    out["retrieve_from_host_Gbps"] = round(8 * payload / (min(t_move["staged_retrieve"],
+                                                              t_move["overlapped_retrieve"]) * 1e-3) / 1e9)
     out["bytes"] = "payload bytes crossing the GPU-host link per direction (1,342,177,280)"
     return out
 

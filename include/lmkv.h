@@ -271,7 +271,8 @@ int lmkv_retrieve_layers(const lmkv_pool_t* pool, const int32_t* block_table, in
  *                   layer of the batch; chunk g's slices sit at
  *                   2 * row_bytes * (tokens of the chunks before g)
  * Everything is enqueued on `stream`; consecutive layers reuse the staging
- * buffer in stream order.  Errors: as lmkv_store_layers; INVALID_ARG if the
+ * buffer in stream order.  A retrieve waits on layer_ready[i] just before layer
+ * i's scatter (its host-to-staging copies do not touch the pool).  Errors: as lmkv_store_layers; INVALID_ARG if the
  * staging buffer is null or too small or a host pointer is null; MISALIGNED
  * if staging is not 16-byte aligned. */
 int lmkv_store_layers_staged(const lmkv_pool_t* pool, const int32_t* block_table,
@@ -287,6 +288,43 @@ int lmkv_retrieve_layers_staged(const lmkv_pool_t* pool, const int32_t* block_ta
                                 void* const* host_chunks, void* staging, int64_t staging_bytes,
                                 int32_t layer_lo, int32_t layer_n, void* const* layer_ready,
                                 void* const* layer_done, int32_t* d_status, void* stream);
+
+/* The staged pipeline with two staging buffers and the copies on their own
+ * stream, so that layer l's copies overlap layer l+1's gather (store) and
+ * layer l's scatter overlaps layer l+1's copies (retrieve): on one stream the
+ * kernel and the copies of every layer take turns on the link.
+ *   staging      : DEVICE, 16-byte aligned, staging_bytes >= 2 layers of the
+ *                  batch (2 * 2 * row_bytes * tokens); layer i uses half i % 2
+ *   stream       : the kernels (and, for store, the end of the call: it
+ *                  waits for the last copies); copy_stream: the copies, a
+ *                  different caller-owned stream
+ *   sync_events  : HOST array of 4 caller-owned cudaEvent_t (as void*): the
+ *                  library records and waits on them to order the two
+ *                  streams (event b: kernel on half b done; event 2 + b: copies
+ *                  of half b done); the copy stream first waits for the work
+ *                  already on `stream`
+ *   layer_ready  : waited on `stream` before layer i's kernel
+ *   layer_done   : store: recorded on copy_stream after layer i's copies
+ *                  (its rows are on the host); retrieve: recorded on `stream`
+ *                  after layer i's scatter
+ * Other arguments, layouts and errors as lmkv_store_layers_staged; also
+ * INVALID_ARG for a null copy stream, copy_stream == stream, or a null event.
+ * Nothing is allocated; the calls can be captured in a CUDA graph. */
+int lmkv_store_layers_overlapped(const lmkv_pool_t* pool, const int32_t* block_table,
+                                 int32_t max_blocks, const int64_t* start, const int64_t* end,
+                                 int32_t num_req, int32_t chunk_size, int32_t save_unfull_chunk,
+                                 void* const* host_chunks, void* staging, int64_t staging_bytes,
+                                 int32_t layer_lo, int32_t layer_n, void* const* layer_ready,
+                                 void* const* layer_done, void* const* sync_events, int32_t* d_status,
+                                 void* stream, void* copy_stream);
+
+int lmkv_retrieve_layers_overlapped(const lmkv_pool_t* pool, const int32_t* block_table,
+                                    int32_t max_blocks, const int64_t* start, const int64_t* end,
+                                    int32_t num_req, int32_t chunk_size, int32_t save_unfull_chunk,
+                                    void* const* host_chunks, void* staging, int64_t staging_bytes,
+                                    int32_t layer_lo, int32_t layer_n, void* const* layer_ready,
+                                    void* const* layer_done, void* const* sync_events,
+                                    int32_t* d_status, void* stream, void* copy_stream);
 
 /* Size of the built-in staging area of lmkv_store_layers_staged_noalloc. */
 #define LMKV_NOALLOC_STAGING_BYTES (64u << 20)

@@ -308,11 +308,18 @@ int layers_entry(bool gather, const lmkv_pool_t* pool, const int32_t* block_tabl
 // the pool and a one-layer DEVICE staging buffer, and one 2-D copy per chunk
 // (the copy engine, no SMs) moves the chunk's K and V slices of that layer
 // between the staging buffer and the chunk's pinned host buffer.
+// The staged pipeline.  With copy_stream == null: per layer, the kernel and
+// the copies run in order on `stream` through one staging buffer.  With a
+// copy stream and four caller-owned events: two staging buffers, kernels on
+// `stream` and copies on `copy_stream`, so that a layer's copies overlap the
+// next layer's kernel; sync[b] marks "kernel on buffer b done", sync[2 + b]
+// "copies of buffer b done".
 int staged_entry(bool store, const lmkv_pool_t* pool, const int32_t* block_table,
                  int32_t max_blocks, const int64_t* start, const int64_t* end, int32_t num_req,
                  int32_t chunk_size, int32_t save_unfull, void* const* host_chunks, void* staging,
                  int64_t staging_bytes, int32_t layer_lo, int32_t layer_n, void* const* ready,
-                 void* const* done, int32_t* d_status, void* stream) {
+                 void* const* done, int32_t* d_status, void* stream, void* copy_stream = nullptr,
+                 void* const* sync = nullptr) {
     int rc = check_pool(pool);
     if (rc != LMKV_OK) return rc;
     if (layer_lo < 0 || layer_n < 0 || (int64_t)layer_lo + layer_n > pool->num_layers)
@@ -329,9 +336,17 @@ int staged_entry(bool store, const lmkv_pool_t* pool, const int32_t* block_table
         if (nch > 0)
             tokens += save_unfull ? end[r] - start[r] : (end[r] - start[r]) / chunk_size * chunk_size;
     }
-    if (staging == nullptr || staging_bytes < 2 * rb * tokens) return LMKV_ERR_INVALID_ARG;
+    const bool two = copy_stream != nullptr;
+    const int64_t layer_bytes = 2 * rb * tokens;                 // one layer's K and V rows
+    if (staging == nullptr || staging_bytes < (two ? 2 : 1) * layer_bytes) return LMKV_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(staging) & 15) return LMKV_ERR_MISALIGNED;
+    if (two && (sync == nullptr || sync[0] == nullptr || sync[1] == nullptr || sync[2] == nullptr ||
+                sync[3] == nullptr))
+        return LMKV_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaStream_t cs = two ? reinterpret_cast<cudaStream_t>(copy_stream) : s;
+    auto ev = [&](int k) { return reinterpret_cast<cudaEvent_t>(sync[k]); };
+    uint8_t* stage_base = static_cast<uint8_t*>(staging);
     const int64_t L = pool->num_layers;
     // Per chunk, rows {K, V} of layer l: n_g * rb bytes each; host pitch
     // L * n_g * rb, staging pitch n_g * rb.  A run of full chunks whose host
@@ -340,15 +355,16 @@ int staged_entry(bool store, const lmkv_pool_t* pool, const int32_t* block_table
     // only within one allocation, so if it declines, the run falls back to one
     // 2-D copy per chunk and no further 3-D copy is tried in this call.
     bool try_3d = true;
+    uint8_t* staging_now = stage_base;           // the buffer of the layer being moved
     auto copy_2d = [&](uint8_t* host, uint8_t* stage, int64_t n) {
         return store ? cudaMemcpy2DAsync(host, L * n * rb, stage, n * rb, n * rb, 2,
-                                         cudaMemcpyDeviceToHost, s)
+                                         cudaMemcpyDeviceToHost, cs)
                      : cudaMemcpy2DAsync(stage, n * rb, host, L * n * rb, n * rb, 2,
-                                         cudaMemcpyHostToDevice, s);
+                                         cudaMemcpyHostToDevice, cs);
     };
     auto copy_run = [&](int32_t l, int64_t g0, int64_t count, int64_t n, int64_t tok_before) -> int {
         uint8_t* host = static_cast<uint8_t*>(host_chunks[g0]) + (int64_t)l * n * rb;
-        uint8_t* stage = static_cast<uint8_t*>(staging) + 2 * rb * tok_before;
+        uint8_t* stage = staging_now + 2 * rb * tok_before;
         if (count > 1 && try_3d) {
             cudaMemcpy3DParms m = {};
             const cudaPitchedPtr hp = make_cudaPitchedPtr(host, (size_t)(L * n * rb), (size_t)(n * rb), 2);
@@ -357,7 +373,7 @@ int staged_entry(bool store, const lmkv_pool_t* pool, const int32_t* block_table
             m.dstPtr = store ? hp : sp;
             m.extent = make_cudaExtent((size_t)(n * rb), 2, (size_t)count);
             m.kind = store ? cudaMemcpyDeviceToHost : cudaMemcpyHostToDevice;
-            if (cudaMemcpy3DAsync(&m, s) == cudaSuccess) return LMKV_OK;
+            if (cudaMemcpy3DAsync(&m, cs) == cudaSuccess) return LMKV_OK;
             (void)cudaGetLastError();
             try_3d = false;
         }
@@ -401,25 +417,51 @@ int staged_entry(bool store, const lmkv_pool_t* pool, const int32_t* block_table
         if (rc2 == LMKV_OK && run_len > 0) rc2 = copy_run(l, run_g0, run_len, chunk_size, run_tok);
         return rc2;
     };
+    auto wait = [&](cudaStream_t on, cudaEvent_t e) {
+        return cuda_status(cudaStreamWaitEvent(on, e, 0));
+    };
+    auto record = [&](cudaEvent_t e, cudaStream_t on) { return cuda_status(cudaEventRecord(e, on)); };
+    if (two) {
+        // the copy stream starts after everything already ordered on `stream`
+        if (record(ev(0), s) != LMKV_OK || wait(cs, ev(0)) != LMKV_OK) return LMKV_ERR_CUDA;
+    }
     for (int32_t i = 0; i < layer_n; ++i) {
         const int32_t l = layer_lo + i;
-        if (ready != nullptr && ready[i] != nullptr &&
-            cuda_status(cudaStreamWaitEvent(s, reinterpret_cast<cudaEvent_t>(ready[i]), 0)) != LMKV_OK)
-            return LMKV_ERR_CUDA;
+        const int b = two ? (i & 1) : 0;
+        staging_now = stage_base + b * layer_bytes;
+        cudaEvent_t ready_i = (ready != nullptr && ready[i] != nullptr) ? reinterpret_cast<cudaEvent_t>(ready[i])
+                                                                        : nullptr;
+        cudaEvent_t done_i = (done != nullptr && done[i] != nullptr) ? reinterpret_cast<cudaEvent_t>(done[i])
+                                                                     : nullptr;
         if (store) {
+            // buffer b is free once the copies of layer i - 2 are done
+            if (two && i >= 2 && wait(s, ev(2 + b)) != LMKV_OK) return LMKV_ERR_CUDA;
+            if (ready_i && wait(s, ready_i) != LMKV_OK) return LMKV_ERR_CUDA;
             rc = move_entry(true, pool, block_table, max_blocks, start, end, num_req, chunk_size,
-                            save_unfull, host_chunks, l, d_status, stream, staging);
-            if (rc == LMKV_OK) rc = copies(l);
-        } else {
+                            save_unfull, host_chunks, l, d_status, stream, staging_now);
+            if (rc != LMKV_OK) return rc;
+            if (two && (record(ev(b), s) != LMKV_OK || wait(cs, ev(b)) != LMKV_OK)) return LMKV_ERR_CUDA;
             rc = copies(l);
-            if (rc == LMKV_OK)
-                rc = move_entry(false, pool, block_table, max_blocks, start, end, num_req,
-                                chunk_size, save_unfull, host_chunks, l, d_status, stream, staging);
+            if (rc != LMKV_OK) return rc;
+            if (two && record(ev(2 + b), cs) != LMKV_OK) return LMKV_ERR_CUDA;
+            if (done_i && record(done_i, cs) != LMKV_OK) return LMKV_ERR_CUDA;
+        } else {
+            // buffer b is free once the kernel of layer i - 2 has read it
+            if (two && i >= 2 && wait(cs, ev(b)) != LMKV_OK) return LMKV_ERR_CUDA;
+            rc = copies(l);
+            if (rc != LMKV_OK) return rc;
+            if (two && (record(ev(2 + b), cs) != LMKV_OK || wait(s, ev(2 + b)) != LMKV_OK)) return LMKV_ERR_CUDA;
+            if (ready_i && wait(s, ready_i) != LMKV_OK) return LMKV_ERR_CUDA;
+            rc = move_entry(false, pool, block_table, max_blocks, start, end, num_req, chunk_size,
+                            save_unfull, host_chunks, l, d_status, stream, staging_now);
+            if (rc != LMKV_OK) return rc;
+            if (two && record(ev(b), s) != LMKV_OK) return LMKV_ERR_CUDA;
+            if (done_i && record(done_i, s) != LMKV_OK) return LMKV_ERR_CUDA;
         }
-        if (rc != LMKV_OK) return rc;
-        if (done != nullptr && done[i] != nullptr &&
-            cuda_status(cudaEventRecord(reinterpret_cast<cudaEvent_t>(done[i]), s)) != LMKV_OK)
-            return LMKV_ERR_CUDA;
+    }
+    if (two && store) {
+        // the call's work ends on `stream`: join the last copies of both buffers
+        if (wait(s, ev(2)) != LMKV_OK || wait(s, ev(3)) != LMKV_OK) return LMKV_ERR_CUDA;
     }
     return LMKV_OK;
 }
@@ -766,6 +808,31 @@ int lmkv_retrieve_layers_staged(const lmkv_pool_t* pool, const int32_t* block_ta
     return staged_entry(false, pool, block_table, max_blocks, start, end, num_req, chunk_size,
                         save_unfull_chunk, host_chunks, staging, staging_bytes, layer_lo, layer_n,
                         layer_ready, layer_done, d_status, stream);
+}
+
+int lmkv_store_layers_overlapped(const lmkv_pool_t* pool, const int32_t* block_table, int32_t max_blocks,
+                                 const int64_t* start, const int64_t* end, int32_t num_req, int32_t chunk_size,
+                                 int32_t save_unfull_chunk, void* const* host_chunks, void* staging,
+                                 int64_t staging_bytes, int32_t layer_lo, int32_t layer_n,
+                                 void* const* layer_ready, void* const* layer_done, void* const* sync_events,
+                                 int32_t* d_status, void* stream, void* copy_stream) {
+    if (copy_stream == nullptr || copy_stream == stream) return LMKV_ERR_INVALID_ARG;
+    return staged_entry(true, pool, block_table, max_blocks, start, end, num_req, chunk_size,
+                        save_unfull_chunk, host_chunks, staging, staging_bytes, layer_lo, layer_n,
+                        layer_ready, layer_done, d_status, stream, copy_stream, sync_events);
+}
+
+int lmkv_retrieve_layers_overlapped(const lmkv_pool_t* pool, const int32_t* block_table, int32_t max_blocks,
+                                    const int64_t* start, const int64_t* end, int32_t num_req,
+                                    int32_t chunk_size, int32_t save_unfull_chunk, void* const* host_chunks,
+                                    void* staging, int64_t staging_bytes, int32_t layer_lo, int32_t layer_n,
+                                    void* const* layer_ready, void* const* layer_done,
+                                    void* const* sync_events, int32_t* d_status, void* stream,
+                                    void* copy_stream) {
+    if (copy_stream == nullptr || copy_stream == stream) return LMKV_ERR_INVALID_ARG;
+    return staged_entry(false, pool, block_table, max_blocks, start, end, num_req, chunk_size,
+                        save_unfull_chunk, host_chunks, staging, staging_bytes, layer_lo, layer_n,
+                        layer_ready, layer_done, d_status, stream, copy_stream, sync_events);
 }
 
 int lmkv_gather_chunks_fp8e4m3(const lmkv_pool_t* pool, const int32_t* block_table,

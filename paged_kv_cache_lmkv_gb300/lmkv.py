@@ -46,6 +46,7 @@ ENTRY_POINTS = (
     "lmkv_cachegen_workspace_bytes", "lmkv_cachegen_encode", "lmkv_cachegen_decode",
     "lmkv_cachegen_store_chunks", "lmkv_cachegen_retrieve_chunks",
     "lmkv_last_cuda_error", "lmkv_cuda_error_name",
+    "lmkv_store_layers_overlapped", "lmkv_retrieve_layers_overlapped",
 )
 
 
@@ -126,6 +127,9 @@ def load() -> ctypes.CDLL:
         lib.lmkv_retrieve_layers_staged.argtypes = staged
         lib.lmkv_store_layers_staged_noalloc.argtypes = [pool_p, P, i32, P, P, i32, i32, i32, P,
                                                          i32, i32, P, P, P, P]
+        overlapped = [pool_p, P, i32, P, P, i32, i32, i32, P, P, i64, i32, i32, P, P, P, P, P, P]
+        lib.lmkv_store_layers_overlapped.argtypes = overlapped
+        lib.lmkv_retrieve_layers_overlapped.argtypes = overlapped
         fp8 = [pool_p, P, i32, P, P, i32, i32, i32, P, P, P, P]
         lib.lmkv_gather_chunks_fp8e4m3.argtypes = fp8
         lib.lmkv_scatter_chunks_fp8e4m3.argtypes = fp8
@@ -147,7 +151,8 @@ def load() -> ctypes.CDLL:
                      "lmkv_gather_chunks_fp8e4m3", "lmkv_scatter_chunks_fp8e4m3",
                      "lmkv_abi_version", "lmkv_store_layers", "lmkv_retrieve_layers",
                      "lmkv_store_layers_staged", "lmkv_retrieve_layers_staged",
-                     "lmkv_store_layers_staged_noalloc"):
+                     "lmkv_store_layers_staged_noalloc", "lmkv_store_layers_overlapped",
+                     "lmkv_retrieve_layers_overlapped"):
             getattr(lib, name).restype = ctypes.c_int
         lib.lmkv_status_string.argtypes = [ctypes.c_int]
         lib.lmkv_status_string.restype = ctypes.c_char_p
@@ -432,6 +437,47 @@ def retrieve_layers_staged(pool, block_table, start, end, chunk_size, save_unful
                                               staging.numel() * staging.element_size(),
                                               int(layer_lo), int(layer_n), r, d, _ptr(status),
                                               _stream_handle(stream))
+
+
+def overlap_events(stream=None):
+    """Four events for the overlapped pipeline (recorded once on `stream`, so
+    that their CUDA handles exist)."""
+    evs = [torch.cuda.Event() for _ in range(4)]
+    for e in evs:
+        e.record(stream)
+    return evs
+
+
+def _overlapped(fn, pool, block_table, start, end, chunk_size, save_unfull, host_chunks, staging,
+                layer_lo, layer_n, sync_events, layer_ready, layer_done, status, stream, copy_stream):
+    a, _keep = _common(pool, block_table, start, end)
+    h = _host_ptr_array(host_chunks)
+    r, d = _event_array(layer_ready, layer_n), _event_array(layer_done, layer_n)
+    e = _event_array(sync_events, 4)
+    if copy_stream is None:
+        raise ValueError("the overlapped pipeline needs a copy stream")
+    return fn(*a, chunk_size, int(save_unfull), h, _ptr(staging), staging.numel() * staging.element_size(),
+              int(layer_lo), int(layer_n), r, d, e, _ptr(status), _stream_handle(stream),
+              _stream_handle(copy_stream))
+
+
+def store_layers_overlapped(pool, block_table, start, end, chunk_size, save_unfull, host_chunks,
+                            staging, layer_lo, layer_n, sync_events, layer_ready=None,
+                            layer_done=None, status=None, stream=None, copy_stream=None) -> int:
+    """lmkv_store_layers_overlapped: two staging halves (staging holds 2 layers),
+    kernels on `stream`, copies on `copy_stream`, 4 sync events (overlap_events())."""
+    return _overlapped(load().lmkv_store_layers_overlapped, pool, block_table, start, end, chunk_size,
+                       save_unfull, host_chunks, staging, layer_lo, layer_n, sync_events, layer_ready,
+                       layer_done, status, stream, copy_stream)
+
+
+def retrieve_layers_overlapped(pool, block_table, start, end, chunk_size, save_unfull, host_chunks,
+                               staging, layer_lo, layer_n, sync_events, layer_ready=None,
+                               layer_done=None, status=None, stream=None, copy_stream=None) -> int:
+    """lmkv_retrieve_layers_overlapped (the inverse of store_layers_overlapped)."""
+    return _overlapped(load().lmkv_retrieve_layers_overlapped, pool, block_table, start, end, chunk_size,
+                       save_unfull, host_chunks, staging, layer_lo, layer_n, sync_events, layer_ready,
+                       layer_done, status, stream, copy_stream)
 
 
 def store_layers_staged_noalloc(pool, block_table, start, end, chunk_size, save_unfull,

@@ -207,3 +207,28 @@ def test_cachegen_pool_forms_host_validation(lib):
         assert fn(fake_pool(elem=4), bt, [0], [512], 256, True, bins, *args) == lmkv.ERR_UNSUPPORTED
         assert fn(fake_pool(), bt, [0], [512], 256, True, [16, 16, 16, 2], *args) == lmkv.ERR_INVALID_ARG
         assert fn(fake_pool(), bt, [0], [100], 256, False, bins, *args) == lmkv.OK   # no chunk
+
+
+def test_overlapped_pipeline_host_validation(lib):
+    """The two-stream staged pipeline needs two layers of staging, a copy
+    stream other than the kernel stream and four events; all checked before
+    anything is enqueued."""
+    import ctypes as C
+    pool = fake_pool(num_layers=4)
+    need = 2 * 2 * 2 * 64 * 2 * 512      # two layers of 2 * row_bytes * tokens
+    ev = (C.c_void_p * 4)(0x1000, 0x2000, 0x3000, 0x4000)
+    ev_null = (C.c_void_p * 4)(0x1000, 0, 0x3000, 0x4000)
+    for fn in (lib.lmkv_store_layers_overlapped, lib.lmkv_retrieve_layers_overlapped):
+        s, e = (C.c_int64 * 1)(0), (C.c_int64 * 1)(512)
+        h = (C.c_void_p * 2)(0x50000, 0x60000)
+
+        def call(stage=0x70000, nbytes=need, events=ev, stream=0x111, copy=0x222, n=4):
+            return fn(pool.struct, 0x10000, 64, s, e, 1, 256, 1, h, stage, nbytes, 0, n, None, None,
+                      events, None, stream, copy)
+        assert call(nbytes=need // 2) == lmkv.ERR_INVALID_ARG           # one layer of staging only
+        assert call(events=None) == lmkv.ERR_INVALID_ARG
+        assert call(events=ev_null) == lmkv.ERR_INVALID_ARG
+        assert call(copy=None) == lmkv.ERR_INVALID_ARG
+        assert call(copy=0x111) == lmkv.ERR_INVALID_ARG                 # the same stream twice
+        assert call(stage=0x70008) == lmkv.ERR_MISALIGNED
+        assert call(n=0) == lmkv.OK                                     # nothing to do

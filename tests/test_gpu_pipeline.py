@@ -180,3 +180,86 @@ def test_staged_layer_range():
         got = host_bytes(x)
         np.testing.assert_array_equal(got[:, 2:5], r[:, 2:5])
         assert (got[:, :2] == 0x77).all() and (got[:, 5:] == 0x77).all()
+
+
+@pytest.mark.parametrize("arena", [False, True], ids=["separate", "arena"])
+@pytest.mark.parametrize("w", STAGED, ids=["two", "many", "no_tail"])
+def test_overlapped_store_and_retrieve_vs_oracle(w, arena):
+    """The two-stream form (two staging halves, copies on their own stream)
+    stores and retrieves exactly what the oracle's gather / scatter give, with
+    the per-layer ready / done events honoured: the compute stream reads layer
+    l after done[l] of the retrieve."""
+    require_gpu()
+    pool = device_pool(w, 0)
+    t1, t2 = wl.block_table(w, 1), wl.block_table(w, 2)
+    a = (w.starts, w.ends, w.chunk_size, w.save_unfull)
+    chunks = pkg.enumerate_chunks(*a)
+    hbufs, _ = host_chunks(chunks, w, arena)
+    staging = torch.empty(2 * max(pkg.staging_bytes(pool, *a), 16), dtype=torch.uint8, device=DEV)
+    compute, kern, copy = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    sync = pkg.overlap_events(kern)
+    torch.cuda.synchronize()
+    ready = [torch.cuda.Event() for _ in range(w.num_layers)]
+    done = [torch.cuda.Event() for _ in range(w.num_layers)]
+    for e in done:
+        e.record(copy)
+    with torch.cuda.stream(compute):
+        for l in range(w.num_layers):
+            torch.cuda._sleep(100_000)
+            ready[l].record(compute)
+    st = new_status()
+    pkg.check(pkg.store_layers_overlapped(pool, torch.from_numpy(t1).to(DEV), *a, hbufs, staging, 0,
+                                          w.num_layers, sync, ready, None, st, kern, copy))
+    kern.synchronize()                       # the call's work ends on the kernel stream
+    assert st.item() == 0
+    host = [host_bytes(t) for t in pool.layers]
+    ref = [np.zeros((2, w.num_layers, n, w.row_bytes), np.uint8) for _, _, n in chunks]
+    assert oracle.gather(oracle.HostPool(host, w.block_size), t1, *a, ref) == 0
+    for g, (x, r) in enumerate(zip(hbufs, ref)):
+        np.testing.assert_array_equal(host_bytes(x), r, err_msg=f"stored chunk {g}")
+    dst = device_pool(w, None, fill="sentinel")
+    torch.cuda.synchronize()
+    pkg.check(pkg.retrieve_layers_overlapped(dst, torch.from_numpy(t2).to(DEV), *a, hbufs, staging, 0,
+                                             w.num_layers, sync, None, done, st, kern, copy))
+    snaps = []
+    with torch.cuda.stream(compute):
+        for l in range(w.num_layers):
+            compute.wait_event(done[l])
+            snaps.append(dst.layers[l].clone())
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    exp = [np.full((2, w.num_blocks, w.block_size, w.row_bytes), wl.SENTINEL_BYTE, np.uint8)
+           for _ in range(w.num_layers)]
+    assert oracle.scatter(oracle.HostPool(exp, w.block_size), t2, *a, ref) == 0
+    for l in range(w.num_layers):
+        np.testing.assert_array_equal(host_bytes(snaps[l]), exp[l], err_msg=f"layer {l}")
+
+
+def test_overlapped_store_per_layer_done_events():
+    """Store: done[l] fires only once layer l's rows are on the host (the host
+    reads them after synchronising on the event alone)."""
+    require_gpu()
+    w = W
+    pool = device_pool(w, 0)
+    t1 = wl.block_table(w, 1)
+    a = (w.starts, w.ends, w.chunk_size, True)
+    chunks = pkg.enumerate_chunks(*a)
+    hbufs, _ = host_chunks(chunks, w, arena=True)
+    for h in hbufs:
+        h.view(torch.uint8).fill_(0x77)
+    staging = torch.empty(2 * pkg.staging_bytes(pool, *a), dtype=torch.uint8, device=DEV)
+    kern, copy = torch.cuda.Stream(), torch.cuda.Stream()
+    sync = pkg.overlap_events(kern)
+    done = [torch.cuda.Event() for _ in range(w.num_layers)]
+    for e in done:
+        e.record(copy)
+    torch.cuda.synchronize()
+    pkg.check(pkg.store_layers_overlapped(pool, torch.from_numpy(t1).to(DEV), *a, hbufs, staging, 0,
+                                          w.num_layers, sync, None, done, None, kern, copy))
+    ref = [np.zeros((2, w.num_layers, n, w.row_bytes), np.uint8) for _, _, n in chunks]
+    oracle.gather(oracle.HostPool([host_bytes(t) for t in pool.layers], w.block_size), t1, *a, ref)
+    for l in range(w.num_layers):
+        done[l].synchronize()
+        for x, r in zip(hbufs, ref):
+            np.testing.assert_array_equal(host_bytes(x)[:, l], r[:, l], err_msg=f"layer {l}")
+    torch.cuda.synchronize()
