@@ -328,3 +328,51 @@ def test_bad_pointers_skip_the_chunk():
         for g in (0, 2):
             s = int(sizes[g].item())
             assert blobs[g][:s].cpu().numpy().tobytes() == cg.encode_chunk(x[g].cpu(), bins), what
+
+
+def test_seventy_b_layer_count_exact():
+    """80 layers (the 70B shape): default bins K 10 x 32 + 70 x 16, V 2 x 32 +
+    78 x 16; one full chunk and one partial chunk against the oracle."""
+    L = 80
+    bins = cg.default_bins(L)
+    assert bins[0].tolist() == [32] * 10 + [16] * 70 and bins[1].tolist() == [32] * 2 + [16] * 78
+    check_against_oracle(L, 1024, [256, 40], seed=80)
+
+
+def test_pool_forms_with_more_chunks_than_one_launch():
+    """A store / retrieve call of 250 chunks (four launch groups of at most
+    64; full and partial chunks) through the pool equals gather + encode and
+    decode + scatter."""
+    w = wl.Workload("cg-many", 2, 1, 64, 16, 1024, (16, 32, 24) * 50, chunk_size=16)
+    pool = device_pool(w, seed=8)
+    table = wl.block_table(w, 9)
+    bt = torch.from_numpy(table).to(DEV)
+    chunks = pkg.enumerate_chunks(w.starts, w.ends, w.chunk_size, w.save_unfull)
+    assert len(chunks) > 2 * 64
+    codec = pkg.CachegenCodec(w.num_layers, w.row_elems, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    blobs, sizes = codec.store(pool, bt, w.starts, w.ends, w.chunk_size, w.save_unfull, status=status)
+    bufs = [torch.empty((2, w.num_layers, n, w.row_elems), dtype=torch.bfloat16, device=DEV) for _, _, n in chunks]
+    pkg.check(pkg.gather_chunks(pool, bt, w.starts, w.ends, w.chunk_size, w.save_unfull,
+                                pkg.pointer_array(bufs, DEV), status, None))
+    blobs2, sizes2 = codec.encode(bufs)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    assert torch.equal(sizes, sizes2)
+    for a, b, s in zip(blobs, blobs2, sizes.cpu().tolist()):
+        assert torch.equal(a[:s], b[:s])
+    for g in (0, 77, len(chunks) - 1):
+        assert blobs[g][:sizes[g]].cpu().numpy().tobytes() == cg.encode_chunk(bufs[g].cpu(), codec.bins)
+    pool2 = device_pool(w, seed=None, fill="sentinel")
+    pool3 = device_pool(w, seed=None, fill="sentinel")
+    table2 = wl.block_table(w, 10)
+    bt2 = torch.from_numpy(table2).to(DEV)
+    codec.retrieve(pool2, bt2, w.starts, w.ends, w.chunk_size, w.save_unfull, blobs, sizes, status=status)
+    outs = [torch.empty_like(b) for b in bufs]
+    codec.decode(blobs, sizes, outs, status=status)
+    pkg.check(pkg.scatter_chunks(pool3, bt2, w.starts, w.ends, w.chunk_size, w.save_unfull,
+                                 pkg.pointer_array(outs, DEV), status, None))
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    for a, b in zip(pool2.layers, pool3.layers):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
