@@ -644,6 +644,7 @@ def bench_cachegen(c: Ctx, clk_mhz, reps: int = 5):
     out["retrieve_two_step_ms"] = round(main["_td"] + times["scatter"], 3)
     out["store_fused_GBps_raw"] = round(raw / (times["store_fused"] * 1e-3) / 1e9, 1)
     out["retrieve_fused_GBps_raw"] = round(raw / (times["retrieve_fused"] * 1e-3) / 1e9, 1)
+    out["host_offload"] = bench_cachegen_offload(c, codec, stream, reps)
     sweep = {}
     for C in wl.CACHEGEN_CHUNK_SIZES:
         ntoks = [C] * (10240 // C) + ([10240 % C] if 10240 % C else [])
@@ -654,6 +655,71 @@ def bench_cachegen(c: Ctx, clk_mhz, reps: int = 5):
         torch.cuda.empty_cache()
     out["chunk_size_sweep"] = sweep
     return out
+
+
+def bench_cachegen_offload(c: Ctx, codec, stream, reps: int):
+    """Compressed offload of the batch to pinned host memory and back through
+    the public API: store = the fused CacheGen store (pool pages -> blobs), the
+    sizes to the host, then only the coded bytes of every blob device-to-host;
+    retrieve = the coded bytes host-to-device, then the fused retrieve (blobs
+    -> pool pages).  Wall time per call sequence (events on the stream, the
+    host waits once for the sizes).  Effective GB/s counts the raw bf16 bytes
+    moved to / from the host, to compare with the uncompressed staged pipeline
+    (link-bound near 190 / 207 GB/s one way); the codec is lossy (each value
+    within half a quantisation step), so this is the trade the pages describe:
+    fewer link bytes for a bounded error."""
+    w = c.w
+    a = (w.starts, w.ends, w.chunk_size, w.save_unfull)
+    ntok = [n for _, _, n in c.chunks]
+    blobs = [torch.empty(codec.layout(n).max_bytes, dtype=torch.uint8, device=c.dev) for n in ntok]
+    sizes = torch.zeros(len(ntok), dtype=torch.int64, device=c.dev)
+    host_sizes = torch.zeros(len(ntok), dtype=torch.int64, pin_memory=True)
+    lib = pkg.lmkv
+    bptr = pkg.pointer_array(blobs, c.dev)
+    ws = codec._workspace(ntok)
+    torch.cuda.synchronize(c.dev)
+    # one store to size the host blobs
+    pkg.check(lib.cachegen_store_chunks(c.pool, c.bt, *a, codec.bins, bptr, sizes, ws, c.status, stream))
+    torch.cuda.synchronize(c.dev)
+    sz = sizes.cpu().tolist()
+    host = torch.empty(sum(sz), dtype=torch.uint8, pin_memory=True)
+    offs = np.concatenate([[0], np.cumsum(sz)]).tolist()
+
+    def store():
+        with torch.cuda.stream(stream):
+            pkg.check(lib.cachegen_store_chunks(c.pool, c.bt, *a, codec.bins, bptr, sizes, ws, c.status,
+                                                stream))
+            host_sizes.copy_(sizes, non_blocking=True)
+        stream.synchronize()
+        with torch.cuda.stream(stream):
+            for g, n in enumerate(host_sizes.tolist()):
+                host[offs[g]:offs[g] + n].copy_(blobs[g][:n], non_blocking=True)
+
+    def retrieve():
+        with torch.cuda.stream(stream):
+            for g, n in enumerate(sz):
+                blobs[g][:n].copy_(host[offs[g]:offs[g] + n], non_blocking=True)
+            pkg.check(lib.cachegen_retrieve_chunks(c.pool2, c.bt2, *a, codec.bins, bptr, sizes, ws,
+                                                   c.status, stream))
+
+    res = {}
+    for name, fn in (("store", store), ("retrieve", retrieve)):
+        fn()
+        torch.cuda.synchronize(c.dev)
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize(c.dev)
+            ts.append(e0.elapsed_time(e1))
+        res[name] = statistics.median(ts)
+    raw = c.payload
+    return {"link_bytes": int(sum(sz)), "raw_bytes": int(raw),
+            "store_ms": round(res["store"], 3), "retrieve_ms": round(res["retrieve"], 3),
+            "store_effective_GBps_raw": round(raw / (res["store"] * 1e-3) / 1e9, 1),
+            "retrieve_effective_GBps_raw": round(raw / (res["retrieve"] * 1e-3) / 1e9, 1)}
 
 
 def bench_codec_only(args):
