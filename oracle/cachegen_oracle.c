@@ -22,7 +22,12 @@
  *     factor = MAX / max1, y = x * factor, z = y + MAX, q = round(z) to the
  *     nearest integer, ties to even; every step one fp32 operation (the bf16
  *     input widened exactly).  q is clamped to [0, 2*MAX]; a row whose max1
- *     is 0 gets q = MAX.  Inputs are finite.
+ *     is 0 gets q = MAX.  Inputs are finite.  The clamp is applied to z
+ *     before the rounding (the same result for every finite z, the bounds
+ *     being integers).  A nonzero max1 below MAX / FLT_MAX (a row of
+ *     subnormal values) makes factor infinite: y is then +-inf, clamped to
+ *     2*MAX or 0, or NaN for x = 0, taken as 0 (as a maximum with 0 treats
+ *     a NaN operand).
  *  R2 CDF (section 3): nsym = 2*MAX + 1 symbols and Lp = nsym + 1 CDF
  *     entries.  Over the n tokens of the chunk, cum[k] = number of tokens
  *     whose symbol is below k (k = 0..nsym); with M = 2^16 - (Lp - 1),
@@ -133,9 +138,10 @@ void cgo_quantize(const uint16_t* x, int32_t n, int32_t H, int32_t bins, uint8_t
             if (m != 0.0f) {
                 volatile float y = bf16_to_f32(row[c]) * factor;
                 volatile float z = y + (float)MAX;
-                q = (int32_t)nearbyintf(z);   /* default mode: nearest, ties even */
-                if (q < 0) q = 0;
-                if (q > 2 * MAX) q = 2 * MAX;
+                /* clamp, then round (default mode: nearest, ties even);
+                   fmaxf takes 0 for a NaN z */
+                float zc = fminf(fmaxf(z, 0.0f), (float)(2 * MAX));
+                q = (int32_t)nearbyintf(zc);
             }
             sym[(int64_t)t * H + c] = (uint8_t)q;
         }

@@ -160,7 +160,8 @@ CG_MUTANTS = {
                                  "        for (int32_t c = 1; c < H; ++c) {\n            float a"),
     "dequant_without_offset": ("(float)((int32_t)sym[(int64_t)t * H + c] - MAX) / (float)MAX",
                                "(float)((int32_t)sym[(int64_t)t * H + c]) / (float)MAX"),
-    "quant_truncates": ("q = (int32_t)nearbyintf(z);", "q = (int32_t)z;"),
+    "quant_truncates": ("q = (int32_t)nearbyintf(zc);", "q = (int32_t)zc;"),
+    "nan_clamps_high": ("fminf(fmaxf(z, 0.0f), (float)(2 * MAX))", "fmaxf(fminf(z, (float)(2 * MAX)), 0.0f)"),
 }
 
 
