@@ -25,6 +25,7 @@
 #include "lmkv.h"
 #include "lmkv_internal.h"
 
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -35,6 +36,8 @@
 #include <vector>
 
 namespace {
+
+namespace cg = cooperative_groups;
 
 constexpr int kBatch = LMKV_CACHEGEN_BATCH;
 constexpr int kMaxChunks = 64;                 // chunks per launch
@@ -51,6 +54,7 @@ struct CgParams {
     int32_t* status;
     uint8_t* ws;
     int32_t L, H, nchunks, cdf_entries;
+    int32_t split;                      // CTAs per slice (CDF pass) / per region (coder, compaction, decoder)
     int32_t ntok[kMaxChunks];
     uint64_t tot_off[kMaxChunks];       // workspace byte offsets per chunk
     uint64_t sym_off[kMaxChunks];
@@ -177,11 +181,13 @@ __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // q = clamp(round(x * factor + MAX), 0, 2*MAX), one fp32 operation per step.
-__device__ __forceinline__ uint32_t quantise(float x, float factor, float maxf, int two_max) {
-    const float z = __fadd_rn(__fmul_rn(x, factor), maxf);
-    int q = __float2int_rn(z);
-    q = q < 0 ? 0 : (q > two_max ? two_max : q);
-    return (uint32_t)q;
+// The clamp is taken first (the bounds are integers, so it commutes with the
+// rounding; a NaN product, 0 * inf for a row of tiny values, clamps to 0),
+// then adding 1.5 * 2^23 rounds to an integer with ties to even (in
+// [2^23, 2^24) the spacing of floats is 1) and leaves it in the low bits.
+__device__ __forceinline__ uint32_t quantise(float x, float factor, float maxf, float two_maxf) {
+    const float z = fminf(fmaxf(__fadd_rn(__fmul_rn(x, factor), maxf), 0.0f), two_maxf);
+    return __float_as_uint(__fadd_rn(z, 12582912.0f)) - 0x4B400000u;
 }
 
 // Channel j (0..kStreams-1) of thread tid: the pairs (2*tid, 2*tid + 1) in
@@ -449,23 +455,42 @@ __device__ __forceinline__ void stream_offsets(const uint32_t (&l)[kStreams], ui
     off[3] = total0 + o1 + l[2];
 }
 
+// Cluster barrier halves (every thread of every CTA of the cluster takes part).
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // ---- encode 1: absmax, symbols, histogram, CDF ----
-// grid (2L, chunks), block = H / kStreams threads rounded up to a warp.
-// Shared memory: uint16 hist[nsym_max][H].
+// grid (2L * split, chunks) in clusters of `split` CTAs along x, one cluster
+// per (chunk, kv, layer) slice; block = H / kStreams threads rounded up to a
+// warp, thread t holding channels chan(t, 0..3).  CTA `part` of a slice takes
+// a contiguous 1/split of its rows.  The histograms are then merged through
+// distributed shared memory: each CTA sums, over the cluster, the channels of
+// its 1/split of the threads, and those threads write their CDFs.
+// Shared memory: uint16 hist[nsym_max][H] (counts <= n <= 4096).
 __global__ void __launch_bounds__(kMaxThreads) cg_cdf_kernel(const __grid_constant__ CgParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
-    __shared__ uint32_t part[2][kRows][kMaxThreads / 32];
-    const int s = blockIdx.x, gi = blockIdx.y;
+    __shared__ uint32_t part_max[2][kRows][kMaxThreads / 32];
+    const int gi = blockIdx.y, S = p.split;
+    const int s = blockIdx.x / S, part = blockIdx.x % S;    // part = rank in the cluster
     const int n = p.ntok[gi], H = p.H, L = p.L;
     const int bins = p.bins[s], MAX = bins / 2 - 1, nsym = 2 * MAX + 1;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = (blockDim.x + 31) >> 5;
-    const bool active = tid < H / kStreams;
+    const int T = H / kStreams, Tl = T / S;
+    const bool active = tid < T;
     uint16_t* hist = reinterpret_cast<uint16_t*>(smem);
 
     uint8_t* blob = p.blob_ptrs[gi];
-    if (!chunk_ok(p, gi)) {
-        if (tid == 0) set_status(p.status, LMKV_ERR_BAD_POINTER);
+    if (!chunk_ok(p, gi)) {            // the same decision in every CTA of the cluster
+        if (tid == 0 && part == 0) set_status(p.status, LMKV_ERR_BAD_POINTER);
         return;
+    }
+    if (part == 0) {                   // the coder adds each region's total into these
+        uint32_t* totals = reinterpret_cast<uint32_t*>(p.ws + p.tot_off[gi]);
+        for (int b = tid; b < batches_of(n); b += blockDim.x) totals[b * 2 * L + s] = 0;
     }
     if (active)
         for (int k = 0; k < nsym; ++k) {
@@ -473,35 +498,47 @@ __global__ void __launch_bounds__(kMaxThreads) cg_cdf_kernel(const __grid_consta
             *reinterpret_cast<uint32_t*>(hist + k * H + chan(tid, 2, H)) = 0;
         }
 
-    // this thread's two bf16 pairs of a row: channels (2t, 2t+1) and (H/2 + 2t, H/2 + 2t + 1)
+    // this CTA's rows [r0, r1); this thread's two bf16 pairs of a row:
+    // channels (2t, 2t+1) and (H/2 + 2t, H/2 + 2t + 1)
+    const int per = (n + S - 1) / S;
+    const int r0 = part * per < n ? part * per : n, r1 = r0 + per < n ? r0 + per : n;
     Rows rows;
-    rows_init(rows, p, gi, s, n, 0);
+    if (r0 < r1) rows_init(rows, p, gi, s, n, r0);
     bool bad_row = false;
     uint32_t* sym = reinterpret_cast<uint32_t*>(p.ws + p.sym_off[gi] + (uint64_t)s * n * H) + tid;
     float* max1_out = reinterpret_cast<float*>(blob) + (uint64_t)s * n;
-    const float maxf = (float)MAX;
+    const float maxf = (float)MAX, two_maxf = (float)(2 * MAX);
+    uint32_t* hist32 = reinterpret_cast<uint32_t*>(smem);
 
-    for (int t0 = 0, buf = 0; t0 < n; t0 += kRows, buf ^= 1) {
-        uint2 v[kRows];
+    // rows are loaded one group of kRows ahead of their use
+    uint2 nxt[kRows];
+    auto load_group = [&](int t0) {
 #pragma unroll
         for (int r = 0; r < kRows; ++r) {
-            v[r] = make_uint2(0, 0);
-            if (t0 + r < n) {
+            nxt[r] = make_uint2(0, 0);
+            if (t0 + r < r1) {
                 const uint8_t* row = rows_ptr(rows);
                 if (row == nullptr) {
                     bad_row = true;                     // a bad block id: the row reads as zeros
                 } else if (active) {
-                    v[r].x = __ldg(reinterpret_cast<const uint32_t*>(row + 4 * tid));
-                    v[r].y = __ldg(reinterpret_cast<const uint32_t*>(row + H + 4 * tid));
+                    nxt[r].x = __ldg(reinterpret_cast<const uint32_t*>(row + 4 * tid));
+                    nxt[r].y = __ldg(reinterpret_cast<const uint32_t*>(row + H + 4 * tid));
                 }
-                rows_next(rows, t0 + r + 1 < n);
+                rows_next(rows, t0 + r + 1 < r1);
             }
         }
+    };
+    if (r0 < r1) load_group(r0);
+    for (int t0 = r0, buf = 0; t0 < r1; t0 += kRows, buf ^= 1) {
+        uint2 v[kRows];
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) v[r] = nxt[r];
+        if (t0 + kRows < r1) load_group(t0 + kRows);
 #pragma unroll
         for (int r = 0; r < kRows; ++r) {
             const uint32_t a = abs_max_bits(v[r].x), b = abs_max_bits(v[r].y);
             const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, a > b ? a : b);
-            if (lane == 0) part[buf][r][warp] = m;
+            if (lane == 0) part_max[buf][r][warp] = m;
         }
         __syncthreads();
         // lane r of every warp finishes row r: the max over the warps' partial
@@ -510,64 +547,90 @@ __global__ void __launch_bounds__(kMaxThreads) cg_cdf_kernel(const __grid_consta
         // shuffles
         uint32_t mb = 0;
         if (lane < kRows)
-            for (int w = 0; w < nw; ++w) mb = mb > part[buf][lane][w] ? mb : part[buf][lane][w];
+            for (int w = 0; w < nw; ++w) mb = mb > part_max[buf][lane][w] ? mb : part_max[buf][lane][w];
         const float mrow = __uint_as_float(mb);
         const float frow = mb ? __fdiv_rn(maxf, mrow) : 0.0f;
-        if (warp == 0 && lane < kRows && t0 + lane < n) max1_out[t0 + lane] = mrow;
+        if (warp == 0 && lane < kRows && t0 + lane < r1) max1_out[t0 + lane] = mrow;
 #pragma unroll
         for (int r = 0; r < kRows; ++r) {
             const int t = t0 + r;
             const float factor = __shfl_sync(0xFFFFFFFFu, frow, r);
-            if (t >= n || !active) continue;
+            if (t >= r1 || !active) continue;
             uint32_t q[kStreams];
-            q[0] = quantise(bf16_lo(v[r].x), factor, maxf, 2 * MAX);
-            q[1] = quantise(bf16_hi(v[r].x), factor, maxf, 2 * MAX);
-            q[2] = quantise(bf16_lo(v[r].y), factor, maxf, 2 * MAX);
-            q[3] = quantise(bf16_hi(v[r].y), factor, maxf, 2 * MAX);
+            q[0] = quantise(bf16_lo(v[r].x), factor, maxf, two_maxf);
+            q[1] = quantise(bf16_hi(v[r].x), factor, maxf, two_maxf);
+            q[2] = quantise(bf16_lo(v[r].y), factor, maxf, two_maxf);
+            q[3] = quantise(bf16_hi(v[r].y), factor, maxf, two_maxf);
             sym[(uint64_t)t * (H / 4)] = q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24);
-#pragma unroll
-            for (int j = 0; j < kStreams; ++j) hist[q[j] * H + chan(tid, j, H)] += 1;
+            // channels (2t, 2t+1) share a 32-bit word of the uint16 histogram
+            // row, low half first; no carry between the halves (counts <= 4096)
+            atomicAdd(hist32 + q[0] * (H / 2) + tid, 1u);
+            atomicAdd(hist32 + q[1] * (H / 2) + tid, 0x10000u);
+            atomicAdd(hist32 + q[2] * (H / 2) + H / 4 + tid, 1u);
+            atomicAdd(hist32 + q[3] * (H / 2) + H / 4 + tid, 0x10000u);
         }
     }
     if (bad_row && tid == 0) set_status(p.status, LMKV_ERR_BAD_BLOCK);
-    if (!active) return;
+    if (S > 1) {
+        cluster_arrive();              // every CTA's histogram is complete ...
+        cluster_wait();
+        // ... and this CTA sums its threads' channels over the cluster: the
+        // pairs [2 part Tl, 2 (part + 1) Tl) of each half of the row, as
+        // 32-bit words of two counts (no carry between the halves: <= 4096)
+        for (int i = tid; i < nsym * 2 * Tl; i += blockDim.x) {
+            const int k = i / (2 * Tl), r = i % (2 * Tl);
+            const int c = (r < Tl ? 0 : H / 2) + 2 * (part * Tl + r % Tl);
+            uint32_t* w = reinterpret_cast<uint32_t*>(hist + k * H + c);
+            uint32_t sum = *w;
+            for (int q = 1; q < S; ++q) sum += *cg::this_cluster().map_shared_rank(w, (unsigned)((part + q) % S));
+            *w = sum;
+        }
+        cluster_arrive();              // this CTA has read its peers' counts
+        __syncthreads();
+    }
     // C[k] = round(cum[k] * (2^16 - (Lp - 1)) / n) + k, ties to even; the
     // blob keeps C[1..nsym-1] per channel.
-    const uint32_t M = 65536u - (uint32_t)nsym;
-    uint16_t* cdf = reinterpret_cast<uint16_t*>(blob + cdf_offset(L, n)) + p.cdf_prefix[s];
+    if (active && tid / Tl == part) {
+        const uint32_t M = 65536u - (uint32_t)nsym;
+        uint16_t* cdf = reinterpret_cast<uint16_t*>(blob + cdf_offset(L, n)) + p.cdf_prefix[s];
 #pragma unroll
-    for (int j = 0; j < kStreams; ++j) {
-        const int c = chan(tid, j, H);
-        uint16_t* dst = cdf + (uint64_t)c * (nsym - 1);
-        uint32_t cum = 0;
-        for (int k = 0; k < nsym; ++k) {
-            const uint32_t num = cum * M;
-            uint32_t q = num / (uint32_t)n;
-            const uint32_t r = num - q * (uint32_t)n;
-            if (2 * r > (uint32_t)n || (2 * r == (uint32_t)n && (q & 1))) ++q;
-            if (k > 0) dst[k - 1] = (uint16_t)(q + k);
-            cum += hist[k * H + c];
+        for (int j = 0; j < kStreams; ++j) {
+            const int c = chan(tid, j, H);
+            uint16_t* dst = cdf + (uint64_t)c * (nsym - 1);
+            uint32_t cum = 0;
+            for (int k = 0; k < nsym; ++k) {
+                const uint32_t num = cum * M;
+                uint32_t q = num / (uint32_t)n;
+                const uint32_t r = num - q * (uint32_t)n;
+                if (2 * r > (uint32_t)n || (2 * r == (uint32_t)n && (q & 1))) ++q;
+                if (k > 0) dst[k - 1] = (uint16_t)(q + k);
+                cum += hist[k * H + c];
+            }
         }
     }
+    if (S > 1) cluster_wait();         // peers may still be reading this CTA's counts
 }
 
-// Load one slice's CDF table from the blob into shared memory:
-// table[k * H + c] = C[k] for k < nsym (C[0] = 0), this thread's channels.
-__device__ __forceinline__ void load_table(uint16_t* table, const uint8_t* blob, const CgParams& p,
-                                           int s, int n, int nsym, int tid) {
-    const int H = p.H;
+// Load this CTA's part of one slice's CDF table from the blob into shared
+// memory: table[k * Hl + cl] = C[k] for k < nsym (C[0] = 0) and 0xFFFF for
+// nsym <= k < rows, cl the local index of the thread's channel (Hl = H /
+// split channels per CTA).
+__device__ __forceinline__ void load_table_part(uint16_t* table, const uint8_t* blob, const CgParams& p,
+                                                int s, int n, int nsym, int tid, int tl, int Hl, int rows) {
     const uint16_t* src = reinterpret_cast<const uint16_t*>(blob + cdf_offset(p.L, n)) + p.cdf_prefix[s];
 #pragma unroll
     for (int j = 0; j < kStreams; ++j) {
-        const int c = chan(tid, j, H);
+        const int c = chan(tid, j, p.H), cl = chan(tl, j, Hl);
         const uint16_t* sc = src + (uint64_t)c * (nsym - 1);
-        table[c] = 0;
-        for (int k = 1; k < nsym; ++k) table[k * H + c] = sc[k - 1];
+        table[cl] = 0;
+        for (int k = 1; k < rows; ++k) table[k * Hl + cl] = k < nsym ? sc[k - 1] : (uint16_t)0xFFFF;
     }
 }
 
-// ---- encode 2: one CTA per (chunk, batch, kv, layer) region ----
-// grid (nb_max * 2L, chunks).  Shared memory: uint16 table[nsym_max][H].
+// ---- encode 2: the coders of one (chunk, batch, kv, layer) region ----
+// grid (nb_max * 2L * split, chunks): CTA `part` of a region runs the threads
+// [part * Tl, (part + 1) * Tl) of the region (Tl = H / kStreams / split), each
+// with kStreams coders.  Shared memory: uint16 table[nsym][H / split].
 // kThreads = 256 (up to 1024 channels) lets three CTAs share an SM's
 // registers; 512 covers up to 2048 channels.
 template <int kThreads>
@@ -575,17 +638,19 @@ __global__ void __launch_bounds__(kThreads, kThreads == 256 ? 3 : 1)
 cg_code_kernel(const __grid_constant__ CgParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ uint64_t red[32];
-    const int gi = blockIdx.y, n = p.ntok[gi], H = p.H, L = p.L;
-    const int region = blockIdx.x, b = region / (2 * L), s = region % (2 * L);
+    const int gi = blockIdx.y, n = p.ntok[gi], H = p.H, L = p.L, S = p.split;
+    const int region = blockIdx.x / S, part = blockIdx.x % S;
+    const int b = region / (2 * L), s = region % (2 * L);
     if (b >= batches_of(n)) return;
     const int nsym = nsym_of(p.bins[s]);
     const int t0 = b * kBatch, nt = n - t0 < kBatch ? n - t0 : kBatch;
-    const int tid = threadIdx.x;
-    const bool active = tid < H / kStreams;
+    const int Hl = H / S, Tl = Hl / kStreams;
+    const int tl = threadIdx.x, tid = part * Tl + tl;
+    const bool active = tl < Tl;
     uint8_t* blob = p.blob_ptrs[gi];
     if (!chunk_ok(p, gi)) return;   // reported by the CDF kernel
     uint16_t* table = reinterpret_cast<uint16_t*>(smem);
-    if (active) load_table(table, blob, p, s, n, nsym, tid);
+    if (active) load_table_part(table, blob, p, s, n, nsym, tid, tl, Hl, nsym);
     __syncthreads();
 
     const uint64_t stride = slot_stride(n);
@@ -600,7 +665,7 @@ cg_code_kernel(const __grid_constant__ CgParams p) {
         for (int j = 0; j < kStreams; ++j) {
             const int c = chan(tid, j, H);
             slot[j] = reinterpret_cast<uint32_t*>(p.ws + p.slot_off[gi] + ((uint64_t)region * H + c) * stride);
-            tab[j] = table + c;
+            tab[j] = table + chan(tl, j, Hl);
             enc_init(e[j]);
         }
         const uint32_t* sym = reinterpret_cast<const uint32_t*>(p.ws + p.sym_off[gi] +
@@ -613,8 +678,8 @@ cg_code_kernel(const __grid_constant__ CgParams p) {
 #pragma unroll
             for (int j = 0; j < kStreams; ++j) {
                 const uint32_t q = (w >> (8 * j)) & 0xFFu;
-                const uint32_t lo = tab[j][q * H];
-                const uint32_t hi = (int)q + 1 < nsym ? (uint32_t)tab[j][(q + 1) * H] : 65536u;
+                const uint32_t lo = tab[j][q * Hl];
+                const uint32_t hi = (int)q + 1 < nsym ? (uint32_t)tab[j][(q + 1) * Hl] : 65536u;
                 enc_symbol(e[j], lo, hi, slot[j], cap_words, overflow);
             }
         }
@@ -630,8 +695,8 @@ cg_code_kernel(const __grid_constant__ CgParams p) {
     }
     if (overflow) set_status(p.status, LMKV_ERR_SCRATCH_LIMIT);   // excluded by the bound
     const uint64_t total = block_sum((uint64_t)len[0] + len[1] + len[2] + len[3], red);
-    if (tid == 0)
-        reinterpret_cast<uint32_t*>(p.ws + p.tot_off[gi])[region] = (uint32_t)total;
+    if (tl == 0)   // the CDF pass zeroed the region totals
+        atomicAdd(reinterpret_cast<uint32_t*>(p.ws + p.tot_off[gi]) + region, (uint32_t)total);
 }
 
 // Byte offset of region `region` within the chunk's streams, and the total
@@ -648,22 +713,37 @@ __device__ __forceinline__ void region_base(const uint32_t* totals, int region, 
     *all = block_sum(c, red);
 }
 
+// 16-byte asynchronous copy from global to shared memory (both 16-byte aligned).
+__device__ __forceinline__ void cp_async16(void* sdst, const void* gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                 :: "r"((uint32_t)__cvta_generic_to_shared(sdst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+constexpr uint32_t kStage = 32768;     // compaction staging bytes per CTA
+
 // ---- encode 3: place every stream at its prefix-sum offset ----
-// grid (nb_max * 2L, chunks), block as the coder.  Shared memory: uint32
-// off[H], len[H].
+// grid (nb_max * 2L * split, chunks), block as the coder of a whole region
+// (every CTA scans the region's lengths).  CTA `part` moves the streams of
+// channels [part H / split, (part + 1) H / split) in batches that fit the
+// staging buffer: the batch's slots are copied into shared memory with 16-byte
+// asynchronous copies (many in flight: the slots were just written and every
+// read waits on memory), then each stream is written to its byte offset in the
+// blob from there.  Shared memory: uint32 off[H], len[H], kStage + 16 bytes of
+// staging.
 __global__ void __launch_bounds__(kMaxThreads) cg_compact_kernel(const __grid_constant__ CgParams p) {
     __shared__ uint64_t red[32];
     __shared__ uint32_t sred[64];
     extern __shared__ __align__(16) uint8_t smem[];
     uint32_t* off = reinterpret_cast<uint32_t*>(smem);
     uint32_t* lens = off + p.H;
-    const int gi = blockIdx.y, n = p.ntok[gi], H = p.H, L = p.L;
-    const int region = blockIdx.x, b = region / (2 * L);
+    const int gi = blockIdx.y, n = p.ntok[gi], H = p.H, L = p.L, S = p.split;
+    const int region = blockIdx.x / S, part = blockIdx.x % S, b = region / (2 * L);
     const int nb = batches_of(n), nregions = nb * 2 * L;
     if (b >= nb) return;
     uint8_t* blob = p.blob_ptrs[gi];
     if (!chunk_ok(p, gi)) {
-        if (region == 0 && threadIdx.x == 0) p.sizes[gi] = 0;     // nothing was encoded
+        if (blockIdx.x == 0 && threadIdx.x == 0) p.sizes[gi] = 0;     // nothing was encoded
         return;
     }
     const int tid = threadIdx.x;
@@ -672,7 +752,7 @@ __global__ void __launch_bounds__(kMaxThreads) cg_compact_kernel(const __grid_co
     region_base(reinterpret_cast<const uint32_t*>(p.ws + p.tot_off[gi]), region, nregions, red,
                 &before, &all);
     const uint64_t bytes0 = bytes_offset(L, n, H, p.cdf_entries);
-    if (region == 0 && tid == 0) p.sizes[gi] = bytes0 + all;
+    if (blockIdx.x == 0 && tid == 0) p.sizes[gi] = bytes0 + all;
 
     const uint32_t* lengths = reinterpret_cast<const uint32_t*>(blob + lengths_offset(L, n, p.cdf_entries)) +
                               (uint64_t)region * H;
@@ -688,31 +768,61 @@ __global__ void __launch_bounds__(kMaxThreads) cg_compact_kernel(const __grid_co
             lens[chan(tid, j, H)] = l[j];
         }
     __syncthreads();
-    // One warp per stream.  The destination is byte-aligned: the bytes before
-    // its first 4-byte boundary and after its last are copied one by one
-    // (those words are shared with the neighbouring streams), the words in
-    // between whole, each assembled from two aligned words of the slot.
-    const int lane = tid & 31, warp = tid >> 5, nw = (blockDim.x + 31) >> 5;
-    const uint64_t stride = slot_stride(n);
+    const uint32_t stride = (uint32_t)slot_stride(n);
     uint8_t* dst0 = blob + bytes0 + before;
     const uint8_t* src0 = p.ws + p.slot_off[gi] + (uint64_t)region * H * stride;
-    for (int c = warp; c < H; c += nw) {
-        const uint32_t len = lens[c];
-        const uint8_t* src = src0 + (uint64_t)c * stride;          // 16-byte aligned
-        uint8_t* dst = dst0 + off[c];
-        uint32_t head = (uint32_t)(-reinterpret_cast<uintptr_t>(dst)) & 3u;
-        head = head < len ? head : len;
-        const uint32_t words = (len - head) >> 2;
-        const uint32_t body = head + 4 * words, tail = len - body;
-        if ((uint32_t)lane < head) dst[lane] = src[lane];
-        if ((uint32_t)lane < tail) dst[body + lane] = src[body + lane];
-        const uint32_t sh = head;                                 // source misalignment
-        const uint32_t* sw = reinterpret_cast<const uint32_t*>(src);
-        uint32_t* dw = reinterpret_cast<uint32_t*>(dst + head);
-        for (uint32_t i = lane; i < words; i += 32) {
-            const uint32_t lo = sw[i], hi = sw[i + 1];           // i + 1 stays in the slot's slack
-            dw[i] = sh ? __funnelshift_r(lo, hi, 8 * sh) : lo;
+    uint8_t* stage = smem + (size_t)H * 8;          // 16-byte aligned (H % 4 == 0)
+    const uint32_t lane = tid & 31;
+    const int warp = tid >> 5, nw = (blockDim.x + 31) >> 5;
+    const int span = H / S, ce = (part + 1) * span;
+    for (int c = part * span; c < ce;) {
+        // The batch [c, e): stream x goes to stage + pos(x), pos(x) =
+        // roundup16(off[x] - off[c]) + 16 (x - c), which leaves room for its
+        // roundup16(len) copied bytes before pos(x + 1).  So "fits" (pos(x)
+        // + roundup16(len[x]) <= kStage) holds for a prefix of the streams,
+        // always including x = c (a stream is at most 578 bytes).
+        const uint32_t base = off[c];
+        auto pos = [&](int x) { return ((off[x] - base + 15u) & ~15u) + 16u * (uint32_t)(x - c); };
+        int e = c;
+        for (int x0 = c; x0 < ce; x0 += blockDim.x) {
+            const int x = x0 + tid;
+            const bool fits = x < ce && pos(x) + ((lens[x] + 15u) & ~15u) <= kStage;
+            const int k = __syncthreads_count(fits);
+            e += k;
+            if (k < (int)blockDim.x) break;
         }
+        // copy in: 8 lanes per stream, 16 bytes each
+        for (int x = c + (tid >> 3); x < e; x += (int)blockDim.x >> 3) {
+            const uint32_t chunks = (lens[x] + 15u) >> 4, at = pos(x);
+            for (uint32_t j = tid & 7; j < chunks; j += 8)
+                cp_async16(stage + at + 16 * j, src0 + (uint64_t)x * stride + 16 * j);
+        }
+        cp_async_wait_all();
+        __syncthreads();
+        // copy out: a warp per stream.  The destination is byte-aligned: the
+        // bytes before its first 4-byte boundary and after its last are
+        // written one by one (those words are shared with the neighbouring
+        // streams), the words in between whole, each assembled from two
+        // aligned words of the staged copy.
+        for (int x = c + warp; x < e; x += nw) {
+            const uint32_t len = lens[x];
+            const uint8_t* src = stage + pos(x);
+            uint8_t* dst = dst0 + off[x];
+            uint32_t head = (uint32_t)(-reinterpret_cast<uintptr_t>(dst)) & 3u;
+            head = head < len ? head : len;
+            const uint32_t words = (len - head) >> 2;
+            const uint32_t body = head + 4 * words, tail = len - body;
+            if (lane < head) dst[lane] = src[lane];
+            if (lane < tail) dst[body + lane] = src[body + lane];
+            const uint32_t* sw = reinterpret_cast<const uint32_t*>(src);
+            uint32_t* dw = reinterpret_cast<uint32_t*>(dst + head);
+            for (uint32_t i = lane; i < words; i += 32) {
+                const uint32_t lo = sw[i], hi = sw[i + 1];   // at most 4 bytes past the copy: in the buffer
+                dw[i] = head ? __funnelshift_r(lo, hi, 8 * head) : lo;
+            }
+        }
+        __syncthreads();                                  // the buffer is reused
+        c = e;
     }
 }
 
@@ -741,41 +851,27 @@ __global__ void __launch_bounds__(256) cg_total_kernel(const __grid_constant__ C
     }
 }
 
-// The decoder's table: C[k] for k < nsym, then 0xFFFF up to the next power of
-// two rows (see dec_symbol).
-__device__ __forceinline__ void load_search_table(uint16_t* table, const uint8_t* blob,
-                                                  const CgParams& p, int s, int n, int nsym, int tid) {
-    const int H = p.H, rows = nsym > 16 ? 32 : 16;
-    const uint16_t* src = reinterpret_cast<const uint16_t*>(blob + cdf_offset(p.L, n)) + p.cdf_prefix[s];
-#pragma unroll
-    for (int j = 0; j < kStreams; ++j) {
-        const int c = chan(tid, j, H);
-        const uint16_t* sc = src + (uint64_t)c * (nsym - 1);
-        table[c] = 0;
-        for (int k = 1; k < rows; ++k) table[k * H + c] = k < nsym ? sc[k - 1] : (uint16_t)0xFFFF;
-    }
-}
-
 // Decode this thread's kStreams streams over the batch's nt tokens and write
 // the dequantised rows.
+// The table holds this CTA's Hl channels (thread tl's at chan(tl, j, Hl)).
 template <int kSteps>
 __device__ __forceinline__ void decode_rows(const uint8_t* blob, uint32_t size, uint32_t start,
                                             const uint32_t (&o)[kStreams], const uint16_t* table, int tid,
-                                            int H, int nsym, const float* deq, const float* max1s, int nt,
-                                            Rows& rows, bool& bad_row) {
+                                            int tl, int H, int Hl, int nsym, const float* deq,
+                                            const float* max1s, int nt, Rows& rows, bool& bad_row) {
     Dec d[kStreams];
     const uint16_t* tab[kStreams];
 #pragma unroll
     for (int j = 0; j < kStreams; ++j) {
         dec_init(d[j], blob, start + o[j], size);
-        tab[j] = table + chan(tid, j, H);
+        tab[j] = table + chan(tl, j, Hl);
     }
     for (int t = 0; t < nt; ++t) {
         const float m = max1s[t];
         float y[kStreams];
 #pragma unroll
         for (int j = 0; j < kStreams; ++j)
-            y[j] = __fmul_rn(deq[dec_symbol<kSteps>(d[j], tab[j], H, nsym, blob, size)], m);
+            y[j] = __fmul_rn(deq[dec_symbol<kSteps>(d[j], tab[j], Hl, nsym, blob, size)], m);
         uint8_t* row = const_cast<uint8_t*>(rows_ptr(rows));
         if (row != nullptr) {
             *reinterpret_cast<__nv_bfloat162*>(row + 4 * tid) = __floats2bfloat162_rn(y[0], y[1]);
@@ -787,8 +883,24 @@ __device__ __forceinline__ void decode_rows(const uint8_t* blob, uint32_t size, 
     }
 }
 
-// ---- decode 2: one CTA per (chunk, batch, kv, layer) region ----
-// grid (nb_max * 2L, chunks).  Shared memory: uint16 table[nsym_max][H].
+// Sum over the region's lengths (H of them) of those channels c with
+// lo <= c < hi, for each of three ranges; every thread gets the sums.
+__device__ __forceinline__ void range_sums(const uint32_t* lengths, int H, const int (&lo)[3],
+                                           const int (&hi)[3], uint64_t* red, uint64_t (&out)[3]) {
+    uint64_t a[3] = {0, 0, 0};
+    for (int c = threadIdx.x; c < H; c += blockDim.x) {
+        const uint32_t v = lengths[c];
+#pragma unroll
+        for (int i = 0; i < 3; ++i) a[i] += (c >= lo[i] && c < hi[i]) ? v : 0u;
+    }
+#pragma unroll
+    for (int i = 0; i < 3; ++i) out[i] = block_sum(a[i], red);
+}
+
+// ---- decode 2: the decoders of one (chunk, batch, kv, layer) region ----
+// grid (nb_max * 2L * split, chunks): CTA `part` of a region runs the threads
+// [part * Tl, (part + 1) * Tl) (Tl = H / kStreams / split).  Shared memory:
+// uint16 table[16 or 32][H / split].
 template <int kThreads>
 __global__ void __launch_bounds__(kThreads, kThreads == 256 ? 3 : 1)
 cg_decode_kernel(const __grid_constant__ CgParams p) {
@@ -797,14 +909,15 @@ cg_decode_kernel(const __grid_constant__ CgParams p) {
     __shared__ uint32_t sred[64];
     __shared__ float deq[32];
     __shared__ float max1s[kBatch];
-    const int gi = blockIdx.y, n = p.ntok[gi], H = p.H, L = p.L;
-    const int region = blockIdx.x, b = region / (2 * L), s = region % (2 * L);
+    const int gi = blockIdx.y, n = p.ntok[gi], H = p.H, L = p.L, S = p.split;
+    const int region = blockIdx.x / S, part = blockIdx.x % S, b = region / (2 * L), s = region % (2 * L);
     const int nb = batches_of(n), nregions = nb * 2 * L;
     if (b >= nb) return;
     const uint8_t* blob = p.blob_ptrs[gi];
     if (!chunk_ok(p, gi)) return;   // reported by the totals kernel
-    const int tid = threadIdx.x;
-    const bool active = tid < H / kStreams;
+    const int Hl = H / S, Tl = Hl / kStreams;
+    const int tl = threadIdx.x, tid = part * Tl + tl;
+    const bool active = tl < Tl;
     const int bins = p.bins[s], MAX = bins / 2 - 1, nsym = 2 * MAX + 1;
     const int t0 = b * kBatch, nt = n - t0 < kBatch ? n - t0 : kBatch;
 
@@ -814,14 +927,14 @@ cg_decode_kernel(const __grid_constant__ CgParams p) {
     const uint64_t bytes0 = bytes_offset(L, n, H, p.cdf_entries);
     const uint64_t size = p.sizes[gi];
     if (bytes0 + all != size) {          // the lengths do not add up to the blob
-        if (tid == 0) set_status(p.status, LMKV_ERR_BAD_DATA);
+        if (tl == 0 && part == 0) set_status(p.status, LMKV_ERR_BAD_DATA);
         return;
     }
     uint16_t* table = reinterpret_cast<uint16_t*>(smem);
-    if (active) load_search_table(table, blob, p, s, n, nsym, tid);
-    if (tid < nsym) deq[tid] = __fdiv_rn((float)(tid - MAX), (float)MAX);
+    if (active) load_table_part(table, blob, p, s, n, nsym, tid, tl, Hl, nsym > 16 ? 32 : 16);
+    if (tl < nsym) deq[tl] = __fdiv_rn((float)(tl - MAX), (float)MAX);
     const float* max1 = reinterpret_cast<const float*>(blob) + (uint64_t)s * n + t0;
-    for (int t = tid; t < nt; t += blockDim.x) max1s[t] = max1[t];
+    for (int t = tl; t < nt; t += blockDim.x) max1s[t] = max1[t];
 
     const uint32_t* lengths = reinterpret_cast<const uint32_t*>(blob + lengths_offset(L, n, p.cdf_entries)) +
                               (uint64_t)region * H;
@@ -829,7 +942,24 @@ cg_decode_kernel(const __grid_constant__ CgParams p) {
     if (active)
 #pragma unroll
         for (int j = 0; j < kStreams; ++j) l[j] = lengths[chan(tid, j, H)];
-    stream_offsets(l, sred, o);          // also orders the shared-memory writes above
+    // The streams lie in channel order.  Within each half of the row the
+    // thread's pair follows those of the threads before it in this CTA (the
+    // scans) and, with a split, the 2 part Tl channels of the CTAs before it.
+    uint32_t tot0, tot1;
+    const uint32_t s0 = block_scan(l[0] + l[1], sred, &tot0);   // also orders the shared-memory writes above
+    const uint32_t s1 = block_scan(l[2] + l[3], sred + 32, &tot1);
+    uint32_t first = 0, second = tot0;
+    if (S > 1) {
+        const int lo[3] = {0, H / 2, 0}, hi[3] = {2 * part * Tl, H / 2 + 2 * part * Tl, H / 2};
+        uint64_t sums[3];
+        range_sums(lengths, H, lo, hi, red, sums);
+        first = (uint32_t)sums[0];
+        second = (uint32_t)(sums[2] + sums[1]);
+    }
+    o[0] = first + s0;
+    o[1] = o[0] + l[0];
+    o[2] = second + s1;
+    o[3] = o[2] + l[2];
     if (!active) return;
     const uint64_t bound = stream_bound(nt);
     bool bad = false;
@@ -844,10 +974,12 @@ cg_decode_kernel(const __grid_constant__ CgParams p) {
     rows_init(rows, p, gi, s, n, t0);
     bool bad_row = false;
     if (nsym > 16)
-        decode_rows<5>(blob, (uint32_t)size, start, o, table, tid, H, nsym, deq, max1s, nt, rows, bad_row);
+        decode_rows<5>(blob, (uint32_t)size, start, o, table, tid, tl, H, Hl, nsym, deq, max1s, nt, rows,
+                       bad_row);
     else
-        decode_rows<4>(blob, (uint32_t)size, start, o, table, tid, H, nsym, deq, max1s, nt, rows, bad_row);
-    if (bad_row && tid == 0) set_status(p.status, LMKV_ERR_BAD_BLOCK);
+        decode_rows<4>(blob, (uint32_t)size, start, o, table, tid, tl, H, Hl, nsym, deq, max1s, nt, rows,
+                       bad_row);
+    if (bad_row && tl == 0) set_status(p.status, LMKV_ERR_BAD_BLOCK);
 }
 
 // ---- host side ----
@@ -899,12 +1031,38 @@ int workspace_size(int32_t L, int32_t H, const int32_t* ntok, int32_t num_chunks
 
 int threads_for(int H) { return ((H / kStreams + 31) / 32) * 32; }
 
-// Allow `bytes` of dynamic shared memory and ask for the largest shared
-// memory carve-out, so that as many CTAs fit per SM as their tables allow.
-// Done once per (device, kernel) with the largest size any codec call can
-// need, so that later calls (and calls inside a stream capture) make no
-// attribute call at all.
-int set_smem(const void* fn, size_t bytes) {
+// CTAs per unit of work (a slice for the CDF pass, a region for the coder,
+// compaction and decoder).  A unit's threads are spread over `split` CTAs so
+// that a small batch still reaches every SM: the split that minimises the
+// most whole units' worth of CTAs one SM must take (ties to the smaller),
+// among those that leave every CTA a whole number of warps of threads.
+int choose_split(int64_t units, int H, int sms) {
+    int best = 1;
+    double best_load = 0;
+    for (int S = 1; S <= 4; S *= 2) {
+        if (S > 1 && (H % (kStreams * S) != 0 || (H / (kStreams * S)) % 32 != 0)) continue;
+        const double load = (double)((units * S + sms - 1) / sms) / S;
+        if (S == 1 || load < best_load) {
+            best = S;
+            best_load = load;
+        }
+    }
+    return best;
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+        return 0;
+    return n;
+}
+
+// Allow the largest dynamic shared memory any codec call can need and ask for
+// the largest shared memory carve-out, so that as many CTAs fit per SM as
+// their tables allow.  Done once per (device, kernel), so that later calls
+// (and calls inside a stream capture) make no attribute call at all.
+int set_smem(const void* fn) {
     static std::mutex mu;
     static std::set<std::pair<int, const void*>> done;
     int dev = 0;
@@ -912,7 +1070,6 @@ int set_smem(const void* fn, size_t bytes) {
     std::lock_guard<std::mutex> lock(mu);
     if (done.count({dev, fn})) return LMKV_OK;
     const size_t most = (size_t)32 * LMKV_CACHEGEN_MAX_CHANNELS * 2;    // 32 table rows of 2-byte entries
-    (void)bytes;
     if (lmkv_internal_cuda_status(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                       (int)most)) != LMKV_OK ||
         lmkv_internal_cuda_status(cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -967,17 +1124,18 @@ int run(Dir dir, void* const* chunk_ptrs, void* const* blob_ptrs, uint64_t* size
         p.block_size = pf->pool->block_size;
     }
     const int threads = threads_for(H);
-    const bool wide = threads > 256;
-    const size_t table_bytes = (size_t)max_nsym * H * 2;
-    const size_t search_bytes = (size_t)(max_nsym > 16 ? 32 : 16) * H * 2;
+    const int sms = sm_count();
+    if (sms == 0) {
+        lmkv_internal_cuda_status(cudaGetLastError());
+        return LMKV_ERR_CUDA;
+    }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (dir == Dir::kEncode) {
-        if (set_smem((const void*)cg_cdf_kernel, table_bytes) != LMKV_OK ||
-            set_smem(wide ? (const void*)cg_code_kernel<512> : (const void*)cg_code_kernel<256>,
-                     table_bytes) != LMKV_OK)
+        if (set_smem((const void*)cg_cdf_kernel) != LMKV_OK || set_smem((const void*)cg_code_kernel<512>) != LMKV_OK ||
+            set_smem((const void*)cg_code_kernel<256>) != LMKV_OK || set_smem((const void*)cg_compact_kernel) != LMKV_OK)
             return LMKV_ERR_CUDA;
-    } else if (set_smem(wide ? (const void*)cg_decode_kernel<512> : (const void*)cg_decode_kernel<256>,
-                        search_bytes) != LMKV_OK) {
+    } else if (set_smem((const void*)cg_decode_kernel<512>) != LMKV_OK ||
+               set_smem((const void*)cg_decode_kernel<256>) != LMKV_OK) {
         return LMKV_ERR_CUDA;
     }
     uint64_t at = 0;
@@ -1002,17 +1160,38 @@ int run(Dir dir, void* const* chunk_ptrs, void* const* blob_ptrs, uint64_t* size
         p.chunk_ptrs = chunk_ptrs ? reinterpret_cast<const uint8_t* const*>(chunk_ptrs) + g0 : nullptr;
         p.blob_ptrs = reinterpret_cast<uint8_t* const*>(blob_ptrs) + g0;
         p.sizes = sizes + g0;
-        const dim3 slices(2 * L, cnt), regions(nb_max * 2 * L, cnt);
+        int64_t units = 0;
+        for (int i = 0; i < cnt; ++i) units += (int64_t)batches_of(p.ntok[i]) * 2 * L;
+        const int S = choose_split(units, H, sms);
+        p.split = S;
+        const int part_threads = threads_for(H / S);       // = H / (kStreams S) when S > 1
+        const size_t table_bytes = (size_t)max_nsym * (H / S) * 2;
+        const size_t search_bytes = (size_t)(max_nsym > 16 ? 32 : 16) * (H / S) * 2;
+        const dim3 regions(nb_max * 2 * L * S, cnt);
         if (dir == Dir::kEncode) {
-            cg_cdf_kernel<<<slices, threads, table_bytes, st>>>(p);
-            if (wide) cg_code_kernel<512><<<regions, threads, table_bytes, st>>>(p);
-            else cg_code_kernel<256><<<regions, threads, table_bytes, st>>>(p);
-            cg_compact_kernel<<<regions, threads, (size_t)H * 8, st>>>(p);
+            // one cluster of S CTAs per slice
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            cfg.gridDim = dim3(2 * L * S, cnt);
+            cfg.blockDim = dim3(threads);
+            cfg.dynamicSmemBytes = (size_t)max_nsym * H * 2;
+            cfg.stream = st;
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = S;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = S > 1 ? 1 : 0;
+            if (lmkv_internal_cuda_status(cudaLaunchKernelEx(&cfg, cg_cdf_kernel, p)) != LMKV_OK)
+                return LMKV_ERR_CUDA;
+            if (part_threads > 256) cg_code_kernel<512><<<regions, part_threads, table_bytes, st>>>(p);
+            else cg_code_kernel<256><<<regions, part_threads, table_bytes, st>>>(p);
+            cg_compact_kernel<<<regions, threads, (size_t)H * 8 + kStage + 16, st>>>(p);
             lmkv_internal_add_launches(3);
         } else {
-            cg_total_kernel<<<regions, 256, 0, st>>>(p);
-            if (wide) cg_decode_kernel<512><<<regions, threads, search_bytes, st>>>(p);
-            else cg_decode_kernel<256><<<regions, threads, search_bytes, st>>>(p);
+            cg_total_kernel<<<dim3(nb_max * 2 * L, cnt), 256, 0, st>>>(p);
+            if (part_threads > 256) cg_decode_kernel<512><<<regions, part_threads, search_bytes, st>>>(p);
+            else cg_decode_kernel<256><<<regions, part_threads, search_bytes, st>>>(p);
             lmkv_internal_add_launches(2);
         }
         if (lmkv_internal_cuda_status(cudaGetLastError()) != LMKV_OK) return LMKV_ERR_CUDA;

@@ -231,8 +231,15 @@ class Pool:
 
 
 def pointer_array(tensors: Sequence[torch.Tensor], device) -> torch.Tensor:
-    """DEVICE int64 array of the tensors' data pointers (chunk_ptrs / code_ptrs)."""
-    return torch.tensor([t.data_ptr() for t in tensors], dtype=torch.int64, device=device)
+    """DEVICE int64 array of the tensors' data pointers (chunk_ptrs / code_ptrs).
+
+    The copy is queued on the current stream from pinned host memory, so the
+    host does not wait for the device (the caching host allocator keeps the
+    pinned block until the copy has run)."""
+    host = torch.tensor([t.data_ptr() for t in tensors], dtype=torch.int64)
+    if torch.device(device).type != "cuda":
+        return host.to(device)
+    return host.pin_memory().to(device, non_blocking=True)
 
 
 def count_chunks(start, end, chunk_size: int, save_unfull: bool) -> int:

@@ -207,11 +207,12 @@ CACHEGEN_CHUNK_SIZES = (64, 128, 256, 768)
 
 
 def cachegen_chunks(num_layers: int, channels: int, ntoks, seed: int, device="cpu",
-                    outliers: bool = False, zero_rows: int = 0) -> list:
+                    outliers: bool = False, zero_rows: int = 0, tiny_rows: int = 0) -> list:
     """Chunk buffers [2][L][n][H] bf16 ~ N(0, 1), one per entry of ntoks, drawn
     on the CPU from a seeded generator (so every device sees the same values),
-    optionally with 1% of each (K/V, layer)'s channels scaled x20 and the
-    first `zero_rows` token rows of every slice set to zero."""
+    optionally with 1% of each (K/V, layer)'s channels scaled x20, the first
+    `zero_rows` token rows of every slice set to zero and the next `tiny_rows`
+    scaled by 1e-39 (bf16 subnormals, some of them zero)."""
     g = generator("cpu", seed)
     out = []
     for n in ntoks:
@@ -224,5 +225,7 @@ def cachegen_chunks(num_layers: int, channels: int, ntoks, seed: int, device="cp
                     x[kv, l, :, idx] *= 20.0
         if zero_rows:
             x[:, :, :zero_rows] = 0
+        if tiny_rows:
+            x[:, :, zero_rows:zero_rows + tiny_rows] *= 1e-39
         out.append(x.to(torch.bfloat16).to(device))
     return out

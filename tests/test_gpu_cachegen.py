@@ -75,6 +75,8 @@ def check_against_oracle(L, H, ntoks, seed, bins=None, **kw):
     (2, 40, [5, 256, 300]),            # ragged last batch, 10 of 32 lanes
     (3, 128, [257, 513, 64]),          # three batches
     (2, 96, [1000]),
+    (1, 512, [1, 3, 5]),               # chunks shorter than their CTAs per slice
+    (2, 1024, [256, 767]),
 ])
 def test_small_shapes_exact(L, H, ntoks):
     bins = cg.default_bins(L)
@@ -91,6 +93,12 @@ def test_benchmark_shape_exact(n):
 
 def test_outliers_and_zero_rows_exact():
     check_against_oracle(4, 1024, [256, 100], seed=5, outliers=True, zero_rows=3)
+
+
+def test_subnormal_rows_exact():
+    """Rows of bf16 subnormals: MAX / max1 overflows to +inf, so the symbols
+    are 2*MAX, 0, and 0 for the zero entries (0 * inf)."""
+    check_against_oracle(2, 256, [40, 300], seed=6, zero_rows=1, tiny_rows=5)
 
 
 def test_largest_sizes_exact():
@@ -160,6 +168,10 @@ def _oracle_gather(w, layers_dev, table, chunks):
     wl.Workload("cg-small", 3, 2, 64, 16, 96, (300, 700), chunk_size=256),
     wl.Workload("cg-ragged", 2, 1, 32, 32, 80, (100, 64, 900), req_start=(0, 0, 256), chunk_size=128),
     wl.Workload("cg-no-tail", 2, 2, 64, 16, 64, (700,), chunk_size=256, save_unfull=False),
+    # few regions of wide rows: each slice and region spread over several CTAs,
+    # whose row ranges start inside pages
+    wl.Workload("cg-wide-few", 2, 4, 128, 16, 96, (300, 200), chunk_size=256),
+    wl.Workload("cg-wide-offset", 3, 8, 128, 16, 400, (1100, 1412), req_start=(0, 512), chunk_size=512),
 ], ids=lambda w: w.name)
 def test_pool_store_and_retrieve_exact(w):
     """lmkv_cachegen_store_chunks gives the oracle's blobs of the oracle's
