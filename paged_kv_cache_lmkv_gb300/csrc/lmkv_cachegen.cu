@@ -2,18 +2,21 @@
 // 压缩：CacheGen 编解码原理、配置方式与源码解析", sections 1-5).
 //
 // Encode, per group of up to kMaxChunks chunks (three kernels):
-//   cg_cdf_kernel     one CTA per (chunk, kv, layer): per-token absmax over the
+//   cg_cdf_kernel     per (chunk, kv, layer) slice: per-token absmax over the
 //                     row (section 2), the symbols (into the workspace), a
 //                     per-channel histogram in shared memory and the 2^16 CDF
 //                     with its arange ramp (section 3), written to the blob.
-//   cg_code_kernel    one CTA per (chunk, 256-token batch, kv, layer): every
+//   cg_code_kernel    per (chunk, 256-token batch, kv, layer) region: every
 //                     thread runs kStreams independent arithmetic coders, one
 //                     per channel (section 4), into fixed-size slots.
-//   cg_compact_kernel one CTA per region: the prefix sums of the stream lengths
-//                     place each slot's bytes into the blob.
+//   cg_compact_kernel per region: the prefix sums of the stream lengths place
+//                     each slot's bytes into the blob.
 // Decode (two kernels): cg_total_kernel sums each region's lengths, then
 // cg_decode_kernel finds each stream by the prefix sums (section 5), decodes
 // kStreams channels per thread and writes the dequantised bf16 rows.
+// A slice or region takes 1, 2 or 4 CTAs (CgParams::split, chosen per launch
+// so that a small batch still covers the SMs): the CDF pass splits the rows
+// over a thread-block cluster, the other kernels split the channels.
 //
 // The coder is the integer arithmetic coder of Witten, Neal and Cleary
 // (CACM 30(6), 1987) with 32-bit registers and frequencies out of 2^16.  Its
