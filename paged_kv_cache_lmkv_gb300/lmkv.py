@@ -581,20 +581,49 @@ class CachegenCodec:
     one codec object must be ordered on one stream (they share the
     workspace)."""
 
+    _POINTER_CACHE = 32      # pointer arrays kept for reuse
+
     def __init__(self, num_layers: int, channels: int, bins=None, device="cuda"):
         self.num_layers, self.channels = num_layers, channels
         self.bins = _i32_array(cachegen_default_bins(num_layers) if bins is None else bins)
         self.device = torch.device(device)
         self.workspace = torch.empty(0, dtype=torch.uint8, device=self.device)
+        self._need = {}          # token counts -> workspace bytes
+        self._ptrs = {}          # data pointers -> (device pointer array, event after its copy)
 
     def layout(self, num_tokens: int) -> CachegenLayout:
         return cachegen_layout(self.num_layers, num_tokens, self.channels, self.bins)
 
     def _workspace(self, ntok):
-        need = cachegen_workspace_bytes(self.num_layers, self.channels, ntok)
+        key = tuple(ntok)
+        need = self._need.get(key)
+        if need is None:
+            need = self._need[key] = cachegen_workspace_bytes(self.num_layers, self.channels, ntok)
         if self.workspace.numel() < need:
             self.workspace = torch.empty(need, dtype=torch.uint8, device=self.device)
         return self.workspace
+
+    def _pointers(self, tensors):
+        """The device pointer array of the tensors, reused while the same
+        addresses come back (a serving loop with fixed buffers builds it once).
+        The current stream waits for the copy that filled it (outside a
+        stream capture; warm up before capturing)."""
+        key = tuple(t.data_ptr() for t in tensors)
+        hit = self._ptrs.pop(key, None)
+        if hit is None:
+            arr = pointer_array(tensors, self.device)
+            ev = torch.cuda.Event()
+            ev.record(torch.cuda.current_stream(self.device))
+            hit = (arr, ev)
+            if len(self._ptrs) >= self._POINTER_CACHE:
+                self._ptrs.pop(next(iter(self._ptrs)))
+        else:
+            cur = torch.cuda.current_stream(self.device)
+            if not torch.cuda.is_current_stream_capturing():
+                cur.wait_event(hit[1])
+            hit[0].record_stream(cur)    # evicted later: freed only after this stream's use
+        self._ptrs[key] = hit            # most recently used last
+        return hit[0]
 
     def encode(self, chunks, blobs=None, sizes=None, status=None, stream=None):
         """Encode the chunk tensors; returns (blobs, sizes): device uint8 tensors
@@ -606,7 +635,7 @@ class CachegenCodec:
         if sizes is None:
             sizes = torch.zeros(len(chunks), dtype=torch.int64, device=self.device)
         ws = self._workspace(ntok)
-        cptr, bptr = pointer_array(chunks, self.device), pointer_array(blobs, self.device)
+        cptr, bptr = self._pointers(chunks), self._pointers(blobs)
         self._order(stream, cptr, bptr)
         check(cachegen_encode(cptr, ntok, self.num_layers, self.channels, self.bins, bptr, sizes, ws,
                               status, stream), "lmkv_cachegen_encode")
@@ -633,7 +662,7 @@ class CachegenCodec:
         if sizes is None:
             sizes = torch.zeros(len(ntok), dtype=torch.int64, device=self.device)
         ws = self._workspace(ntok)
-        bptr = pointer_array(blobs, self.device)
+        bptr = self._pointers(blobs)
         self._order(stream, bptr)
         check(cachegen_store_chunks(pool, block_table, start, end, chunk_size, save_unfull, self.bins,
                                     bptr, sizes, ws, status, stream), "lmkv_cachegen_store_chunks")
@@ -644,7 +673,7 @@ class CachegenCodec:
         """Decode blobs straight into the pool's pages of a retrieve call's chunks."""
         ntok = [n for _, _, n in enumerate_chunks(start, end, chunk_size, save_unfull)]
         ws = self._workspace(ntok)
-        bptr = pointer_array(blobs, self.device)
+        bptr = self._pointers(blobs)
         self._order(stream, bptr)
         check(cachegen_retrieve_chunks(pool, block_table, start, end, chunk_size, save_unfull, self.bins,
                                        bptr, sizes, ws, status, stream), "lmkv_cachegen_retrieve_chunks")
@@ -653,7 +682,7 @@ class CachegenCodec:
         """Decode into the chunk tensors (their token counts give n)."""
         ntok = [int(c.shape[2]) for c in chunks]
         ws = self._workspace(ntok)
-        bptr, cptr = pointer_array(blobs, self.device), pointer_array(chunks, self.device)
+        bptr, cptr = self._pointers(blobs), self._pointers(chunks)
         self._order(stream, bptr, cptr)
         check(cachegen_decode(bptr, sizes, ntok, self.num_layers, self.channels, self.bins, cptr, ws,
                               status, stream), "lmkv_cachegen_decode")

@@ -304,6 +304,36 @@ def test_codec_calls_capture_in_a_cuda_graph():
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
+def test_codec_reuses_pointer_arrays():
+    """Calls with the same buffers reuse one device pointer array each and give
+    the same blobs; new buffers (another stream) get their own."""
+    L, H, ntoks = 2, 512, [256, 77]
+    codec = pkg.CachegenCodec(L, H, device=DEV)
+    x = wl.cachegen_chunks(L, H, ntoks, seed=41, device=DEV)
+    expect = [cg.encode_chunk(c.cpu(), codec.bins) for c in x]
+    blobs, sizes = codec.encode(x)
+    cached = len(codec._ptrs)
+    for _ in range(3):
+        codec.encode(x, blobs, sizes)
+    assert len(codec._ptrs) == cached
+    torch.cuda.synchronize()
+    got = [b[:s].cpu().numpy().tobytes() for b, s in zip(blobs, sizes.cpu().tolist())]
+    assert got == expect
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        x2 = [t.clone() for t in x]
+        blobs2, sizes2 = codec.encode(x2)
+        outs = [torch.empty_like(t) for t in x2]
+        codec.decode(blobs2, sizes2, outs)
+    torch.cuda.synchronize()
+    assert len(codec._ptrs) == cached + 3
+    got2 = [b[:s].cpu().numpy().tobytes() for b, s in zip(blobs2, sizes2.cpu().tolist())]
+    assert got2 == expect
+    for o, e, n in zip(outs, expect, ntoks):
+        assert np.array_equal(host_u16(o), cg.decode_chunk(e, L, n, H, codec.bins))
+
+
 def test_bad_pointers_skip_the_chunk():
     """A null or misaligned blob, a misaligned chunk buffer: that chunk is
     skipped by every kernel (size 0, nothing written) and the call reports
