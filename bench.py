@@ -65,7 +65,8 @@ def parse_args():
                     help="skip the layer-wise pipeline measurement (host round trip per layer)")
     ap.add_argument("--codec-chunks", type=int, default=40,
                     help="--case codec: number of 256-token chunks")
-    ap.add_argument("--case", choices=["llama8b", "profile-small", "codec", "llama70b"], default="llama8b",
+    ap.add_argument("--case", choices=["llama8b", "profile-small", "codec", "llama70b", "qwen32b"],
+                    default="llama8b",
                     help="profile-small: the 8B shape with a 1024-block pool and a 4096-token "
                          "request (16 chunks), for ncu captures only")
     return ap.parse_args()
@@ -1000,6 +1001,103 @@ def config_dict(w, c):
             "parallelism": "replicas (one independent batch per GPU, no collective)"}
 
 
+def plain_copy_per_layer(c: Ctx, stream, reps: int = 20):
+    """Context for the per-layer rows: a plain contiguous device copy
+    (torch's copy kernel) of one layer's payload, issued num_layers times
+    back to back on the stream after an L2 flush, like one per-layer phase.
+    It shows what a copy of that size reaches without any paging."""
+    w = c.w
+    layer_bytes = c.payload // w.num_layers
+    # one slice per layer, like the per-layer calls: the phase moves more
+    # than L2 holds, so no call finds its data in L2
+    src = torch.empty((w.num_layers, layer_bytes // 2), dtype=torch.bfloat16, device=c.dev)
+    dst = torch.empty_like(src)
+    src.fill_(1.0)
+    times = []
+    with torch.cuda.stream(stream):
+        for k in range(reps + 3):
+            c.flush.fill_(k & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for l in range(w.num_layers):
+                dst[l].copy_(src[l])
+            e1.record(stream)
+            e1.synchronize()
+            if k >= 3:
+                times.append(e0.elapsed_time(e1))
+    ms = statistics.median(times)
+    us = ms * 1e3 / w.num_layers
+    return {"what": "torch dst.copy_(src) of one layer's payload (contiguous, no pages), "
+                    f"{w.num_layers} back to back, median of {reps}",
+            "bytes_per_call": int(2 * layer_bytes), "us_per_call": round(us, 2),
+            "GB/s": round(2 * layer_bytes / (us * 1e-6) / 1e9, 1)}
+
+
+def bench_qwen_sweep(args, dev, stream, rank, world, local):
+    """--case qwen32b: the device phases on the Qwen2.5-32B KV shape (64 layers,
+    8 KV heads x 128, one 16384-token request = 64 chunks, 1% of channels x20)
+    at page sizes 16, 32 and 64 tokens (65536 token slots per layer).  Each
+    page size is set up, timed like the default case, and freed before the
+    next.  `value` = bytes of all three steps / their summed device time."""
+    peak, peak_src = load_peaks()
+    sweep, tot_bytes, tot_ms, launches, clocks = {}, 0, 0.0, 0, []
+    for bs in (16, 32, 64):
+        w = wl.qwen_with_block_size(bs)
+        c = setup(dev, w)
+        per_phase, n_launch, clk, _ = bench_device(c, args, stream, rank, world, local)
+        phase_ms = {n: statistics.mean(v) for n, v in per_phase.items()}
+        entry = {}
+        for n in PHASES:
+            gbs = c.phase_bytes[n] / (phase_ms[n] * 1e-3) / 1e9
+            entry[n] = {"ms": round(phase_ms[n], 4), "GB/s": round(gbs, 1),
+                        "frac_of_peak": round(gbs / peak, 4)}
+        for n in ("gather_layer", "scatter_layer"):
+            entry[n]["us_per_call"] = round(phase_ms[n] * 1e3 / w.num_layers, 2)
+        step_ms, step_bytes = sum(phase_ms.values()), sum(c.phase_bytes.values())
+        entry["step"] = {"ms": round(step_ms, 4), "bytes": int(step_bytes),
+                         "GB/s": round(step_bytes / (step_ms * 1e-3) / 1e9, 1)}
+        sweep[f"block_size_{bs}"] = entry
+        tot_bytes += step_bytes
+        tot_ms += step_ms
+        launches += n_launch
+        clocks.append(clk)
+        del c
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
+    total_ms = max_over_ranks(tot_ms * args.steps, world)
+    value = job_value(tot_bytes, world, args.steps, total_ms)
+    g = sweep["block_size_16"]["gather"]
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 KV, 1% of channels x20 "
+                                     "per (K/V, layer), random block tables)",
+            "config": {"workload": "qwen2.5-32b KV batch: 64 layers x 8 KV heads x head_dim 128 "
+                                   "bf16 with outlier channels, one 16384-token request = 64 "
+                                   "chunks of 256, pages of 16 / 32 / 64 tokens (65536 token "
+                                   "slots per layer); one step = the six phases at each page size",
+                       "steps_include": list(PHASES), "per_layer_calls": 64,
+                       "bytes_per_step": int(tot_bytes),
+                       "l2": "flushed between phases (256 MiB fill, outside the timed events); "
+                             "every phase also reads > 1 GB, larger than L2",
+                       "parallelism": "replicas (one independent batch per GPU, no collective)"},
+            "frac_of_hbm_peak": round(value / world / peak, 4),
+            "roofline": {"bound": "hbm", "kernel": "lmkv gather_chunks (move_lsu_kernel<gather>), "
+                                                   "16-token pages",
+                         "achieved": g["GB/s"], "peak": peak, "unit": "GB/s",
+                         "frac": g["frac_of_peak"], "peak_source": f"{peak_src} hbm_gbs",
+                         "traffic": None},
+            "page_size_sweep": sweep,
+            "e2e": None,
+            "cpu_baseline": None,
+            "gpu_launches": int(launches),
+            "clocks": clocks,
+        }
+        print(json.dumps(out), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
@@ -1025,8 +1123,14 @@ def main():
         # each other; device phases only
         w = wl.LLAMA70B.with_(num_blocks=4608)
         args.no_pipeline = args.no_cachegen = args.no_cpu_baseline = True
-    c = setup(dev, w)
     stream = torch.cuda.Stream(dev)
+    if args.case == "qwen32b":
+        bench_qwen_sweep(args, dev, stream, rank, world, local)
+        if world > 1:
+            torch.distributed.barrier()
+            torch.distributed.destroy_process_group()
+        return
+    c = setup(dev, w)
     try:
         per_phase, launches, clk, wall = bench_device(c, args, stream, rank, world, local)
     except pkg.LmkvError as exc:
@@ -1053,6 +1157,7 @@ def main():
                         "frac_of_peak": round(gbs / peak, 4)}
     breakdown["gather_layer"]["us_per_call"] = round(phase_ms["gather_layer"] * 1e3 / w.num_layers, 2)
     breakdown["scatter_layer"]["us_per_call"] = round(phase_ms["scatter_layer"] * 1e3 / w.num_layers, 2)
+    breakdown["per_layer_plain_copy"] = plain_copy_per_layer(c, stream)
     e2e = bench_e2e(c, args, stream) if args.case != "llama70b" else None
     pipeline = bench_layer_pipeline(c) if not args.no_pipeline else None
     decode = bench_decode_store(c) if not args.no_pipeline else None

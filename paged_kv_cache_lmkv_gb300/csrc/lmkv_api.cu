@@ -241,12 +241,22 @@ int launch_move(const Call& c, cudaStream_t stream) {
     });
 }
 
-// (Measured on the 8B layer-wise calls: splitting 32 KiB runs into 2, 4 or 8
-// parts was 2-120% slower than one CTA per run.)
-int32_t choose_parts(const lmkv_pool_t* pool, int32_t layer_n) {
-    (void)pool;
-    (void)layer_n;
-    return 1;
+// Items of about 32 KiB: a page larger than that is split into equal parts
+// (a divisor of block_size), so that calls on 32- and 64-token pages launch
+// as many CTAs of the same size as calls on 16-token pages of 2 KiB rows
+// (one per-layer call on 64-token pages otherwise has a quarter of the CTAs,
+// each looping four times).  Pages of up to 32 KiB stay whole: splitting the
+// 8B layer-wise calls' 32 KiB runs into 2, 4 or 8 parts measured 2-120%
+// slower than one CTA per run.
+constexpr int64_t kItemBytes = 32 * 1024;
+
+int32_t choose_parts(const lmkv_pool_t* pool) {
+    const int64_t row = (int64_t)pool->num_kv_heads * pool->head_dim * pool->elem_bytes;
+    const int64_t page = row * pool->block_size;
+    int32_t parts = 1;
+    for (int32_t q = 2; q <= pool->block_size && page / q >= kItemBytes; ++q)
+        if (pool->block_size % q == 0) parts = q;
+    return parts;
 }
 
 int move_entry(bool gather, const lmkv_pool_t* pool, const int32_t* block_table,
@@ -262,7 +272,7 @@ int move_entry(bool gather, const lmkv_pool_t* pool, const int32_t* block_table,
         c.layer_lo = layer;
         c.layer_n = 1;
     }
-    c.parts = choose_parts(pool, c.layer_n);
+    c.parts = choose_parts(pool);
     const int rc = validate(c);
     if (rc != LMKV_OK || c.num_chunks == 0) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -326,7 +336,7 @@ int staged_entry(bool store, const lmkv_pool_t* pool, const int32_t* block_table
         return LMKV_ERR_INVALID_ARG;
     if (layer_n == 0) return LMKV_OK;
     Call c{pool, block_table, max_blocks, start, end, num_req, chunk_size, save_unfull,
-           host_chunks, d_status, layer_lo, layer_n, 1, 0, 0, staging};
+           host_chunks, d_status, layer_lo, layer_n, choose_parts(pool), 0, 0, staging};
     rc = validate(c);
     if (rc != LMKV_OK || c.num_chunks == 0) return rc;
     const int64_t rb = (int64_t)pool->num_kv_heads * pool->head_dim * pool->elem_bytes;
@@ -552,7 +562,7 @@ int fp8_entry(bool gather, const lmkv_pool_t* pool, const int32_t* block_table, 
     int rc = check_fp8_pool(pool, chunk_size);
     if (rc != LMKV_OK) return rc;
     Call c{pool, block_table, max_blocks, start, end, num_req, chunk_size, save_unfull,
-           code_ptrs, d_status, 0, pool->num_layers, 1, 0, 0, nullptr};
+           code_ptrs, d_status, 0, pool->num_layers, choose_parts(pool), 0, 0, nullptr};
     rc = validate(c);
     if (rc != LMKV_OK || c.num_chunks == 0) return rc;
     if (scales == nullptr) return LMKV_ERR_INVALID_ARG;

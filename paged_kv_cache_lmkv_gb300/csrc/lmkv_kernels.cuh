@@ -669,15 +669,21 @@ quant_gather_hybrid_kernel(const __grid_constant__ B p) {
         }
         for (int i = lane; i < kQuantMaxRows / 32; i += 32) row_ok[i] = 0;
         __syncwarp();
+        // One bulk copy per piece of P = block_size / parts rows (pages of at
+        // most 32 KiB are one piece; larger pages are cut so that several
+        // copies are in flight, as with small pages).  Piece i covers slice
+        // rows [i*P, (i+1)*P), inside page i / parts.
         const uint32_t bs = (uint32_t)p.block_size;
+        const uint32_t P = bs / (uint32_t)p.parts;
+        const UDiv pdiv(P), qdiv((uint32_t)p.parts);
         const uint32_t s0 = r0 + h;
-        const uint32_t jb0 = nrows_s ? sm.bdiv.div(s0) : 0u;
-        const uint32_t jb_end = nrows_s ? sm.bdiv.div(s0 + nrows_s - 1) + 1 : 0u;
+        const uint32_t pi0 = nrows_s ? pdiv.div(s0) : 0u;
+        const uint32_t pi_end = nrows_s ? pdiv.div(s0 + nrows_s - 1) + 1 : 0u;
         uint32_t bytes = 0;
         bool bad = false;
-        for (uint32_t jb = jb0 + lane; ptr_ok && jb < jb_end; jb += 32) {
-            const uint32_t a = max(s0, jb * bs), e = min(s0 + nrows_s, (jb + 1) * bs);
-            const int32_t blk = sm.bt[jb];
+        for (uint32_t pi = pi0 + lane; ptr_ok && pi < pi_end; pi += 32) {
+            const uint32_t a = max(s0, pi * P), e = min(s0 + nrows_s, (pi + 1) * P);
+            const int32_t blk = sm.bt[qdiv.div(pi)];
             if ((uint32_t)blk < (uint32_t)p.num_blocks) {
                 bytes += (e - a) * row_bytes;
                 for (uint32_t r = a - s0; r < e - s0; ++r) atomicOr(&row_ok[r >> 5], 1u << (r & 31));
@@ -692,8 +698,9 @@ quant_gather_hybrid_kernel(const __grid_constant__ B p) {
             mbar_arrive_expect_tx(&bar, total);
         }
         __syncwarp();
-        for (uint32_t jb = jb0 + lane; ptr_ok && jb < jb_end; jb += 32) {
-            const uint32_t a = max(s0, jb * bs), e = min(s0 + nrows_s, (jb + 1) * bs);
+        for (uint32_t pi = pi0 + lane; ptr_ok && pi < pi_end; pi += 32) {
+            const uint32_t a = max(s0, pi * P), e = min(s0 + nrows_s, (pi + 1) * P);
+            const uint32_t jb = qdiv.div(pi);
             const int32_t blk = sm.bt[jb];
             if ((uint32_t)blk < (uint32_t)p.num_blocks)
                 bulk_g2s(slice + (size_t)(a - s0) * row_bytes,
