@@ -63,6 +63,8 @@ def parse_args():
                     help="skip the CacheGen codec measurement")
     ap.add_argument("--no-pipeline", action="store_true",
                     help="skip the layer-wise pipeline measurement (host round trip per layer)")
+    ap.add_argument("--no-context", action="store_true",
+                    help="skip the context gathers (torch index_select, one copy per page)")
     ap.add_argument("--codec-chunks", type=int, default=40,
                     help="--case codec: number of 256-token chunks")
     ap.add_argument("--case", choices=["llama8b", "profile-small", "codec", "llama70b", "qwen32b"],
@@ -1033,6 +1035,71 @@ def plain_copy_per_layer(c: Ctx, stream, reps: int = 20):
             "GB/s": round(2 * layer_bytes / (us * 1e-6) / 1e9, 1)}
 
 
+def context_gathers(c: Ctx, stream, reps: int = 5):
+    """Context for the gather row, two ways of doing the same movement without
+    this library (single request of full chunks only):
+      index_select: per (layer, K/V) one torch index_select of the batch's
+        token rows into a [T, H*D] temporary, then one strided copy into a
+        [G, 2, L, 256, H*D] chunk tensor (a PyTorch user's composition; it
+        moves every byte twice);
+      per_page_copy: one torch copy (a cudaMemcpyAsync device-to-device) per
+        (chunk, K/V, layer, page): the per-page transfer pattern the LMCache
+        paper sets its chunked transfers against, issued from Python.
+    Both are timed with CUDA events on the stream after a warm-up, L2 flushed
+    first; GB/s counts the gather's algorithmic bytes."""
+    w = c.w
+    if len(w.ends) != 1 or int(w.starts[0]) != 0 or int(w.ends[0]) % w.chunk_size:
+        return None
+    T, G, HD, B = int(w.ends[0]), int(w.ends[0]) // w.chunk_size, w.row_elems, w.block_size
+    bt = torch.from_numpy(c.table[0, :T // B].astype(np.int64)).to(c.dev)
+    rows = (bt[:, None] * B + torch.arange(B, device=c.dev)[None, :]).reshape(-1)
+    out = torch.empty((G, 2, w.num_layers, w.chunk_size, HD), dtype=torch.bfloat16, device=c.dev)
+    tmp = torch.empty((T, HD), dtype=torch.bfloat16, device=c.dev)
+
+    def via_index_select():
+        for l in range(w.num_layers):
+            for kv in range(2):
+                torch.index_select(c.pool.layers[l][kv].view(-1, HD), 0, rows, out=tmp)
+                out[:, kv, l].copy_(tmp.view(G, w.chunk_size, HD))
+
+    blocks = c.table[0, :T // B].tolist()
+    per_chunk = w.chunk_size // B
+
+    def via_per_page():
+        for g in range(G):
+            for kv in range(2):
+                for l in range(w.num_layers):
+                    src = c.pool.layers[l][kv]
+                    dst = out[g, kv, l]
+                    for j in range(per_chunk):
+                        dst[j * B:(j + 1) * B].copy_(src[blocks[g * per_chunk + j]])
+
+    res = {}
+    with torch.cuda.stream(stream):
+        for name, fn, n in (("index_select", via_index_select, reps), ("per_page_copy", via_per_page, 1)):
+            fn()
+            times = []
+            for k in range(n):
+                c.flush.fill_(k & 0xFF)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                e1.synchronize()
+                times.append(e0.elapsed_time(e1))
+            ms = statistics.median(times)
+            res[name] = {"ms": round(ms, 3),
+                         "GB/s": round(c.phase_bytes["gather"] / (ms * 1e-3) / 1e9, 1)}
+    ok = all(torch.equal(out[g].view(torch.int16), c.bufs[g].view(torch.int16)) for g in range(G))
+    res["per_page_copies"] = G * 2 * w.num_layers * per_chunk
+    res["matches_library_gather"] = bool(ok)
+    res["what"] = ("same gather without this library: torch index_select + strided copy per "
+                   "(layer, K/V); one torch D2D copy per page issued from Python (the "
+                   "per-page pattern); algorithmic bytes, L2 flushed before each timing")
+    del out, tmp
+    return res
+
+
 def bench_qwen_sweep(args, dev, stream, rank, world, local):
     """--case qwen32b: the device phases on the Qwen2.5-32B KV shape (64 layers,
     8 KV heads x 128, one 16384-token request = 64 chunks, 1% of channels x20)
@@ -1158,6 +1225,7 @@ def main():
     breakdown["gather_layer"]["us_per_call"] = round(phase_ms["gather_layer"] * 1e3 / w.num_layers, 2)
     breakdown["scatter_layer"]["us_per_call"] = round(phase_ms["scatter_layer"] * 1e3 / w.num_layers, 2)
     breakdown["per_layer_plain_copy"] = plain_copy_per_layer(c, stream)
+    context = context_gathers(c, stream) if not args.no_context else None
     e2e = bench_e2e(c, args, stream) if args.case != "llama70b" else None
     pipeline = bench_layer_pipeline(c) if not args.no_pipeline else None
     decode = bench_decode_store(c) if not args.no_pipeline else None
@@ -1181,6 +1249,7 @@ def main():
                          "traffic": profiled_traffic() if args.case == "llama8b" else None,
                          "algorithmic_bytes_per_launch": int(c.phase_bytes["gather"])},
             "breakdown": breakdown,
+            "context_gathers": context,
             "e2e": e2e,
             "layer_pipeline": pipeline,
             "decode_store": decode,
