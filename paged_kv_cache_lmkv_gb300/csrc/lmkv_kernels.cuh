@@ -92,6 +92,18 @@ __device__ __forceinline__ void pdl_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// x / d for a runtime divisor that is usually a power of two.
+struct UDiv {
+    uint32_t d;
+    int32_t shift;      // log2(d) when d is a power of two, else -1
+    __device__ __forceinline__ explicit UDiv(uint32_t dv) : d(dv), shift(-1) {
+#ifdef __CUDA_ARCH__
+        if (__popc(dv) == 1) shift = __ffs(dv) - 1;
+#endif
+    }
+    __device__ __forceinline__ uint32_t div(uint32_t x) const { return shift >= 0 ? x >> shift : x / d; }
+};
+
 struct ChunkRef {
     int32_t req_row;
     int32_t ntok;
@@ -129,18 +141,44 @@ struct Run {
     uint8_t* pool;
     uint8_t* chunk;
     uint32_t bytes;
+    int32_t kv, ll, gl;     // the item's K/V half, layer (within the call) and local chunk
 };
+
+// item -> (chunk gl, kv, layer ll, page j, part q).  Items below 2^32 (every
+// launch in practice) are split with 32-bit shifts or divisions: the 64-bit
+// divisions by runtime values are a long serial chain at the start of every
+// CTA.
+template <class B>
+__device__ __forceinline__ void decode_item(const B& p, int64_t item, int& q, int& j, int& ll,
+                                            int& kv, int& gl) {
+    if (item <= 0xFFFFFFFFll) {
+        const UDiv dq((uint32_t)p.parts), dj((uint32_t)p.blocks_per_chunk), dl((uint32_t)p.layer_n);
+        const uint32_t i0 = (uint32_t)item;
+        const uint32_t i1 = dq.div(i0), i2 = dj.div(i1), i3 = dl.div(i2);
+        q = (int)(i0 - i1 * (uint32_t)p.parts);
+        j = (int)(i1 - i2 * (uint32_t)p.blocks_per_chunk);
+        ll = (int)(i2 - i3 * (uint32_t)p.layer_n);
+        kv = (int)(i3 & 1u);
+        gl = (int)(i3 >> 1);
+    } else {
+        q = (int)(item % p.parts);
+        int64_t t = item / p.parts;
+        j = (int)(t % p.blocks_per_chunk);
+        t /= p.blocks_per_chunk;
+        ll = (int)(t % p.layer_n);
+        t /= p.layer_n;
+        kv = (int)(t & 1);
+        gl = (int)(t >> 1);
+    }
+}
 
 template <class B>
 __device__ __forceinline__ bool item_run(const B& p, int64_t item, Run& run) {
-    const int q = (int)(item % p.parts);
-    int64_t t = item / p.parts;
-    const int j = (int)(t % p.blocks_per_chunk);
-    t /= p.blocks_per_chunk;
-    const int ll = (int)(t % p.layer_n);
-    t /= p.layer_n;
-    const int kv = (int)(t & 1);
-    const int gl = (int)(t >> 1);
+    int q, j, ll, kv, gl;
+    decode_item(p, item, q, j, ll, kv, gl);
+    run.kv = kv;
+    run.ll = ll;
+    run.gl = gl;
     const ChunkRef c = resolve_chunk(p, gl);
     const int part_rows = p.block_size / p.parts;
     const int row0 = j * p.block_size + q * part_rows;     // first row inside the chunk
@@ -293,17 +331,6 @@ __device__ __forceinline__ uint32_t absmax_bf16x8(uint32_t acc, const uint4& v) 
     return *reinterpret_cast<const uint32_t*>(&a);
 }
 
-// x / d for a runtime divisor that is usually a power of two.
-struct UDiv {
-    uint32_t d;
-    int32_t shift;      // log2(d) when d is a power of two, else -1
-    __device__ __forceinline__ explicit UDiv(uint32_t dv) : d(dv), shift(-1) {
-#ifdef __CUDA_ARCH__
-        if (__popc(dv) == 1) shift = __ffs(dv) - 1;
-#endif
-    }
-    __device__ __forceinline__ uint32_t div(uint32_t x) const { return shift >= 0 ? x >> shift : x / d; }
-};
 
 // Correctly rounded x / s for a per-tile constant s, from the correctly
 // rounded reciprocal r = RN(1/s): q0 = RN(x*r) is within an ulp of x/s, the
@@ -814,12 +841,8 @@ dequant_scatter_kernel(const __grid_constant__ B p, int64_t num_items) {
         // Decode the item against a bf16 pool, then derive the code run from it.
         Run run;
         if (!item_run(p, item, run)) continue;
-        int64_t t = item / p.parts / p.blocks_per_chunk;
-        const int ll = (int)(t % p.layer_n);
-        t /= p.layer_n;
-        const int kv = (int)(t & 1);
-        const int gl = (int)(t >> 1);
-        const int l = p.layer_lo + ll;
+        const int kv = run.kv, gl = run.gl;
+        const int l = p.layer_lo + run.ll;
         const float scale = p.scales[((int64_t)(p.chunk_base + gl) * 2 + kv) * p.num_layers + l];
         // chunk-side offset of the run in bf16 bytes -> the same rows in code bytes
         const uint8_t* cb = p.chunk_ptrs[p.chunk_base + gl];

@@ -107,11 +107,13 @@ STAGED = [
     W,                                                                    # 2 requests, partial chunk
     wl.Workload("many", 3, 1, 16, 4, 24000, tuple(range(0, 600, 2)), chunk_size=16),  # 300 requests
     W.with_(save_unfull=False),
+    # 64-token pages of 2 KiB rows: each page moves as four 32 KiB items
+    wl.Workload("bigpage", 3, 8, 128, 64, 48, (900, 300), chunk_size=256),
 ]
 
 
 @pytest.mark.parametrize("arena", [False, True], ids=["separate", "arena"])
-@pytest.mark.parametrize("w", STAGED, ids=["two", "many", "no_tail"])
+@pytest.mark.parametrize("w", STAGED, ids=["two", "many", "no_tail", "big_pages"])
 def test_staged_store_and_retrieve_vs_oracle(w, arena):
     require_gpu()
     pool = device_pool(w, 0)
@@ -183,7 +185,7 @@ def test_staged_layer_range():
 
 
 @pytest.mark.parametrize("arena", [False, True], ids=["separate", "arena"])
-@pytest.mark.parametrize("w", STAGED, ids=["two", "many", "no_tail"])
+@pytest.mark.parametrize("w", STAGED, ids=["two", "many", "no_tail", "big_pages"])
 def test_overlapped_store_and_retrieve_vs_oracle(w, arena):
     """The two-stream form (two staging halves, copies on their own stream)
     stores and retrieves exactly what the oracle's gather / scatter give, with
