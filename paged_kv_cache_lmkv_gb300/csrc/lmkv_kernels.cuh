@@ -186,26 +186,26 @@ __device__ __forceinline__ bool item_run(const B& p, int64_t item, Run& run) {
     const int rows = min(part_rows, c.ntok - row0);
     const int l = p.layer_lo + ll;
     const int64_t col = c.col0 + j;
-    const int64_t blk = p.block_table[(int64_t)c.req_row * p.bt_stride + col];
-    if (blk < 0 || blk >= p.num_blocks) { report(p, kStatusBadBlock); return false; }
-    uint8_t* lb = const_cast<uint8_t*>(p.layer_base[l]);
     const int64_t rb = p.row_bytes;
+    // The block id and both base pointers are read before any of them is
+    // checked, so the three loads are in flight together (every index is in
+    // range whatever the values turn out to be).
+    const int64_t blk = p.block_table[(int64_t)c.req_row * p.bt_stride + col];
+    uint8_t* lb = const_cast<uint8_t*>(p.layer_base[l]);
     // Chunk side: chunk g's buffer [2][L][n_g][row], or -- in staging mode --
     // the one-layer staging buffer, where chunk g's [2][n_g][row] slices sit
     // at 2 * row * (tokens enumerated before chunk g).
-    uint8_t* cb;
-    int64_t chunk_layers, layer_slot;
-    if (p.staging != nullptr) {
+    const bool staged = p.staging != nullptr;
+    uint8_t* cb = staged ? nullptr : p.chunk_ptrs[p.chunk_base + gl];
+    int64_t chunk_layers = p.num_layers, layer_slot = l;
+    if (staged) {
         const int64_t tok_before = p.stage_tok_base + p.req_tok_prefix[c.req] +
                                    (int64_t)(gl - p.req_chunk_begin[c.req]) * p.chunk_size;
         cb = p.staging + 2 * rb * tok_before;
         chunk_layers = 1;
         layer_slot = 0;
-    } else {
-        cb = p.chunk_ptrs[p.chunk_base + gl];
-        chunk_layers = p.num_layers;
-        layer_slot = l;
     }
+    if (blk < 0 || blk >= p.num_blocks) { report(p, kStatusBadBlock); return false; }
     if (lb == nullptr || cb == nullptr || ((reinterpret_cast<uintptr_t>(lb) |
                                             reinterpret_cast<uintptr_t>(cb)) & 15)) {
         report(p, kStatusBadPointer);
