@@ -832,7 +832,7 @@ __device__ __forceinline__ uint32_t dequant_pair(uint16_t two_codes, float scale
     return *reinterpret_cast<const uint32_t*>(&b);
 }
 
-template <class B, int kThreads>
+template <class B, int kThreads, int kUnroll>
 __global__ void __launch_bounds__(kThreads)
 dequant_scatter_kernel(const __grid_constant__ B p, int64_t num_items) {
     pdl_launch_dependents();
@@ -850,19 +850,33 @@ dequant_scatter_kernel(const __grid_constant__ B p, int64_t num_items) {
         const uint4* src = reinterpret_cast<const uint4*>(cb + code_off);
         uint4* dst = reinterpret_cast<uint4*>(run.pool);
         const int n16 = (int)(run.bytes >> 5);     // 16 codes per step
-        for (int v = threadIdx.x; v < n16; v += kThreads) {
-            const int4 ci = ld_stream(reinterpret_cast<const int4*>(src) + v);
-            const uint32_t cw[4] = {(uint32_t)ci.x, (uint32_t)ci.y, (uint32_t)ci.z, (uint32_t)ci.w};
-            uint32_t o[8];
+        // kUnroll code vectors per thread are loaded before their stores (the
+        // code and pool pointers may alias, so the compiler never moves a
+        // load above an earlier store by itself)
+        for (int base = threadIdx.x; base < n16; base += kThreads * kUnroll) {
+            int4 ci[kUnroll];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                o[2 * k] = dequant_pair((uint16_t)(cw[k] & 0xFFFFu), scale);
-                o[2 * k + 1] = dequant_pair((uint16_t)(cw[k] >> 16), scale);
+            for (int u = 0; u < kUnroll; ++u) {
+                const int v = base + u * kThreads;
+                if (v < n16) ci[u] = ld_stream(reinterpret_cast<const int4*>(src) + v);
             }
-            st_stream(reinterpret_cast<int4*>(dst + 2 * v),
-                      make_int4((int)o[0], (int)o[1], (int)o[2], (int)o[3]));
-            st_stream(reinterpret_cast<int4*>(dst + 2 * v + 1),
-                      make_int4((int)o[4], (int)o[5], (int)o[6], (int)o[7]));
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int v = base + u * kThreads;
+                if (v >= n16) continue;
+                const uint32_t cw[4] = {(uint32_t)ci[u].x, (uint32_t)ci[u].y, (uint32_t)ci[u].z,
+                                        (uint32_t)ci[u].w};
+                uint32_t o[8];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    o[2 * k] = dequant_pair((uint16_t)(cw[k] & 0xFFFFu), scale);
+                    o[2 * k + 1] = dequant_pair((uint16_t)(cw[k] >> 16), scale);
+                }
+                st_stream(reinterpret_cast<int4*>(dst + 2 * v),
+                          make_int4((int)o[0], (int)o[1], (int)o[2], (int)o[3]));
+                st_stream(reinterpret_cast<int4*>(dst + 2 * v + 1),
+                          make_int4((int)o[4], (int)o[5], (int)o[6], (int)o[7]));
+            }
         }
     }
 }
