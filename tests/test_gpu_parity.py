@@ -81,6 +81,7 @@ SHAPES = [
     (4, 1, 16, 4, 256, (255, 1, 700), (0, 0, 512), 128, 1, True),  # 16-byte rows
     (2, 8, 128, 32, 64, (900,), (0,), 256, 2, True),      # 64 KiB pages
     (2, 8, 128, 64, 32, (1100,), (256,), 256, 2, True),   # 128 KiB pages
+    (2, 8, 128, 64, 40, (1000,), (0,), 256, 4, True),     # 256 KiB pages (fp32 rows): 8 items each
     (1, 2, 64, 16, 64, (0, 256, 256), (0, 0, 256), 256, 2, True),  # empty requests
 ]
 
