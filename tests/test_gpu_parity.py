@@ -252,3 +252,52 @@ def test_llama70b_batch_sampled(flag):
     assert oracle.scatter(oracle.HostPool(hs, 16), tab, s, e, 256, True, ref) == 0
     for a, b in zip(hp.layers, hs):
         np.testing.assert_array_equal(a, b)
+
+
+@pytest.mark.parametrize("block_size", [32, 64])
+def test_qwen32b_bf16_full_size_sampled(block_size):
+    """Qwen2.5-32B shape (64 layers, one 16384-token request) on 32- and
+    64-token pages, the launches `bench.py --case qwen32b` times: pages of
+    64 / 128 KiB move as 32 KiB items.  Whole-batch gather against the oracle
+    on sampled chunks; per-layer gather equal to it; whole-batch and per-layer
+    scatter equal to each other and, on the sampled chunks, to the oracle."""
+    w = wl.qwen_with_block_size(block_size)
+    pool = device_pool(w, 0)
+    t1, t2 = wl.block_table(w, 1), wl.block_table(w, 2)
+    bt, bt2 = torch.from_numpy(t1).to(DEV), torch.from_numpy(t2).to(DEV)
+    chunks = pkg.enumerate_chunks(w.starts, w.ends, 256, True)
+    assert len(chunks) == 64
+    bufs, ptrs = alloc_chunks(chunks, w)
+    st = new_status()
+    pkg.check(pkg.gather_chunks(pool, bt, w.starts, w.ends, 256, True, ptrs, st))
+    torch.cuda.synchronize()
+    sample = [0, 33, 63]
+    ref = oracle_chunks_for(pool.layers, t1, chunks, sample, 256, w.num_layers, w.row_bytes)
+    for g, r in zip(sample, ref):
+        np.testing.assert_array_equal(host_bytes(bufs[g]), r, err_msg=f"chunk {g}")
+    lbufs, lptrs = alloc_chunks(chunks, w, fill=0)
+    for l in range(w.num_layers):
+        pkg.check(pkg.gather_layer(pool, bt, w.starts, w.ends, 256, True, lptrs, l, st))
+    torch.cuda.synchronize()
+    for a, b in zip(bufs, lbufs):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    del lbufs, lptrs, pool
+    torch.cuda.empty_cache()
+    pool2 = device_pool(w, None, fill="sentinel")
+    pkg.check(pkg.scatter_chunks(pool2, bt2, w.starts, w.ends, 256, True, ptrs, st))
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert nonsentinel_rows(pool2.layers) == 2 * w.num_layers * 16384
+    hp, tab, s, e, _ = compact_subbatch(pool2.layers, t2, chunks, sample)
+    hs = [np.full_like(a, wl.SENTINEL_BYTE) for a in hp.layers]
+    assert oracle.scatter(oracle.HostPool(hs, block_size), tab, s, e, 256, True, ref) == 0
+    for a, b in zip(hp.layers, hs):
+        np.testing.assert_array_equal(a, b)
+    del hp, hs
+    pool3 = device_pool(w, None, fill="sentinel")
+    for l in range(w.num_layers):
+        pkg.check(pkg.scatter_layer(pool3, bt2, w.starts, w.ends, 256, True, ptrs, l, st))
+    torch.cuda.synchronize()
+    for a, b in zip(pool2.layers, pool3.layers):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert st.item() == 0
