@@ -67,10 +67,12 @@ def parse_args():
                     help="skip the context gathers (torch index_select, one copy per page)")
     ap.add_argument("--codec-chunks", type=int, default=40,
                     help="--case codec: number of 256-token chunks")
-    ap.add_argument("--case", choices=["llama8b", "profile-small", "codec", "llama70b", "qwen32b"],
+    ap.add_argument("--case", choices=["llama8b", "profile-small", "profile-layer", "codec", "llama70b",
+                                       "qwen32b"],
                     default="llama8b",
                     help="profile-small: the 8B shape with a 1024-block pool and a 4096-token "
-                         "request (16 chunks), for ncu captures only")
+                         "request (16 chunks); profile-layer: the 8B batch (10240 tokens) in a "
+                         "pool of exactly its 640 pages; both for ncu captures only")
     return ap.parse_args()
 
 
@@ -1183,6 +1185,8 @@ def main():
     w = wl.LLAMA8B
     if args.case == "profile-small":
         w = w.with_(num_blocks=1024, req_tokens=(4096,))
+    if args.case == "profile-layer":
+        w = w.with_(num_blocks=640)
     if args.case == "llama70b":
         # the 70B batch (4096 / 9000 / 20000 / 32768 tokens, partial last chunks,
         # interleaved tables); the pool holds 4608 blocks per layer (the batch
