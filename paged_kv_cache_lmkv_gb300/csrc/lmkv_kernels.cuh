@@ -61,7 +61,7 @@ struct BatchT {
     int32_t num_req;                    // requests packed in this launch (all with >= 1 chunk)
     int32_t chunk_base;                 // global index of this launch's chunk 0
     int32_t num_chunks;                 // chunks in this launch
-    int32_t pad_;
+    int32_t prefetch_ahead;             // copy kernel: L2 prefetch distance in items (0 = none)
     uint8_t* staging;                   // DEVICE one-layer staging buffer, or null (see item_run)
     int64_t stage_tok_base;             // enumerated tokens of the call before this launch
     int64_t req_tok0[kCap];             // first enumerated token of packed request i
@@ -172,7 +172,7 @@ __device__ __forceinline__ void decode_item(const B& p, int64_t item, int& q, in
     }
 }
 
-template <class B>
+template <class B, bool kReport = true>
 __device__ __forceinline__ bool item_run(const B& p, int64_t item, Run& run) {
     int q, j, ll, kv, gl;
     decode_item(p, item, q, j, ll, kv, gl);
@@ -205,10 +205,13 @@ __device__ __forceinline__ bool item_run(const B& p, int64_t item, Run& run) {
         chunk_layers = 1;
         layer_slot = 0;
     }
-    if (blk < 0 || blk >= p.num_blocks) { report(p, kStatusBadBlock); return false; }
+    if (blk < 0 || blk >= p.num_blocks) {
+        if (kReport) report(p, kStatusBadBlock);
+        return false;
+    }
     if (lb == nullptr || cb == nullptr || ((reinterpret_cast<uintptr_t>(lb) |
                                             reinterpret_cast<uintptr_t>(cb)) & 15)) {
-        report(p, kStatusBadPointer);
+        if (kReport) report(p, kStatusBadPointer);
         return false;
     }
     run.pool = lb + ((kv * p.num_blocks + blk) * p.block_size + q * part_rows) * rb;
@@ -253,14 +256,31 @@ __device__ __forceinline__ void cta_copy(const uint8_t* __restrict__ src, uint8_
     }
 }
 
+// L2 prefetch of `bytes` (a multiple of 16) from a 16-byte aligned global
+// address, issued to the TMA unit (no registers wait for it).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(src), "r"(bytes) : "memory");
+}
+
 // LSU engine.  kGather: pool -> chunk, else chunk -> pool.  Grid-stride over
 // items, so the grid may be the item count (one CTA per item) or smaller.
+// With p.prefetch_ahead > 0 (one-layer calls), thread 0 first asks the TMA
+// unit to bring the source run of item + prefetch_ahead into L2, so the CTA
+// that later takes that item finds its rows there: a one-layer call is short
+// enough that the loads of its CTAs alone keep too few bytes in flight.  The
+// address comes from the same checked lookup as that item's own (after the
+// dependency wait); errors are left for the owning CTA to report.
 template <class B, bool kGather, int kThreads, int kUnroll>
 __global__ void __launch_bounds__(kThreads)
 move_lsu_kernel(const __grid_constant__ B p, int64_t num_items) {
     pdl_launch_dependents();
     pdl_wait();
     for (int64_t item = blockIdx.x; item < num_items; item += gridDim.x) {
+        if (p.prefetch_ahead > 0 && threadIdx.x == 0 && item + p.prefetch_ahead < num_items) {
+            Run ahead;
+            if (item_run<B, false>(p, item + p.prefetch_ahead, ahead))
+                bulk_prefetch_l2(kGather ? ahead.pool : ahead.chunk, ahead.bytes);
+        }
         Run run;
         if (!item_run(p, item, run)) continue;
         if (kGather) cta_copy<kThreads, kUnroll>(run.pool, run.chunk, run.bytes);
@@ -638,7 +658,8 @@ __device__ __forceinline__ uint32_t absmax_smem_slice(const uint8_t* slice, uint
 // the CTA's slice (as many whole rows as kThreads * kVPT 16-byte vectors hold)
 // are loaded into registers with ordinary loads while warp 0 looks up the page
 // runs of the remaining rows in parallel and issues one cp.async.bulk copy per
-// run into shared memory, completing one mbarrier; both halves are in flight
+// run of at most 32 KiB (a page, or a piece of a larger page) into shared
+// memory, completing one mbarrier; both halves are in flight
 // together.  The CTA takes the absmax over registers and shared memory, the
 // cluster exchanges CTA maxima through distributed shared memory (one split
 // cluster barrier; lane r reads CTA r's maximum), and every CTA quantises its
