@@ -266,17 +266,21 @@ int32_t choose_parts(const lmkv_pool_t* pool) {
     return parts;
 }
 
-// L2 prefetch distance of one-layer calls, in items: five eighths of the
-// copy kernel's CTAs resident at once (4 per SM x 152 SMs -> 380 on GB300).
-// Measured on the 8B per-layer calls (gather / scatter, us per call): no
-// prefetch 15.7 / 15.5; 228 items ahead 15.2 / 14.9; 304 and 380 15.1 / 14.8;
-// 456 15.2 / 14.8; 608 15.5 / 15.3; each CTA prefetching its own run 15.4 /
-// 15.2.  Whole-batch calls are already bound by HBM and prefetch nothing.
+// L2 prefetch distance, in items, of the copy kernel's one-layer calls: five
+// eighths of the kernel's CTAs resident at once (occupancy x SM count: 4 x
+// 152 -> 380 on GB300).  Measured on the 8B per-layer calls (gather /
+// scatter, us per call): no prefetch 15.7 / 15.5; 228 items ahead 15.2 /
+// 14.9; 304 and 380 15.1 / 14.8; 456 15.2 / 14.8; 608 15.5 / 15.3; each CTA
+// prefetching its own run 15.4 / 15.2.  Whole-batch copies are bound by HBM
+// and gain nothing (prefetching there measured -1% to +0.5%).  (The
+// dequantising scatter gained 2.4% with a fixed distance at 47 registers and
+// 5 CTAs per SM, but lost 2% once its registers fell to 40 and 6 CTAs per SM;
+// it does not prefetch.)
 // Cached per device after the first call made outside a stream capture (no
 // device query is made while `stream` is capturing: such a call, before the
 // value is known, prefetches nothing); 0 (no prefetch) if a query fails.
-int32_t lsu_prefetch_ahead(cudaStream_t stream) {
-    static std::atomic<int32_t> cache[64];
+template <class Kernel>
+int32_t prefetch_distance(Kernel kernel, int threads, std::atomic<int32_t>* cache, cudaStream_t stream) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
         (void)cudaGetLastError();
@@ -290,9 +294,7 @@ int32_t lsu_prefetch_ahead(cudaStream_t stream) {
         return 0;
     }
     int per_sm = 0, sms = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &per_sm, lmkv::move_lsu_kernel<lmkv::BatchSmall, true, kLsuThreads, kLsuUnroll>, kLsuThreads, 0) !=
-            cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
         (void)cudaGetLastError();
         return 0;
@@ -300,6 +302,12 @@ int32_t lsu_prefetch_ahead(cudaStream_t stream) {
     const int32_t ahead = (int32_t)((int64_t)per_sm * sms * 5 / 8);
     if (ahead > 0) cache[dev].store(ahead, std::memory_order_relaxed);
     return ahead > 0 ? ahead : 0;
+}
+
+int32_t lsu_prefetch_ahead(cudaStream_t stream) {
+    static std::atomic<int32_t> cache[64];
+    return prefetch_distance(lmkv::move_lsu_kernel<lmkv::BatchSmall, true, kLsuThreads, kLsuUnroll>,
+                             kLsuThreads, cache, stream);
 }
 
 int move_entry(bool gather, const lmkv_pool_t* pool, const int32_t* block_table,
@@ -611,6 +619,7 @@ int fp8_entry(bool gather, const lmkv_pool_t* pool, const int32_t* block_table, 
     if (rc != LMKV_OK || c.num_chunks == 0) return rc;
     if (scales == nullptr) return LMKV_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
     if (c.nonempty <= lmkv::kSmallBatch)
         return gather ? launch_quant<lmkv::BatchSmall>(c, scales, s)
                       : launch_dequant<lmkv::BatchSmall>(c, scales, s);
