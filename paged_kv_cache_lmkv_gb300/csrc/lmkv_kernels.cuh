@@ -652,6 +652,40 @@ __device__ __forceinline__ uint32_t absmax_smem_slice(const uint8_t* slice, uint
     return acc;
 }
 
+// Warp 0 of a quantiser CTA, once its own rows have arrived: ask the TMA unit
+// to bring into L2 the slice of the same-rank CTA of tile t2 (a CTA that
+// starts about half a wave of clusters later), so that DRAM keeps working
+// while this CTA reduces, waits for its cluster and quantises.  Same lookups
+// and checks as the slice's own staging; bad ids and pointers are skipped
+// (the owning CTA reports them).
+template <int kCluster, class B>
+__device__ __forceinline__ void prefetch_slice(const B& p, uint32_t t2, uint32_t rank, int lane) {
+    if (t2 >= gridDim.x / kCluster) return;
+    const uint32_t row_bytes = (uint32_t)p.row_bytes;
+    const uint32_t bs = (uint32_t)p.block_size;
+    const uint32_t P = bs / (uint32_t)p.parts;
+    const UDiv pdiv(P), qdiv((uint32_t)p.parts);
+    const uint32_t ll = t2 % (uint32_t)p.layer_n;
+    const uint32_t kv = (t2 / (uint32_t)p.layer_n) & 1u;
+    const int gl = (int)(t2 / (uint32_t)p.layer_n / 2u);
+    const ChunkRef c = resolve_chunk(p, gl);
+    const uint32_t rows_per = (uint32_t)(c.ntok + kCluster - 1) / kCluster;
+    const uint32_t r0 = rank * rows_per;
+    const uint32_t nrows = (uint32_t)max(0, min(c.ntok, (int)(r0 + rows_per)) - (int)r0);
+    const uint8_t* lb = p.layer_base[p.layer_lo + (int)ll];
+    if (nrows == 0 || lb == nullptr || (reinterpret_cast<uintptr_t>(lb) & 15)) return;
+    const uint8_t* kv_base = lb + (int64_t)kv * p.num_blocks * p.block_size * row_bytes;
+    const int32_t* bt = p.block_table + (int64_t)c.req_row * p.bt_stride + c.col0;
+    const uint32_t pi_end = pdiv.div(r0 + nrows - 1) + 1;
+    for (uint32_t pi = pdiv.div(r0) + lane; pi < pi_end; pi += 32) {
+        const uint32_t a = max(r0, pi * P), e = min(r0 + nrows, (pi + 1) * P);
+        const uint32_t jb = qdiv.div(pi);
+        const int32_t blk = bt[jb];
+        if ((uint32_t)blk < (uint32_t)p.num_blocks)
+            bulk_prefetch_l2(kv_base + ((int64_t)blk * bs + (a - jb * bs)) * row_bytes, (e - a) * row_bytes);
+    }
+}
+
 // Staged quantising gather (the default when the staged rows fit in shared
 // memory).  One thread-block cluster of kCluster CTAs per (chunk, K/V, layer)
 // tile; CTA r owns rows [r*n/kCluster, (r+1)*n/kCluster).  The first h rows of
@@ -792,6 +826,8 @@ quant_gather_hybrid_kernel(const __grid_constant__ B p) {
         (void)mbar_wait_bounded(&bar, 0);
     }
     if (threadIdx.x == 0 && any_bad) report(p, kStatusBadBlock);
+    if (p.prefetch_ahead > 0 && threadIdx.x < 32)
+        prefetch_slice<kCluster>(p, tile + (uint32_t)p.prefetch_ahead, rank, lane);
     const bool check_rows = any_bad != 0;
     {
         const uint32_t a2 = check_rows ? absmax_smem_slice<true, kThreads>(slice, nvec_s, sm.vdiv, row_ok)
