@@ -41,6 +41,14 @@
  * default stream).  Pointers marked DEVICE must be device memory of the
  * current device; HOST arrays are read before the call returns.
  *
+ * CUDA graphs.  Calls can be captured in a CUDA graph.  The first call of an
+ * entry point on a device sets kernel attributes (the shared-memory size of
+ * the fp8 quantiser and of the CacheGen kernels) and looks up the kernels'
+ * occupancy, which sizes the L2 prefetch distances; make that first call
+ * outside any stream capture (a warm-up call).  A call whose occupancy
+ * lookup has not happened yet makes none while its stream is capturing, and
+ * runs without the L2 prefetch.
+ *
  * Errors.  Every call returns an lmkv_status value.  Argument errors are
  * detected on the host before anything is launched (nothing is written).
  * Errors found by the kernels (a block id outside [0, num_blocks), a null or
