@@ -48,11 +48,12 @@ constexpr int kQuantCluster = 4;
 constexpr int kQuantClusterWide = 8;
 constexpr int kQuantHybridVPT = 4;        // register vectors per thread of the staged quantiser
 constexpr int kDequantThreads = 256;
-// Code vectors per thread loaded before their stores.  Measured on the 8B
-// batch: 1 -> 0.319 ms, 2 -> 0.316, 4 -> 0.357, 8 -> 0.361 (more reads in
-// flight per SM than two per thread slows this kernel down, as more CTAs per
-// SM slow the copy kernel).
-constexpr int kDequantUnroll = 2;
+// 8-byte code words per thread loaded before their stores (each word -> one
+// contiguous 16-byte store).  Measured on the 8B batch: 2 -> 0.329 ms, 4 ->
+// 0.314, 8 -> 0.308 (8 covers a whole 16-row item of 2 KiB rows in one pass).
+// The earlier form, 16-byte code vectors each stored as two 16-byte halves
+// 32 bytes apart, measured 1 -> 0.319, 2 -> 0.316, 4 -> 0.357, 8 -> 0.361.
+constexpr int kDequantUnroll = 8;
 
 // Chunks of one request (cache_engine.py walk-through, "store()").
 inline int64_t request_chunks(int64_t s, int64_t e, int32_t chunk_size, int32_t save_unfull) {

@@ -881,7 +881,13 @@ quant_gather_hybrid_kernel(const __grid_constant__ B p) {
 
 // ---------------------------------------------------------------------------
 // fp8 e4m3 dequantising scatter: per item (chunk, kv, layer, block part),
-// 16 codes (16 bytes) in, 16 bf16 (32 bytes) out per thread step.
+// 8 codes (8 bytes) in, 8 bf16 (16 bytes) out per thread step.
+__device__ __forceinline__ uint2 ld_stream8(const uint2* ptr) {
+    uint2 r;
+    asm("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(ptr));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t dequant_pair(uint16_t two_codes, float scale) {
     const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two_codes, __NV_E4M3);
     const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
@@ -904,35 +910,29 @@ dequant_scatter_kernel(const __grid_constant__ B p, int64_t num_items) {
         // chunk-side offset of the run in bf16 bytes -> the same rows in code bytes
         const uint8_t* cb = p.chunk_ptrs[p.chunk_base + gl];
         const int64_t code_off = (run.chunk - cb) >> 1;
-        const uint4* src = reinterpret_cast<const uint4*>(cb + code_off);
-        uint4* dst = reinterpret_cast<uint4*>(run.pool);
-        const int n16 = (int)(run.bytes >> 5);     // 16 codes per step
-        // kUnroll code vectors per thread are loaded before their stores (the
-        // code and pool pointers may alias, so the compiler never moves a
-        // load above an earlier store by itself)
-        for (int base = threadIdx.x; base < n16; base += kThreads * kUnroll) {
-            int4 ci[kUnroll];
+        // 8 codes (8 bytes) per thread step -> one 16-byte store, so that a
+        // warp's store instruction covers 512 contiguous bytes; kUnroll code
+        // words per thread are loaded before their stores (the code and pool
+        // pointers may alias, so the compiler never moves a load above an
+        // earlier store by itself)
+        const int n8 = (int)(run.bytes >> 4);
+        const uint2* src = reinterpret_cast<const uint2*>(cb + code_off);
+        int4* dst = reinterpret_cast<int4*>(run.pool);
+        for (int base = threadIdx.x; base < n8; base += kThreads * kUnroll) {
+            uint2 ci[kUnroll];
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 const int v = base + u * kThreads;
-                if (v < n16) ci[u] = ld_stream(reinterpret_cast<const int4*>(src) + v);
+                if (v < n8) ci[u] = ld_stream8(src + v);
             }
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 const int v = base + u * kThreads;
-                if (v >= n16) continue;
-                const uint32_t cw[4] = {(uint32_t)ci[u].x, (uint32_t)ci[u].y, (uint32_t)ci[u].z,
-                                        (uint32_t)ci[u].w};
-                uint32_t o[8];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    o[2 * k] = dequant_pair((uint16_t)(cw[k] & 0xFFFFu), scale);
-                    o[2 * k + 1] = dequant_pair((uint16_t)(cw[k] >> 16), scale);
-                }
-                st_stream(reinterpret_cast<int4*>(dst + 2 * v),
-                          make_int4((int)o[0], (int)o[1], (int)o[2], (int)o[3]));
-                st_stream(reinterpret_cast<int4*>(dst + 2 * v + 1),
-                          make_int4((int)o[4], (int)o[5], (int)o[6], (int)o[7]));
+                if (v >= n8) continue;
+                st_stream(dst + v, make_int4((int)dequant_pair((uint16_t)(ci[u].x & 0xFFFFu), scale),
+                                             (int)dequant_pair((uint16_t)(ci[u].x >> 16), scale),
+                                             (int)dequant_pair((uint16_t)(ci[u].y & 0xFFFFu), scale),
+                                             (int)dequant_pair((uint16_t)(ci[u].y >> 16), scale)));
             }
         }
     }
