@@ -46,8 +46,12 @@ UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 SPEC_HBM_GBS = 8000.0
 PROFILE = os.path.join(ROOT, "profiles", "gather_chunks_llama8b.md")
-KERNEL_SOURCES = [os.path.join(ROOT, "paged_kv_cache_lmkv_gb300", "csrc", f)
-                  for f in ("lmkv_kernels.cuh", "lmkv_api.cu")]
+# the copy kernel's device source: the committed DRAM counters of the gather
+# stand for the current kernel only while this file is unchanged
+KERNEL_SOURCES = [os.path.join(ROOT, "paged_kv_cache_lmkv_gb300", "csrc", "lmkv_kernels.cuh")]
+TRAFFIC_SOURCE = ("dram__bytes_read.sum + dram__bytes_write.sum of one 16-chunk gather (ncu, "
+                  "--case profile-small), scaled by 40/16 to the 40-chunk launch; from "
+                  "profiles/gather_chunks_llama8b.md, null unless taken on the current copy-kernel source")
 PHASES = ("gather", "scatter", "gather_layer", "scatter_layer", "fp8_gather", "fp8_scatter")
 
 
@@ -57,12 +61,16 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="--impl reference: host seconds the warm-up and timed steps should take")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-cachegen", action="store_true",
                     help="skip the CacheGen codec measurement")
     ap.add_argument("--no-pipeline", action="store_true",
                     help="skip the layer-wise pipeline measurement (host round trip per layer)")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="default case: skip the 70B batch and the Qwen2.5-32B page-size sweep")
     ap.add_argument("--no-context", action="store_true",
                     help="skip the context gathers (torch index_select, one copy per page)")
     ap.add_argument("--codec-chunks", type=int, default=40,
@@ -119,13 +127,13 @@ def kernel_source_hash() -> str:
 
 
 def profiled_traffic():
-    """Per-launch DRAM bytes of the gather from the committed ncu summary, if
-    it was taken on the current kernel sources."""
+    """Per-launch DRAM bytes of the 8B gather, scaled from the committed
+    small-case ncu capture, if it was taken on the current copy-kernel source."""
     try:
         text = open(PROFILE).read()
     except OSError:
         return None
-    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
+    m = re.search(r"traffic_bytes_per_launch_scaled:\s*(\d+)", text)
     s = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
     if not m or not s or s.group(1) != kernel_source_hash():
         return None
@@ -223,6 +231,13 @@ def setup(dev, w: wl.Workload) -> Ctx:
     c.ptrs = pkg.pointer_array(c.bufs, dev)
     c.lbufs = [torch.empty_like(b) for b in c.bufs]
     c.lptrs = pkg.pointer_array(c.lbufs, dev)
+    setup_common(c)
+    return c
+
+
+def setup_common(c: Ctx):
+    """fp8 buffers, status word, L2 flush buffer and the phases' byte counts."""
+    w, dev = c.w, c.dev
     c.codes = [torch.empty((2, w.num_layers, n, w.row_elems), dtype=torch.uint8, device=dev)
                for _, _, n in c.chunks]
     c.cptrs = pkg.pointer_array(c.codes, dev)
@@ -230,18 +245,38 @@ def setup(dev, w: wl.Workload) -> Ctx:
     c.status = torch.zeros(1, dtype=torch.int32, device=dev)
     c.flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     torch.cuda.synchronize(dev)         # inputs are written on the default stream
-    n_tok = sum(n for _, _, n in c.chunks)
-    payload = n_tok * 2 * w.num_layers * w.row_bytes          # bf16 bytes of all moved rows
-    tiles = len(c.chunks) * 2 * w.num_layers
-    c.payload = payload
-    c.phase_bytes = {
-        "gather": 2 * payload,
-        "scatter": 2 * payload,
-        "gather_layer": 2 * payload,
-        "scatter_layer": 2 * payload,
-        "fp8_gather": payload + payload // 2 + 4 * tiles,
-        "fp8_scatter": payload // 2 + 4 * tiles + payload,
-    }
+    c.phase_bytes = full_phase_bytes(w, c.chunks)
+    c.payload = c.phase_bytes["gather"] // 2
+
+
+def setup_llama70b(dev) -> Ctx:
+    """The 70B batch in its stated pool: 32768 blocks of 16 tokens per layer
+    (160 GiB), the 4117 blocks of the batch (interleaved tables, seed 1) hold
+    N(0,1) values and every other row a sentinel; the scatters write into 4117
+    other, unused blocks of the same pool (seed 2).  The per-layer calls reuse
+    the chunk buffers of the whole-batch calls."""
+    w = wl.LLAMA70B
+    c = Ctx()
+    c.w, c.dev = w, dev
+    c.table = wl.block_table(w, 1)
+    used = set(int(x) for x in c.table[c.table >= 0])
+    c.table2 = wl.block_table(w, 2, exclude=used)
+    layers = wl.make_pool(w, dev, None, fill="sentinel")
+    ids = torch.as_tensor(sorted(used), dtype=torch.long, device=dev)
+    vals = torch.empty((2, len(ids), w.block_size, w.row_elems), dtype=torch.bfloat16, device=dev)
+    for l, t in enumerate(layers):
+        wl.fill_normal_(vals, 1000 + l)
+        t.index_copy_(1, ids, vals)
+    del vals
+    c.pool = c.pool2 = pkg.Pool(layers, w.num_kv_heads, w.head_dim)
+    c.bt = torch.from_numpy(c.table).to(dev)
+    c.bt2 = torch.from_numpy(c.table2).to(dev)
+    c.chunks = pkg.enumerate_chunks(w.starts, w.ends, w.chunk_size, w.save_unfull)
+    c.bufs = [torch.empty((2, w.num_layers, n, w.row_elems), dtype=torch.bfloat16, device=dev)
+              for _, _, n in c.chunks]
+    c.ptrs = c.lptrs = pkg.pointer_array(c.bufs, dev)
+    c.lbufs = c.bufs
+    setup_common(c)
     return c
 
 
@@ -308,6 +343,38 @@ def bench_device(c: Ctx, args, stream, rank, world, gpu_index):
     return per_phase_ms, launches, clk, wall
 
 
+def host_numa(dev):
+    """Where the process runs relative to the GPU: the GPU's NUMA node (from
+    its PCI device), the NUMA nodes of the CPUs this process may run on, and
+    the host's node list.  Pinned host memory is placed on the node of the
+    thread that allocates it."""
+    out = {}
+    try:
+        bus = subprocess.run(["nvidia-smi", "--query-gpu=pci.bus_id", "--format=csv,noheader",
+                              "-i", smi_id(dev.index or 0)], capture_output=True, text=True,
+                             timeout=20).stdout.strip().lower()
+        bus = bus[4:] if bus.startswith("0000") and len(bus) > 12 else bus
+        with open(f"/sys/bus/pci/devices/{bus}/numa_node") as f:
+            out["gpu_node"] = int(f.read().strip())
+    except (OSError, ValueError, subprocess.SubprocessError):
+        out["gpu_node"] = None
+    nodes = set()
+    for cpu in sorted(os.sched_getaffinity(0)):
+        try:
+            for name in os.listdir(f"/sys/devices/system/cpu/cpu{cpu}"):
+                if name.startswith("node") and name[4:].isdigit():
+                    nodes.add(int(name[4:]))
+        except OSError:
+            pass
+    out["cpu_nodes"] = sorted(nodes)
+    out["cpus"] = len(os.sched_getaffinity(0))
+    try:
+        out["host_nodes"] = open("/sys/devices/system/node/online").read().strip()
+    except OSError:
+        out["host_nodes"] = None
+    return out
+
+
 def pinned_arena(bufs):
     """Pinned host copies of the chunk buffers' shapes as consecutive slices of
     one allocation (the staged pipeline moves a run of such full chunks with
@@ -368,18 +435,25 @@ def bench_e2e(c: Ctx, args, stream):
     for _ in range(3):
         one()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
+    # one event per step boundary: the job's time is first to last, and the
+    # steps' own times give the spread
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.e2e_steps + 1)]
+    evs[0].record(stream)
+    for k in range(args.e2e_steps):
         one()
-    e1.record(stream)
+        evs[k + 1].record(stream)
     torch.cuda.synchronize()
     assert int(host_status.item()) == 0
-    ms = e0.elapsed_time(e1) / args.e2e_steps
+    ms = evs[0].elapsed_time(evs[-1]) / args.e2e_steps
+    per_step = sorted(evs[k].elapsed_time(evs[k + 1]) for k in range(args.e2e_steps))
     bytes_step = c.phase_bytes["gather"] + c.phase_bytes["scatter"]
     return {"value": round(bytes_step / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "ms_per_step": round(ms, 4),
+            "ms_per_step_median_min_max": [round(statistics.median(per_step), 3), round(per_step[0], 3),
+                                           round(per_step[-1], 3)],
+            "link_GBps_payload_both_ways": round(2 * c.payload / (ms * 1e-3) / 1e9, 1),
+            "host_numa": host_numa(c.dev),
             "what": "store of the batch to pinned host memory concurrent with the retrieve of an "
                     "earlier stored batch, both through the overlapped layer-wise pipeline (kernel "
                     "<-> two device staging halves, copy engine <-> host on a copy stream), H2D "
@@ -601,6 +675,11 @@ def bench_cachegen(c: Ctx, clk_mhz, reps: int = 5):
     out = {"workload": "CacheGen on the 8B gather output: 40 chunks x 256 tokens x 32 layers x "
                        "1024 channels bf16 N(0,1), default bins (K 10x32 + 22x16, V 2x32 + 30x16)"}
     out.update({k: v for k, v in main.items() if not k.startswith("_")})
+    # coded symbols per second per SM: a figure that does not depend on how
+    # many instructions the coder spends per symbol
+    sms = torch.cuda.get_device_properties(c.dev).multi_processor_count
+    out["encode_Msymbols_per_s_per_SM"] = round(main["_symbols"] / (main["_te"] * 1e-3) / sms / 1e6, 2)
+    out["decode_Msymbols_per_s_per_SM"] = round(main["_symbols"] / (main["_td"] * 1e-3) / sms / 1e6, 2)
     if inst is not None and clk_mhz:
         peak = 152 * 4 * clk_mhz * 1e6                     # warp instructions per second
         roof = {}
@@ -836,6 +915,16 @@ def codec_source_hash() -> str:
 # ---------------------------------------------------------------------------
 # CPU oracle (baseline leg and --impl reference).
 
+def full_phase_bytes(w, chunks):
+    """Algorithmic bytes of every phase of one step over the given chunks."""
+    n_tok = sum(n for _, _, n in chunks)
+    payload = n_tok * 2 * w.num_layers * w.row_bytes          # bf16 bytes of all moved rows
+    tiles = len(chunks) * 2 * w.num_layers
+    return {"gather": 2 * payload, "scatter": 2 * payload, "gather_layer": 2 * payload,
+            "scatter_layer": 2 * payload, "fp8_gather": payload + payload // 2 + 4 * tiles,
+            "fp8_scatter": payload // 2 + 4 * tiles + payload}
+
+
 def host_sample(c: Ctx, ntok: int):
     """Host copy of the blocks behind the first `ntok` tokens of the batch,
     compacted (the oracle's input)."""
@@ -844,19 +933,30 @@ def host_sample(c: Ctx, ntok: int):
     ids = torch.as_tensor(c.table[0, :nb], dtype=torch.long, device=c.dev)
     host = [t.index_select(1, ids).cpu().view(torch.int16).numpy().view(np.uint16)
             for t in c.pool.layers]
-    return host, nb
+    return host
+
+
+def synthetic_host_sample(w, ntok: int, seed: int = 0):
+    """Compact host pool of the first `ntok` tokens' blocks, N(0,1) bf16 drawn
+    on the CPU from a seeded generator (the reference arm needs no GPU)."""
+    nb = -(-ntok // w.block_size)
+    g = wl.generator("cpu", seed)
+    return [torch.randn((2, nb, w.block_size, w.row_elems), generator=g).to(torch.bfloat16)
+            .view(torch.int16).numpy().view(np.uint16) for _ in range(w.num_layers)]
 
 
 class OracleSample:
     """The CPU oracle on the first `ntok` tokens of the batch (one request of
-    ntok tokens, chunked like the batch), every phase of the step."""
+    ntok tokens, chunked like the batch), every phase of the step.  `host`
+    holds those tokens' blocks, compacted; `full_bytes` are the full batch's
+    phase bytes, by which a sampled step's time is scaled."""
 
-    def __init__(self, c: Ctx, ntok: int):
+    def __init__(self, w, ntok: int, host, full_bytes):
         import oracle
         self.oracle = oracle
-        w = c.w
-        self.c, self.w, self.ntok = c, w, ntok
-        host, nb = host_sample(c, ntok)
+        self.w, self.ntok, self.full_bytes = w, ntok, full_bytes
+        self.total_tokens = int(sum(int(e) - int(s) for s, e in zip(w.starts, w.ends)))
+        nb = host[0].shape[1]
         self.tab = np.arange(nb, dtype=np.int32)[None, :]
         self.tab2 = np.random.default_rng(2).permutation(nb).astype(np.int32)[None, :]
         self.s, self.e = np.array([0]), np.array([ntok])
@@ -866,12 +966,7 @@ class OracleSample:
         self.X = [np.empty((2, w.num_layers, n, w.row_elems), np.uint16) for _, _, n in ch]
         self.Q = [np.empty((2, w.num_layers, n, w.row_elems), np.uint8) for _, _, n in ch]
         self.S = np.empty((len(ch), 2, w.num_layers), np.float32)
-        payload = ntok * 2 * w.num_layers * w.row_bytes
-        tiles = len(ch) * 2 * w.num_layers
-        self.bytes = {"gather": 2 * payload, "scatter": 2 * payload, "gather_layer": 2 * payload,
-                      "scatter_layer": 2 * payload,
-                      "fp8_gather": payload + payload // 2 + 4 * tiles,
-                      "fp8_scatter": payload // 2 + 4 * tiles + payload}
+        self.bytes = full_phase_bytes(w, ch)
 
     def run(self, name):
         o, w, C = self.oracle, self.w, self.w.chunk_size
@@ -892,26 +987,28 @@ class OracleSample:
             o.scatter_fp8(self.hp2, self.tab2, *a, self.Q, self.S)
 
     def step(self):
-        """One pass of every phase; returns the full-batch step throughput
-        (GB/s) it implies: full bytes / sum of (full bytes / sampled rate)."""
+        """One pass of every phase over the sample.  Returns (the full-batch
+        step throughput it implies in GB/s = full bytes / sum of (full bytes /
+        sampled rate), the extrapolated full-batch step time in s, the
+        sample's own time in s)."""
         secs = {}
         for name in PHASES:
             t0 = time.perf_counter()
             self.run(name)
             secs[name] = time.perf_counter() - t0
-        step_s = sum(self.c.phase_bytes[n] * secs[n] / self.bytes[n] for n in PHASES)
-        return sum(self.c.phase_bytes.values()) / step_s / 1e9, step_s, sum(secs.values())
+        step_s = sum(self.full_bytes[n] * secs[n] / self.bytes[n] for n in PHASES)
+        return sum(self.full_bytes.values()) / step_s / 1e9, step_s, sum(secs.values())
 
     def describe(self, seconds):
         return (f"oracle (plain C, single thread) on the first {self.ntok} of "
-                f"{sum(n for _, _, n in self.c.chunks)} tokens of the batch (host copies of "
+                f"{self.total_tokens} tokens of the batch (host copies of "
                 f"their blocks, all {self.w.num_layers} layers), every phase of the step run "
                 f"once per step, {seconds:.0f} s of CPU work in total; GB/s scaled by bytes "
                 f"to the full step")
 
 
 def cpu_baseline(c: Ctx, budget_s: float = 20.0):
-    smp = OracleSample(c, 1024)
+    smp = OracleSample(c.w, 1024, host_sample(c, 1024), c.phase_bytes)
     vals, t_all = [], 0.0
     while t_all < budget_s and len(vals) < 20:
         gbs, _, t = smp.step()
@@ -928,7 +1025,9 @@ def cpu_baseline_all_cores(c: Ctx, rounds: int = 3):
     ctypes, which releases the interpreter lock, so the threads run in
     parallel; the oracle itself is unchanged."""
     n = len(os.sched_getaffinity(0))
-    smps = [OracleSample(c, c.w.chunk_size) for _ in range(n)]
+    host = host_sample(c, c.w.chunk_size)
+    smps = [OracleSample(c.w, c.w.chunk_size, [a.copy() for a in host], c.phase_bytes)
+            for _ in range(n)]
     per = sum(smps[0].bytes.values())
 
     def work(s):
@@ -951,34 +1050,47 @@ def cpu_baseline_all_cores(c: Ctx, rounds: int = 3):
 
 
 def bench_reference(args):
+    """The reference arm: the CPU oracle as it stands, single-threaded, on a
+    bounded sample of the Llama-3.1-8B batch drawn on the host.  No GPU, no
+    CUDA library: only the oracle runs."""
     rank, world, local = dist_env()
     if rank != 0:
         return
-    dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
+    import oracle
     w = wl.LLAMA8B
-    c = setup(dev, w)
-    # size the per-step sample so that W + K steps take about two minutes
-    probe = OracleSample(c, 256)
+    full_chunks = oracle.enumerate_chunks(w.starts, w.ends, w.chunk_size, w.save_unfull)
+    full_bytes = full_phase_bytes(w, full_chunks)
+    # size the per-step sample so that W + K steps take about --ref-seconds
+    probe = OracleSample(w, 256, synthetic_host_sample(w, 256), full_bytes)
     _, _, t256 = probe.step()
-    per_step = 120.0 / max(1, args.warmup + args.steps)
+    per_step = args.ref_seconds / max(1, args.warmup + args.steps)
     ntok = int(max(16, min(2048, 256 * per_step / max(t256, 1e-6))) // 16 * 16)
-    smp = OracleSample(c, ntok)
+    smp = OracleSample(w, ntok, synthetic_host_sample(w, ntok), full_bytes)
     for _ in range(args.warmup):
         smp.step()
-    vals, steps_s, t_all = [], [], 0.0
+    vals, steps_full, steps_own, t_all = [], [], [], 0.0
     for _ in range(args.steps):
         gbs, step_s, t = smp.step()
         vals.append(gbs)
-        steps_s.append(step_s)
+        steps_full.append(step_s)
+        steps_own.append(t)
         t_all += t
     gbs = statistics.median(vals)
+    what = (f"llama3.1-8b KV batch: {w.num_layers} layers x {w.num_kv_heads} KV heads x head_dim "
+            f"{w.head_dim} bf16, {w.block_size}-token pages, {int(w.ends.sum())} tokens = "
+            f"{len(full_chunks)} chunks of {w.chunk_size}")
     out = {
         "metric": METRIC, "value": round(gbs, 3), "unit": UNIT, "impl": "reference",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(statistics.median(steps_s) * 1e3, 2),
+        "ms_per_step": round(statistics.median(steps_own) * 1e3, 2),
+        "ms_per_step_what": f"the sample's own time per step ({ntok} of {int(w.ends.sum())} tokens)",
+        "ms_per_step_full_batch_extrapolated": round(statistics.median(steps_full) * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1) bf16 KV, random block tables)",
-        "config": config_dict(w, c),
+        "data": "synthetic (seeded N(0,1) bf16 KV drawn on the host)",
+        "config": {"workload": what, "steps_include": list(PHASES),
+                   "per_layer_calls": w.num_layers,
+                   "bytes_per_step": int(sum(full_bytes.values())),
+                   "parallelism": "one host thread (the oracle as it stands)"},
         "cpu_baseline": {"value": round(gbs, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": smp.describe(t_all)},
         "e2e": {"value": round(gbs, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -988,14 +1100,9 @@ def bench_reference(args):
 
 
 def config_dict(w, c):
-    if w.name == "llama3.1-70b":
-        what = ("llama3.1-70b KV batch: 80 layers x 8 KV heads x head_dim 128 bf16, 16-token "
-                "pages (4608-block pool/layer), requests of 4096 / 9000 / 20000 / 32768 tokens "
-                f"= {len(c.chunks)} chunks (partial last chunks kept), interleaved block tables")
-    else:
-        what = (f"{w.name} KV batch: {w.num_layers} layers x {w.num_kv_heads} KV heads x head_dim "
-                f"{w.head_dim} bf16, {w.block_size}-token pages ({w.num_blocks}-block pool/layer), "
-                f"{int(w.ends.sum())} tokens = {len(c.chunks)} chunks of {w.chunk_size}")
+    what = (f"{w.name} KV batch: {w.num_layers} layers x {w.num_kv_heads} KV heads x head_dim "
+            f"{w.head_dim} bf16, {w.block_size}-token pages ({w.num_blocks}-block pool/layer), "
+            f"{int(w.ends.sum())} tokens = {len(c.chunks)} chunks of {w.chunk_size}")
     return {"workload": what,
             "steps_include": list(PHASES),
             "per_layer_calls": w.num_layers,
@@ -1115,69 +1222,90 @@ PAGES_CONTEXT = {
 }
 
 
-def bench_qwen_sweep(args, dev, stream, rank, world, local):
-    """--case qwen32b: the device phases on the Qwen2.5-32B KV shape (64 layers,
-    8 KV heads x 128, one 16384-token request = 64 chunks, 1% of channels x20)
-    at page sizes 16, 32 and 64 tokens (65536 token slots per layer).  Each
-    page size is set up, timed like the default case, and freed before the
-    next.  `value` = bytes of all three steps / their summed device time."""
-    peak, peak_src = load_peaks()
-    sweep, tot_bytes, tot_ms, launches, clocks = {}, 0, 0.0, 0, []
+def phase_summary(c: Ctx, per_phase, peak):
+    """Per phase: mean ms, GB/s and fraction of the measured copy peak (and
+    us per call for the per-layer phases); the step's totals."""
+    phase_ms = {n: statistics.mean(v) for n, v in per_phase.items()}
+    out = {}
+    for n in PHASES:
+        gbs = c.phase_bytes[n] / (phase_ms[n] * 1e-3) / 1e9
+        out[n] = {"ms": round(phase_ms[n], 4), "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)}
+    for n in ("gather_layer", "scatter_layer"):
+        out[n]["us_per_call"] = round(phase_ms[n] * 1e3 / c.w.num_layers, 2)
+    step_ms, step_bytes = sum(phase_ms.values()), sum(c.phase_bytes.values())
+    out["step"] = {"ms": round(step_ms, 4), "bytes": int(step_bytes),
+                   "GB/s": round(step_bytes / (step_ms * 1e-3) / 1e9, 1),
+                   "frac_of_peak": round(step_bytes / (step_ms * 1e-3) / 1e9 / peak, 4)}
+    return out, step_ms, step_bytes
+
+
+def bench_llama70b(args, dev, stream, rank, world, local, peak):
+    """The device phases on the Llama-3.1-70B batch in its stated 160 GiB pool
+    (requests of 4096 / 9000 / 20000 / 32768 tokens = 259 chunks with partial
+    last chunks, interleaved tables; scatters into unused blocks of the same
+    pool), timed like the 8B step."""
+    c = setup_llama70b(dev)
+    per_phase, launches, clk, _ = bench_device(c, args, stream, rank, world, local)
+    summary, step_ms, step_bytes = phase_summary(c, per_phase, peak)
+    out = {"workload": "llama3.1-70b KV batch: 80 layers x 8 KV heads x head_dim 128 bf16, 16-token "
+                       "pages in a 32768-block pool per layer (160 GiB), requests of 4096 / 9000 / 20000 "
+                       f"/ 32768 tokens = {len(c.chunks)} chunks (partial last chunks kept), interleaved "
+                       "block tables; scatters into 4117 unused blocks of the same pool",
+           **summary, "gpu_launches": int(launches), "clocks": clk}
+    del c
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    return out, step_ms, step_bytes, launches
+
+
+def bench_qwen(args, dev, stream, rank, world, local, peak):
+    """The device phases on the Qwen2.5-32B KV shape (64 layers, 8 KV heads x
+    128, one 16384-token request = 64 chunks, 1% of channels x20) at page
+    sizes 16, 32 and 64 tokens (65536 token slots per layer).  Each page size
+    is set up, timed like the 8B step, and freed before the next."""
+    sweep, tot_bytes, tot_ms, launches = {}, 0, 0.0, 0
     for bs in (16, 32, 64):
         w = wl.qwen_with_block_size(bs)
         c = setup(dev, w)
         per_phase, n_launch, clk, _ = bench_device(c, args, stream, rank, world, local)
-        phase_ms = {n: statistics.mean(v) for n, v in per_phase.items()}
-        entry = {}
-        for n in PHASES:
-            gbs = c.phase_bytes[n] / (phase_ms[n] * 1e-3) / 1e9
-            entry[n] = {"ms": round(phase_ms[n], 4), "GB/s": round(gbs, 1),
-                        "frac_of_peak": round(gbs / peak, 4)}
-        for n in ("gather_layer", "scatter_layer"):
-            entry[n]["us_per_call"] = round(phase_ms[n] * 1e3 / w.num_layers, 2)
-        step_ms, step_bytes = sum(phase_ms.values()), sum(c.phase_bytes.values())
-        entry["step"] = {"ms": round(step_ms, 4), "bytes": int(step_bytes),
-                         "GB/s": round(step_bytes / (step_ms * 1e-3) / 1e9, 1)}
-        sweep[f"block_size_{bs}"] = entry
+        summary, step_ms, step_bytes = phase_summary(c, per_phase, peak)
+        sweep[f"block_size_{bs}"] = {**summary, "clocks": clk}
         tot_bytes += step_bytes
         tot_ms += step_ms
         launches += n_launch
-        clocks.append(clk)
         del c
         torch.cuda.synchronize(dev)
         torch.cuda.empty_cache()
-    total_ms = max_over_ranks(tot_ms * args.steps, world)
-    value = job_value(tot_bytes, world, args.steps, total_ms)
-    g = sweep["block_size_16"]["gather"]
-    if rank == 0:
-        out = {
-            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_ms, 4),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 KV, 1% of channels x20 "
-                                     "per (K/V, layer), random block tables)",
-            "config": {"workload": "qwen2.5-32b KV batch: 64 layers x 8 KV heads x head_dim 128 "
-                                   "bf16 with outlier channels, one 16384-token request = 64 "
-                                   "chunks of 256, pages of 16 / 32 / 64 tokens (65536 token "
-                                   "slots per layer); one step = the six phases at each page size",
-                       "steps_include": list(PHASES), "per_layer_calls": 64,
-                       "bytes_per_step": int(tot_bytes),
-                       "l2": "flushed between phases (256 MiB fill, outside the timed events); "
-                             "every phase also reads > 1 GB, larger than L2",
-                       "parallelism": "replicas (one independent batch per GPU, no collective)"},
-            "frac_of_hbm_peak": round(value / world / peak, 4),
-            "roofline": {"bound": "hbm", "kernel": "lmkv gather_chunks (move_lsu_kernel<gather>), "
-                                                   "16-token pages",
-                         "achieved": g["GB/s"], "peak": peak, "unit": "GB/s",
-                         "frac": g["frac_of_peak"], "peak_source": f"{peak_src} hbm_gbs",
-                         "traffic": None},
-            "page_size_sweep": sweep,
-            "e2e": None,
-            "cpu_baseline": None,
-            "gpu_launches": int(launches),
-            "clocks": clocks,
-        }
-        print(json.dumps(out), flush=True)
+    out = {"workload": "qwen2.5-32b KV batch: 64 layers x 8 KV heads x head_dim 128 bf16 with outlier "
+                       "channels (1% x20 per K/V and layer), one 16384-token request = 64 chunks of "
+                       "256, pages of 16 / 32 / 64 tokens (65536 token slots per layer)",
+           "page_size_sweep": sweep,
+           "all_page_sizes": {"ms": round(tot_ms, 4), "bytes": int(tot_bytes),
+                              "GB/s": round(tot_bytes / (tot_ms * 1e-3) / 1e9, 1)},
+           "gpu_launches": int(launches)}
+    return out, tot_ms, tot_bytes, launches
+
+
+def emit_case_line(args, world, rank, name, res, step_ms, step_bytes, launches, peak, peak_src):
+    """--case llama70b / qwen32b: that workload's own JSON line."""
+    total_ms = max_over_ranks(step_ms * args.steps, world)
+    value = job_value(step_bytes, world, args.steps, total_ms)
+    if rank != 0:
+        return
+    g = (res["page_size_sweep"]["block_size_16"] if name == "qwen32b" else res)["gather"]
+    print(json.dumps({
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 KV, random block tables)",
+        "config": {"workload": res["workload"], "steps_include": list(PHASES),
+                   "l2": "flushed between phases (256 MiB fill, outside the timed events); every "
+                         "phase also reads > 1 GB, larger than L2",
+                   "parallelism": "replicas (one independent batch per GPU, no collective)"},
+        "roofline": {"bound": "hbm", "kernel": "lmkv gather_chunks (move_lsu_kernel<gather>)",
+                     "achieved": g["GB/s"], "peak": peak, "unit": "GB/s", "frac": g["frac_of_peak"],
+                     "peak_source": f"{peak_src} hbm_gbs", "traffic": None},
+        name: res, "e2e": None, "cpu_baseline": None, "gpu_launches": int(launches)}), flush=True)
 
 
 def main():
@@ -1195,25 +1323,21 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     pkg.lmkv.load()
+    peak, peak_src = load_peaks()
+    stream = torch.cuda.Stream(dev)
+    if args.case in ("llama70b", "qwen32b"):
+        fn = bench_llama70b if args.case == "llama70b" else bench_qwen
+        res, step_ms, step_bytes, launches = fn(args, dev, stream, rank, world, local, peak)
+        emit_case_line(args, world, rank, args.case, res, step_ms, step_bytes, launches, peak, peak_src)
+        if world > 1:
+            torch.distributed.barrier()
+            torch.distributed.destroy_process_group()
+        return
     w = wl.LLAMA8B
     if args.case == "profile-small":
         w = w.with_(num_blocks=1024, req_tokens=(4096,))
     if args.case == "profile-layer":
         w = w.with_(num_blocks=640)
-    if args.case == "llama70b":
-        # the 70B batch (4096 / 9000 / 20000 / 32768 tokens, partial last chunks,
-        # interleaved tables); the pool holds 4608 blocks per layer (the batch
-        # needs 4117), so that both pools and the chunk buffers fit beside
-        # each other; device phases only
-        w = wl.LLAMA70B.with_(num_blocks=4608)
-        args.no_pipeline = args.no_cachegen = args.no_cpu_baseline = True
-    stream = torch.cuda.Stream(dev)
-    if args.case == "qwen32b":
-        bench_qwen_sweep(args, dev, stream, rank, world, local)
-        if world > 1:
-            torch.distributed.barrier()
-            torch.distributed.destroy_process_group()
-        return
     c = setup(dev, w)
     try:
         per_phase, launches, clk, wall = bench_device(c, args, stream, rank, world, local)
@@ -1231,19 +1355,12 @@ def main():
     total_ms = max_over_ranks(step_ms * args.steps, world)
     step_bytes = sum(c.phase_bytes.values())
     value = job_value(step_bytes, world, args.steps, total_ms)
-    peak, peak_src = load_peaks()
     g_ms = phase_ms["gather"]
     achieved = c.phase_bytes["gather"] / (g_ms * 1e-3) / 1e9
-    breakdown = {}
-    for n in PHASES:
-        gbs = c.phase_bytes[n] / (phase_ms[n] * 1e-3) / 1e9
-        breakdown[n] = {"ms": round(phase_ms[n], 4), "GB/s": round(gbs, 1),
-                        "frac_of_peak": round(gbs / peak, 4)}
-    breakdown["gather_layer"]["us_per_call"] = round(phase_ms["gather_layer"] * 1e3 / w.num_layers, 2)
-    breakdown["scatter_layer"]["us_per_call"] = round(phase_ms["scatter_layer"] * 1e3 / w.num_layers, 2)
+    breakdown, _, _ = phase_summary(c, per_phase, peak)
     breakdown["per_layer_plain_copy"] = plain_copy_per_layer(c, stream)
     context = context_gathers(c, stream) if not args.no_context else None
-    e2e = bench_e2e(c, args, stream) if args.case != "llama70b" else None
+    e2e = bench_e2e(c, args, stream)
     pipeline = bench_layer_pipeline(c) if not args.no_pipeline else None
     decode = bench_decode_store(c) if not args.no_pipeline else None
     cachegen = bench_cachegen(c, clk.get("sm_mhz") if clk else None) if not args.no_cachegen else None
@@ -1251,21 +1368,32 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(c)
         cpu_all = cpu_baseline_all_cores(c)
+    config = config_dict(w, c)
+    gather_bytes = int(c.phase_bytes["gather"])
+    del c
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    other = {}
+    if args.case == "llama8b" and not args.no_other_workloads:
+        other["llama70b"] = bench_llama70b(args, dev, stream, rank, world, local, peak)[0]
+        other["qwen32b"] = bench_qwen(args, dev, stream, rank, world, local, peak)[0]
     if rank == 0:
         out = {
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 KV, random block tables)",
-            "config": config_dict(w, c),
+            "config": config,
             "frac_of_hbm_peak": round(value / world / peak, 4),
             "frac_of_hbm_spec_8tbs": round(value / world / SPEC_HBM_GBS, 4),
             "roofline": {"bound": "hbm", "kernel": "lmkv gather_chunks (move_lsu_kernel<gather>)",
                          "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} hbm_gbs",
                          "traffic": profiled_traffic() if args.case == "llama8b" else None,
-                         "algorithmic_bytes_per_launch": int(c.phase_bytes["gather"])},
+                         "traffic_source": TRAFFIC_SOURCE,
+                         "algorithmic_bytes_per_launch": gather_bytes},
             "breakdown": breakdown,
+            **other,
             "context_gathers": context,
             "pages_context": PAGES_CONTEXT,
             "e2e": e2e,

@@ -80,7 +80,10 @@ typedef enum lmkv_status {
     LMKV_ERR_UNSUPPORTED = 4,   /* host: e.g. the fp8 variant on a pool that is not bf16 */
     LMKV_ERR_BAD_BLOCK = 5,     /* device: a block id outside [0, num_blocks); token skipped */
     LMKV_ERR_BAD_POINTER = 6,   /* device: null or misaligned entry in a pointer array; skipped */
-    LMKV_ERR_TIMEOUT = 7,       /* device: a bounded wait on an asynchronous copy gave up */
+    LMKV_ERR_TIMEOUT = 7,       /* device: an asynchronous copy did not complete within 1 s (the
+                                   tile's codes are not written; the CTA waits up to 10 s more
+                                   for the copy before it exits).  The GPU is then not serving
+                                   memory requests: treat the context as unusable. */
     LMKV_ERR_SCRATCH_LIMIT = 8, /* host: the batch needs more than the library's built-in scratch */
     LMKV_ERR_BAD_DATA = 9       /* device: an encoded blob is inconsistent (stream skipped) */
 } lmkv_status;
@@ -346,11 +349,14 @@ int lmkv_retrieve_layers_overlapped(const lmkv_pool_t* pool, const int32_t* bloc
  *
  * The staging area is a fixed device array of LMKV_NOALLOC_STAGING_BYTES
  * (64 MiB) inside the library: every GPU that loads the library holds it until
- * the process exits.  The first call on a device looks up that array's device
- * address for the device that is current at the time (a one-time set-up per
- * device), so make that first call before any stream capture.  All other
- * arguments, the layout of the host chunks and the per-layer behaviour are
- * those of lmkv_store_layers_staged.  The call allocates and frees nothing.
+ * the process exits.  Every call looks up that array's device address on the
+ * device that is current at the time (cudaGetSymbolAddress; the first lookup
+ * on a device loads the library's device code there, a one-time set-up per
+ * device, so make that first call before any stream capture).  Because the
+ * address is not cached, calls made after a cudaDeviceReset use the array of
+ * the new context.  All other arguments, the layout of the host chunks and
+ * the per-layer behaviour are those of lmkv_store_layers_staged.  The call
+ * allocates and frees nothing.
  *
  * Every call on a device uses the same staging area, and it keeps whatever
  * the last call left there; nothing in it needs to start at zero (each layer's
@@ -384,6 +390,10 @@ int lmkv_store_layers_staged_noalloc(const lmkv_pool_t* pool, const int32_t* blo
  *               codes [2][L][n_g][HD] uint8, 16-byte aligned
  *   scales    : DEVICE float32 [num_chunks][2][L]
  * Rows with a bad block id are skipped (not part of amax, codes not written).
+ * Non-finite values follow the same formulas in IEEE arithmetic: a NaN takes
+ * no part in amax and its code is 0x7F (the canonical e4m3fn NaN); an
+ * infinity makes amax and the scale infinite, so the tile's finite values
+ * code as +-0 (0x00 / 0x80) and its infinities (inf / inf = NaN) as 0x7F.
  * UNSUPPORTED if elem_bytes != 2 or HD is not a multiple of 16. */
 int lmkv_gather_chunks_fp8e4m3(const lmkv_pool_t* pool, const int32_t* block_table,
                                int32_t max_blocks, const int64_t* start, const int64_t* end,
@@ -392,7 +402,9 @@ int lmkv_gather_chunks_fp8e4m3(const lmkv_pool_t* pool, const int32_t* block_tab
                                void* stream);
 
 /* Dequantising retrieve: P[...] = bf16_round_nearest_even(float(e4m3(code)) * scale),
- * one fp32 multiply per element, into the enumerated tokens' rows. */
+ * one fp32 multiply per element, into the enumerated tokens' rows.  A NaN
+ * result (a NaN code, or 0 * an infinite scale) is stored as a bf16 NaN; which
+ * NaN bit pattern is not specified. */
 int lmkv_scatter_chunks_fp8e4m3(const lmkv_pool_t* pool, const int32_t* block_table,
                                 int32_t max_blocks, const int64_t* start, const int64_t* end,
                                 int32_t num_req, int32_t chunk_size, int32_t save_unfull_chunk,

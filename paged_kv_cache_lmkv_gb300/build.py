@@ -11,7 +11,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "liblmkv.so")
 SOURCES = [os.path.join(CSRC, "lmkv_api.cu"), os.path.join(CSRC, "lmkv_cachegen.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, "lmkv_kernels.cuh"), os.path.join(CSRC, "lmkv_internal.h"),
+DEPS = SOURCES + [os.path.join(CSRC, "lmkv_kernels.cuh"), os.path.join(CSRC, "lmkv_fp8.cuh"),
+                  os.path.join(CSRC, "lmkv_internal.h"),
                   os.path.join(INCLUDE, "lmkv.h")]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 

@@ -8,7 +8,7 @@
 // and nothing is synchronised.
 #include "lmkv.h"
 #include "lmkv_internal.h"
-#include "lmkv_kernels.cuh"
+#include "lmkv_fp8.cuh"
 
 #include <atomic>
 #include <map>
@@ -676,23 +676,17 @@ static __device__ __align__(256) uint8_t g_noalloc_staging[LMKV_NOALLOC_STAGING_
 
 namespace {
 
-std::mutex g_noalloc_mutex;
-void* g_noalloc_address[64] = {};
-
 // Device address of g_noalloc_staging on the current device (null on error).
+// Looked up on every call rather than cached: after a device reset the
+// library's module is loaded again and the array may sit elsewhere.  The
+// first lookup on a device loads the module there (the set-up).
 void* noalloc_staging_address() {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (g_noalloc_address[dev] == nullptr) {
-        void* ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_noalloc_staging) != cudaSuccess) {
-            (void)cudaGetLastError();
-            return nullptr;
-        }
-        g_noalloc_address[dev] = ptr;
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_staging) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
     }
-    return g_noalloc_address[dev];
+    return ptr;
 }
 
 }  // namespace
@@ -986,13 +980,18 @@ int lmkv_store_layers_staged_noalloc(const lmkv_pool_t* pool, const int32_t* blo
     int64_t chunks = 0;
     if (check_requests(start, end, num_req, chunk_size, save_unfull_chunk, &chunks, nullptr) != LMKV_OK)
         return LMKV_ERR_INVALID_ARG;
-    int64_t tokens = 0;
-    for (int32_t r = 0; r < num_req; ++r)
-        if (request_chunks(start[r], end[r], chunk_size, save_unfull_chunk) > 0)
-            tokens += save_unfull_chunk ? end[r] - start[r]
-                                        : (end[r] - start[r]) / chunk_size * chunk_size;
+    // Tokens the staging area can hold (K and V rows of one layer); each
+    // request's count is checked against what is left before it is added, so
+    // no product or sum can overflow whatever the offsets are.
     const int64_t row = (int64_t)pool->num_kv_heads * pool->head_dim * pool->elem_bytes;
-    if (2 * row * tokens > (int64_t)LMKV_NOALLOC_STAGING_BYTES) return LMKV_ERR_SCRATCH_LIMIT;
+    const int64_t cap = (int64_t)LMKV_NOALLOC_STAGING_BYTES / (2 * row);
+    int64_t tokens = 0;
+    for (int32_t r = 0; r < num_req; ++r) {
+        if (request_chunks(start[r], end[r], chunk_size, save_unfull_chunk) == 0) continue;
+        const int64_t n = save_unfull_chunk ? end[r] - start[r] : (end[r] - start[r]) / chunk_size * chunk_size;
+        if (n > cap - tokens) return LMKV_ERR_SCRATCH_LIMIT;
+        tokens += n;
+    }
     void* staging = noalloc_staging_address();
     if (staging == nullptr) return LMKV_ERR_CUDA;
     return staged_entry(true, pool, block_table, max_blocks, start, end, num_req, chunk_size,

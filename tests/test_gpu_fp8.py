@@ -171,3 +171,97 @@ def test_quant_error_bound_full_8b_shape():
         bound = torch.maximum(x.abs() * 2.0 ** -4, s * 2.0 ** -10) * (1 + 2.0 ** -8) + \
             x.abs() * 2.0 ** -8
         assert bool(((y - x).abs() <= bound).all())
+
+
+def bf16_nan_mask(a: np.ndarray) -> np.ndarray:
+    return (a & 0x7FFF) > 0x7F80
+
+
+@pytest.mark.parametrize("shape", [
+    # L, H, D, B, nb, ends, C: the bench's launch shape (clusters of 4: 8 rows of each
+    # CTA's quarter in registers, 56 in shared memory), and the register-staged kernel
+    (4, 8, 128, 16, 64, (512,), 256),
+    (2, 8, 128, 16, 256, (2048 + 700,), 2048),
+], ids=["staged", "register"])
+def test_non_finite_values_vs_oracle(shape):
+    """NaN and infinity in register-held and shared-memory-held rows: codes and
+    scales bit for bit against the oracle (a NaN is left out of the absmax and
+    codes as 0x7F; an infinite scale codes finite values as signed zeros); the
+    dequantised pool against the oracle's, with NaN where the oracle has NaN."""
+    L, H, D, B, nb, ends, C = shape
+    w = wl.Workload("nf", L, H, D, B, nb, ends, chunk_size=C)
+    table, table2 = wl.block_table(w, 1), wl.block_table(w, 2)
+    layers = [t.view(torch.int16).numpy().view(np.uint16).copy() for t in wl.make_pool(w, "cpu", 0)]
+    rows_per_cta = C // 4 if C == 256 else C // 8
+
+    def put(l, kv, tok, col, bits):
+        layers[l][kv, table[0, tok // B], tok % B, col] = bits
+
+    put(0, 0, 3, 11, 0x7FC0)                          # NaN in a register-held row of CTA 0
+    put(0, 1, rows_per_cta + 40, 5, 0xFF81)           # -NaN in a staged row of CTA 1
+    put(1, 0, 2 * rows_per_cta + 1, 7, 0x7F80)        # +inf, register row
+    put(1, 1, 3 * rows_per_cta + 50, 9, 0xFF80)       # -inf, staged row
+    if L > 2:
+        put(2, 0, 70, 1, 0x7F80)                      # inf and NaN in one tile
+        put(2, 0, 200, 2, 0x7FFF)
+        zero = table[0, :C // B]
+        layers[3][1][zero] = 0                        # zeros and a single NaN: scale 0
+        put(3, 1, 100, 0, 0xFFC0)
+        put(3, 0, C + 10, 3, 0x7FC0)                  # a NaN in the second chunk
+    pool = pkg.Pool([torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(DEV) for a in layers],
+                    H, D)
+    chunks, codes, cptrs, scales, st = gpu_quant(pool, w, table, True)
+    assert st.item() == 0
+    rc = [np.full((2, L, n, w.row_elems), 0xEE, np.uint8) for _, _, n in chunks]
+    rs = np.full((len(chunks), 2, L), -1.0, np.float32)
+    assert oracle.gather_fp8(oracle.HostPool(layers, B), table, w.starts, w.ends, C, True, rc, rs) == 0
+    assert np.isinf(rs).any() and (rs == 0).any() == (L > 2)
+    np.testing.assert_array_equal(scales.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+    for g, (a, b) in enumerate(zip(codes, rc)):
+        np.testing.assert_array_equal(a.cpu().numpy(), b, err_msg=f"codes chunk {g}")
+    pool2 = device_pool(w, None, fill="sentinel")
+    st.zero_()
+    pkg.check(pkg.scatter_chunks_fp8e4m3(pool2, torch.from_numpy(table2).to(DEV), w.starts,
+                                         w.ends, C, True, cptrs, scales, st))
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    h2 = [np.full_like(a, wl.SENTINEL_BF16) for a in layers]
+    assert oracle.scatter_fp8(oracle.HostPool(h2, B), table2, w.starts, w.ends, C, True, rc, rs) == 0
+    for l, (t, h) in enumerate(zip(pool2.layers, h2)):
+        got = host_u16(t)
+        nan = bf16_nan_mask(h)
+        np.testing.assert_array_equal(bf16_nan_mask(got), nan, err_msg=f"NaN positions, layer {l}")
+        np.testing.assert_array_equal(got[~nan], h[~nan], err_msg=f"dequant layer {l}")
+
+
+def test_llama8b_fp8_bench_launch_sampled():
+    """The fp8 pair exactly as `bench.py` times it (Llama-3.1-8B batch, N(0,1)
+    values without outliers, tables of seeds 1 and 2): codes and scales of
+    sampled chunks bit for bit against the oracle, and the dequantised pages
+    of those chunks against the oracle's scatter."""
+    w = wl.LLAMA8B
+    table, table2 = wl.block_table(w, 1), wl.block_table(w, 2)
+    pool = device_pool(w, 0)
+    chunks, codes, cptrs, scales, st = gpu_quant(pool, w, table, True)
+    assert st.item() == 0 and len(chunks) == 40
+    sample = [0, 21, 39]
+    hp, tab, s, e, _ = compact_subbatch(pool.layers, table, chunks, sample)
+    hp16 = oracle.HostPool([a.view(np.uint16) for a in hp.layers], 16)
+    rc = [np.zeros((2, 32, 256, 1024), np.uint8) for _ in sample]
+    rs = np.zeros((len(sample), 2, 32), np.float32)
+    assert oracle.gather_fp8(hp16, tab, s, e, 256, True, rc, rs) == 0
+    for i, g in enumerate(sample):
+        np.testing.assert_array_equal(scales[g].cpu().numpy().view(np.uint32), rs[i].view(np.uint32))
+        np.testing.assert_array_equal(codes[g].cpu().numpy(), rc[i], err_msg=f"chunk {g}")
+    del pool
+    torch.cuda.empty_cache()
+    pool2 = device_pool(w, None, fill="sentinel")
+    pkg.check(pkg.scatter_chunks_fp8e4m3(pool2, torch.from_numpy(table2).to(DEV), w.starts,
+                                         w.ends, 256, True, cptrs, scales, st))
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    hq, tab2, s2, e2, _ = compact_subbatch(pool2.layers, table2, chunks, sample)
+    h2 = [np.full(a.shape[:3] + (a.shape[3] // 2,), wl.SENTINEL_BF16, np.uint16) for a in hq.layers]
+    assert oracle.scatter_fp8(oracle.HostPool(h2, 16), tab2, s2, e2, 256, True, rc, rs) == 0
+    for a, b in zip(hq.layers, h2):
+        np.testing.assert_array_equal(a.view(np.uint16), b)

@@ -254,10 +254,10 @@ def test_llama70b_batch_sampled(flag):
         np.testing.assert_array_equal(a, b)
 
 
-@pytest.mark.parametrize("block_size", [32, 64])
+@pytest.mark.parametrize("block_size", [16, 32, 64])
 def test_qwen32b_bf16_full_size_sampled(block_size):
-    """Qwen2.5-32B shape (64 layers, one 16384-token request) on 32- and
-    64-token pages, the launches `bench.py --case qwen32b` times: pages of
+    """Qwen2.5-32B shape (64 layers, one 16384-token request) on 16-, 32- and
+    64-token pages, the launches the bench times for this shape: pages of
     64 / 128 KiB move as 32 KiB items.  Whole-batch gather against the oracle
     on sampled chunks; per-layer gather equal to it; whole-batch and per-layer
     scatter equal to each other and, on the sampled chunks, to the oracle."""
@@ -301,3 +301,79 @@ def test_qwen32b_bf16_full_size_sampled(block_size):
     for a, b in zip(pool2.layers, pool3.layers):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
     assert st.item() == 0
+
+
+def test_llama70b_per_layer_and_fp8_sampled():
+    """The 70B batch as the bench times it (160 GiB pool, interleaved tables,
+    partial last chunks): the 80 per-layer gathers equal the whole-batch gather
+    and, on sampled chunks, the oracle; the per-layer scatters into disjoint
+    unused blocks of the same pool and the fp8 pair (dequantised into a third
+    disjoint set of blocks) match the oracle on the sampled chunks."""
+    w = wl.LLAMA70B
+    L = w.num_layers
+    t1 = wl.block_table(w, 1)
+    used = set(int(x) for x in t1[t1 >= 0])
+    t2 = wl.block_table(w, 2, exclude=used)
+    used2 = used | set(int(x) for x in t2[t2 >= 0])
+    t3 = wl.block_table(w, 3, exclude=used2)
+    layers = wl.make_pool(w, DEV, None, fill="sentinel")
+    ids = torch.as_tensor(sorted(used), dtype=torch.long, device=DEV)
+    for l, t in enumerate(layers):
+        vals = torch.empty((2, len(ids), w.block_size, w.row_elems), dtype=torch.bfloat16, device=DEV)
+        wl.fill_normal_(vals, 1000 + l)
+        t.index_copy_(1, ids, vals)
+    del vals
+    pool = pkg.Pool(layers, w.num_kv_heads, w.head_dim)
+    bt, bt2, bt3 = (torch.from_numpy(t).to(DEV) for t in (t1, t2, t3))
+    a = (w.starts, w.ends, 256, True)
+    chunks = pkg.enumerate_chunks(*a)
+    assert len(chunks) == 259
+    bufs, ptrs = alloc_chunks(chunks, w)
+    lbufs, lptrs = alloc_chunks(chunks, w, fill=0)
+    st = new_status()
+    pkg.check(pkg.gather_chunks(pool, bt, *a, ptrs, st))
+    for l in range(L):
+        pkg.check(pkg.gather_layer(pool, bt, *a, lptrs, l, st))
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    for g, (x, y) in enumerate(zip(bufs, lbufs)):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16)), f"per-layer gather, chunk {g}"
+    last = np.cumsum([len(pkg.enumerate_chunks([0], [e], 256, True)) for e in w.ends]) - 1
+    sample = sorted(set([0, 16, int(last[1]), int(last[2]), int(last[3]), 130]))
+    ref = oracle_chunks_for(pool.layers, t1, chunks, sample, 256, L, w.row_bytes)
+    for g, r in zip(sample, ref):
+        np.testing.assert_array_equal(host_bytes(lbufs[g]), r, err_msg=f"chunk {g}")
+    del lbufs, lptrs
+    torch.cuda.empty_cache()
+    # per-layer scatter into the second set of blocks
+    for l in range(L):
+        pkg.check(pkg.scatter_layer(pool, bt2, *a, ptrs, l, st))
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    hp, tab, s, e, _ = compact_subbatch(pool.layers, t2, chunks, sample)
+    hs = [np.full_like(x, wl.SENTINEL_BYTE) for x in hp.layers]
+    assert oracle.scatter(oracle.HostPool(hs, 16), tab, s, e, 256, True, ref) == 0
+    for x, y in zip(hp.layers, hs):
+        np.testing.assert_array_equal(x, y)
+    del bufs, ptrs, hp, hs
+    torch.cuda.empty_cache()
+    # fp8 pair: quantise from the first set, dequantise into the third
+    codes, cptrs = alloc_chunks(chunks, w, dtype=torch.uint8, fill=0xEE)
+    scales = torch.full((len(chunks), 2, L), -1.0, dtype=torch.float32, device=DEV)
+    pkg.check(pkg.gather_chunks_fp8e4m3(pool, bt, *a, cptrs, scales, st))
+    pkg.check(pkg.scatter_chunks_fp8e4m3(pool, bt3, *a, cptrs, scales, st))
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    hp, tab, s, e, _ = compact_subbatch(pool.layers, t1, chunks, sample)
+    hp16 = oracle.HostPool([x.view(np.uint16) for x in hp.layers], 16)
+    rc = [np.zeros((2, L, chunks[g][2], w.row_elems), np.uint8) for g in sample]
+    rs = np.zeros((len(sample), 2, L), np.float32)
+    assert oracle.gather_fp8(hp16, tab, s, e, 256, True, rc, rs) == 0
+    for i, g in enumerate(sample):
+        np.testing.assert_array_equal(scales[g].cpu().numpy().view(np.uint32), rs[i].view(np.uint32))
+        np.testing.assert_array_equal(codes[g].cpu().numpy(), rc[i], err_msg=f"codes chunk {g}")
+    hq, tab3, s3, e3, _ = compact_subbatch(pool.layers, t3, chunks, sample)
+    h3 = [np.full(x.shape[:3] + (x.shape[3] // 2,), wl.SENTINEL_BF16, np.uint16) for x in hq.layers]
+    assert oracle.scatter_fp8(oracle.HostPool(h3, 16), tab3, s3, e3, 256, True, rc, rs) == 0
+    for x, y in zip(hq.layers, h3):
+        np.testing.assert_array_equal(x.view(np.uint16), y)

@@ -227,3 +227,58 @@ def test_zero_tile():
     p2 = [np.full((2, 8, 4, 16), 0x1234, np.uint16)]
     oracle.scatter_fp8(oracle.HostPool(p2, 4), table, [0], [8], 8, True, codes, scales)
     assert (p2[0][:, :2] == 0).all()
+
+
+def test_non_finite_values():
+    """Tiles holding NaN or infinity, against the formulas evaluated with
+    numpy's IEEE float32 arithmetic: a NaN takes no part in the absmax
+    (numpy's nanmax) and codes as the canonical e4m3fn NaN 0x7F; an infinity
+    makes the scale infinite, so finite values code as signed zeros (x / inf)
+    and the infinities as NaN (inf / inf); a tile whose only non-zero value is
+    a NaN has scale 0 and all codes 0."""
+    w = wl.Workload("nf", 4, 1, 32, 16, 32, (64,), chunk_size=64)
+    layers = bf16_pool(w, 7)
+    table = wl.block_table(w, seed=1)
+
+    def put(l, kv, tok, col, bits):
+        layers[l][kv, table[0, tok // 16], tok % 16, col] = bits
+
+    put(0, 0, 5, 3, 0x7FC0)            # +NaN
+    put(0, 0, 40, 9, 0xFF81)           # -NaN with a payload
+    put(1, 1, 17, 0, 0x7F80)           # +inf
+    put(1, 1, 18, 1, 0xFF80)           # -inf
+    put(2, 0, 3, 4, 0x7F80)            # inf and NaN in one tile
+    put(2, 0, 60, 5, 0x7FC1)
+    layers[3][1][table[0, :4]] = 0     # layer 3 V: zeros and one NaN
+    put(3, 1, 30, 2, 0xFFC0)
+    codes = [np.zeros((2, 4, 64, 32), np.uint8)]
+    scales = np.zeros((1, 2, 4), np.float32)
+    assert oracle.gather_fp8(oracle.HostPool(layers, 16), table, [0], [64], 64, True, codes, scales) == 0
+    for l in range(4):
+        for kv in range(2):
+            rows = np.stack([layers[l][kv, table[0, t // 16], t % 16] for t in range(64)])
+            x = (rows.astype(np.uint32) << 16).view(np.float32)
+            nan = np.isnan(x)
+            s = np.float32(np.nanmax(np.abs(x))) / np.float32(448.0)
+            assert scales[0, kv, l].tobytes() == np.float32(s).tobytes(), (l, kv)
+            c = codes[0][kv, l]
+            if s == 0:
+                assert (c == 0).all()
+                continue
+            with np.errstate(invalid="ignore", divide="ignore"):
+                y = x / s
+            ok = ~np.isnan(y)
+            ref = torch.from_numpy(y[ok]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            np.testing.assert_array_equal(c[ok], ref)
+            assert (c[~ok] == 0x7F).all()
+            assert (c[nan] == 0x7F).all()
+            if np.isinf(s):
+                assert set(np.unique(c[ok]).tolist()) <= {0x00, 0x80}
+                np.testing.assert_array_equal(c[ok] == 0x80, np.signbit(x[ok]))
+    # the round trip: NaN codes and 0 * inf give NaN, the rest is the plain formula
+    p2 = [np.zeros_like(a) for a in layers]
+    assert oracle.scatter_fp8(oracle.HostPool(p2, 16), table, [0], [64], 64, True, codes, scales) == 0
+    y = (p2[2][0, table[0, 0]].astype(np.uint32) << 16).view(np.float32)
+    assert np.isnan(y).all()                       # every value of the inf tile: 0 * inf or NaN
+    y = (p2[0][0, table[0, 0], 5, 3].astype(np.uint32) << 16).view(np.float32)
+    assert np.isnan(y)

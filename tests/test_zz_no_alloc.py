@@ -5,15 +5,17 @@ cache -- for example a runtime whose device memory is all owned by its own
 pool, a process held to a strict memory budget, or a callback path where
 cudaMalloc is not allowed.  For them the library offers one entry point that
 uses its own built-in staging area instead of a caller buffer.  These tests
-call it through the C ABI and compare what it writes with what the ordinary
-staged store (caller-provided staging buffer) writes, on two calls in a row
-with different batches; they also check the size limit.  This file is
-collected last so that a failure here does not stop the other tests.
+call it through the C ABI and compare what it writes with the CPU oracle's
+gather of the same batch and with what the ordinary staged store
+(caller-provided staging buffer) writes, on two calls in a row with different
+batches; they also check the size limit.  This file is collected last so that
+a failure here does not stop the other tests.
 """
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import paged_kv_cache_lmkv_gb300 as pkg
 from paged_kv_cache_lmkv_gb300 import workloads as wl
 
@@ -34,9 +36,11 @@ def host_arena(chunks, w):
 
 
 def store_both_ways(w, seed):
-    """(no-alloc result, caller-buffer result) as lists of host tensors."""
+    """(no-alloc result, caller-buffer result, oracle result) as lists of host
+    arrays of the chunks' bytes."""
     pool = pkg.Pool(wl.make_pool(w, DEV, seed), w.num_kv_heads, w.head_dim)
-    bt = torch.from_numpy(wl.block_table(w, seed + 1)).to(DEV)
+    table = wl.block_table(w, seed + 1)
+    bt = torch.from_numpy(table).to(DEV)
     a = (w.starts, w.ends, w.chunk_size, w.save_unfull)
     chunks = pkg.enumerate_chunks(*a)
     mine, ref = host_arena(chunks, w), host_arena(chunks, w)
@@ -49,7 +53,11 @@ def store_both_ways(w, seed):
                                       status=status))
     torch.cuda.synchronize()
     assert status.item() == 0
-    return mine, ref
+    host = [t.cpu().view(torch.uint8).numpy().reshape(t.shape[:3] + (w.row_bytes,)) for t in pool.layers]
+    want = [np.zeros((2, w.num_layers, n, w.row_bytes), np.uint8) for _, _, n in chunks]
+    assert oracle.gather(oracle.HostPool(host, w.block_size), table, *a, want) == 0
+    as_bytes = lambda ts: [t.view(torch.uint8).numpy().reshape(o.shape) for t, o in zip(ts, want)]
+    return as_bytes(mine), as_bytes(ref), want
 
 
 def test_two_calls_match_the_caller_buffer_form():
@@ -58,10 +66,11 @@ def test_two_calls_match_the_caller_buffer_form():
     first = wl.Workload("a", 6, 2, 64, 16, 160, (700, 300), chunk_size=256)
     second = wl.Workload("b", 4, 8, 128, 16, 1024, (10240,), chunk_size=256)   # 42 MB per layer
     for w, seed in ((first, 10), (second, 20)):
-        mine, ref = store_both_ways(w, seed)
-        for g, (x, y) in enumerate(zip(mine, ref)):
-            assert torch.equal(x.view(torch.int16), y.view(torch.int16)), f"{w.name} chunk {g}"
-            assert (x.view(torch.int16) != 0).any()
+        mine, ref, want = store_both_ways(w, seed)
+        for g, (x, y, z) in enumerate(zip(mine, ref, want)):
+            np.testing.assert_array_equal(x, z, err_msg=f"{w.name} chunk {g} against the oracle")
+            np.testing.assert_array_equal(x, y, err_msg=f"{w.name} chunk {g} against the staged store")
+            assert (x != 0).any()
 
 
 def test_batch_beyond_the_staging_area_is_rejected():
