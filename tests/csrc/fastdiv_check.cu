@@ -4,7 +4,7 @@
 // every finite bf16 x with |x| <= A, the e4m3 code that the kernel's 8-wide
 // quantiser produces with the reciprocal + correction division must equal
 // the code it produces with IEEE division.
-#include "lmkv_kernels.cuh"
+#include "lmkv_fp8.cuh"
 
 __global__ void fastdiv_exhaustive(unsigned long long* out) {
     const uint32_t a_bits = blockIdx.y + 1;                        // 0x0001 .. 0x7F7F

@@ -50,6 +50,7 @@ SMALL = [
     (2, 8, 128, 32, 64, (900,), (0,), 256, True),
     (2, 8, 128, 64, 32, (1100,), (256,), 256, True),
     (1, 1, 32, 8, 600, (2000,), (0,), 1024, True),     # chunk larger than the cluster's registers
+    (2, 8, 128, 16, 96, (1100,), (0,), 512, True),     # 128 rows per quarter: one tile per cluster of 8
     (1, 8, 128, 16, 256, (2048 + 700,), (0,), 2048, True),  # slice beyond shared memory: register path
 ]
 
@@ -178,21 +179,24 @@ def bf16_nan_mask(a: np.ndarray) -> np.ndarray:
 
 
 @pytest.mark.parametrize("shape", [
-    # L, H, D, B, nb, ends, C: the bench's launch shape (clusters of 4: 8 rows of each
-    # CTA's quarter in registers, 56 in shared memory), and the register-staged kernel
-    (4, 8, 128, 16, 64, (512,), 256),
-    (2, 8, 128, 16, 256, (2048 + 700,), 2048),
-], ids=["staged", "register"])
+    # L, H, D, B, nb, ends, C, rows per CTA.  The bench's launch shape (persistent
+    # clusters of 4: rows 0-31 of each CTA's 64 in registers, 32-63 in shared
+    # memory); 512-token chunks (one tile per cluster of 8: rows 0-7 of 64 in
+    # registers, 8-63 staged by bulk copies); 2048-token chunks (register-staged
+    # kernel, 256 rows per CTA, re-reading what does not fit)
+    (4, 8, 128, 16, 64, (512,), 256, 64),
+    (4, 8, 128, 16, 96, (1024,), 512, 64),
+    (2, 8, 128, 16, 256, (2048 + 700,), 2048, 256),
+], ids=["persistent", "staged", "register"])
 def test_non_finite_values_vs_oracle(shape):
     """NaN and infinity in register-held and shared-memory-held rows: codes and
     scales bit for bit against the oracle (a NaN is left out of the absmax and
     codes as 0x7F; an infinite scale codes finite values as signed zeros); the
     dequantised pool against the oracle's, with NaN where the oracle has NaN."""
-    L, H, D, B, nb, ends, C = shape
+    L, H, D, B, nb, ends, C, rows_per_cta = shape
     w = wl.Workload("nf", L, H, D, B, nb, ends, chunk_size=C)
     table, table2 = wl.block_table(w, 1), wl.block_table(w, 2)
     layers = [t.view(torch.int16).numpy().view(np.uint16).copy() for t in wl.make_pool(w, "cpu", 0)]
-    rows_per_cta = C // 4 if C == 256 else C // 8
 
     def put(l, kv, tok, col, bits):
         layers[l][kv, table[0, tok // B], tok % B, col] = bits
