@@ -69,6 +69,7 @@ def parse_args():
                     help="skip the CacheGen codec measurement")
     ap.add_argument("--no-pipeline", action="store_true",
                     help="skip the layer-wise pipeline measurement (host round trip per layer)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end host round trip")
     ap.add_argument("--no-other-workloads", action="store_true",
                     help="default case: skip the 70B batch and the Qwen2.5-32B page-size sweep")
     ap.add_argument("--no-context", action="store_true",
@@ -438,14 +439,18 @@ def bench_e2e(c: Ctx, args, stream):
     # one event per step boundary: the job's time is first to last, and the
     # steps' own times give the spread
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.e2e_steps + 1)]
+    host_ms = []
     evs[0].record(stream)
     for k in range(args.e2e_steps):
+        t0 = time.perf_counter()
         one()
+        host_ms.append((time.perf_counter() - t0) * 1e3)
         evs[k + 1].record(stream)
     torch.cuda.synchronize()
     assert int(host_status.item()) == 0
     ms = evs[0].elapsed_time(evs[-1]) / args.e2e_steps
-    per_step = sorted(evs[k].elapsed_time(evs[k + 1]) for k in range(args.e2e_steps))
+    steps_ms = [evs[k].elapsed_time(evs[k + 1]) for k in range(args.e2e_steps)]
+    per_step = sorted(steps_ms)
     bytes_step = c.phase_bytes["gather"] + c.phase_bytes["scatter"]
     return {"value": round(bytes_step / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
@@ -453,6 +458,8 @@ def bench_e2e(c: Ctx, args, stream):
             "ms_per_step_median_min_max": [round(statistics.median(per_step), 3), round(per_step[0], 3),
                                            round(per_step[-1], 3)],
             "link_GBps_payload_both_ways": round(2 * c.payload / (ms * 1e-3) / 1e9, 1),
+            "steps_ms": [round(x, 2) for x in steps_ms],
+            "host_enqueue_ms": [round(x, 2) for x in host_ms],
             "host_numa": host_numa(c.dev),
             "what": "store of the batch to pinned host memory concurrent with the retrieve of an "
                     "earlier stored batch, both through the overlapped layer-wise pipeline (kernel "
@@ -1360,7 +1367,7 @@ def main():
     breakdown, _, _ = phase_summary(c, per_phase, peak)
     breakdown["per_layer_plain_copy"] = plain_copy_per_layer(c, stream)
     context = context_gathers(c, stream) if not args.no_context else None
-    e2e = bench_e2e(c, args, stream)
+    e2e = bench_e2e(c, args, stream) if not args.no_e2e else None
     pipeline = bench_layer_pipeline(c) if not args.no_pipeline else None
     decode = bench_decode_store(c) if not args.no_pipeline else None
     cachegen = bench_cachegen(c, clk.get("sm_mhz") if clk else None) if not args.no_cachegen else None

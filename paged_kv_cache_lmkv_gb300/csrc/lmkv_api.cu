@@ -623,81 +623,8 @@ int launch_hybrid(const Call& c, float* scales, cudaStream_t stream, int64_t hsm
     });
 }
 
-// Persistent quantiser: clusters of 4 CTAs of 512 threads, one CTA per SM;
-// per tile each thread holds 4 pairs of 16-byte vectors in registers and 4 in
-// shared memory, twice over (two tiles in flight): 128 KiB of shared memory.
-constexpr int kPersistThreads = 512;
-constexpr int kPersistPairs = 4;
-constexpr int kPersistCluster = 4;
-constexpr int64_t kPersistSmem = 2 * (int64_t)kPersistPairs * kPersistThreads * 32;
-
-// Whether every CTA's slice of a tile fits the persistent kernel's registers
-// and one shared-memory stage (rows of whole 32-byte pairs).
-bool persistent_fits(const Call& c) {
-    const int64_t row = (int64_t)c.pool->num_kv_heads * c.pool->head_dim * c.pool->elem_bytes;
-    if (row % 32 != 0) return false;
-    const int64_t reg_rows = (int64_t)kPersistThreads * kPersistPairs / (row / 32);
-    const int64_t rows = (c.chunk_size + kPersistCluster - 1) / kPersistCluster;
-    return reg_rows >= 1 && rows <= 2 * reg_rows;
-}
-
-// Clusters of the persistent quantiser resident at once (occupancy query,
-// cached per device after the first call made outside a stream capture); 0
-// while unknown or if the query fails, and the caller then uses the
-// one-tile-per-cluster kernel.
-template <class Kernel>
-int32_t persistent_clusters(Kernel kernel, cudaStream_t stream) {
-    static std::atomic<int32_t> cache[64];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
-        (void)cudaGetLastError();
-        return 0;
-    }
-    const int32_t v = cache[dev].load(std::memory_order_relaxed);
-    if (v != 0) return v > 0 ? v : 0;
-    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
-        (void)cudaGetLastError();
-        return 0;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kPersistCluster * 256, 1, 1);
-    cfg.blockDim = dim3(kPersistThreads, 1, 1);
-    cfg.dynamicSmemBytes = (size_t)kPersistSmem;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) {
-        (void)cudaGetLastError();
-        cache[dev].store(-1, std::memory_order_relaxed);
-        return 0;
-    }
-    cache[dev].store(n, std::memory_order_relaxed);
-    return n;
-}
-
-// The persistent quantiser for this call, if it applies (LMKV_OK with
-// *launched = true), else *launched = false and nothing is enqueued.
-template <class B>
-int launch_persistent(const Call& c, float* scales, cudaStream_t stream, bool* launched) {
-    *launched = false;
-    if (!persistent_fits(c)) return LMKV_OK;
-    auto kern = lmkv::quant_gather_persistent_kernel<B, kPersistThreads, kPersistPairs, kPersistCluster>;
-    static std::atomic<int> smem_cache[64];
-    if (!ensure_smem(kern, kPersistSmem, smem_cache)) return LMKV_OK;
-    const int32_t clusters = persistent_clusters(kern, stream);
-    if (clusters <= 0) return LMKV_OK;
-    *launched = true;
-    return for_each_block<B>(c, scales, [&](const B& b) {
-        const int64_t tiles = (int64_t)b.num_chunks * 2 * b.layer_n;
-        const int64_t ncl = tiles < clusters ? tiles : clusters;
-        return launch_pdl_smem(kern, ncl * kPersistCluster, kPersistThreads, kPersistSmem, stream, b);
-    });
-}
-
 template <class B>
 int launch_quant(const Call& c, float* scales, cudaStream_t stream) {
-    bool launched = false;
-    const int rc = launch_persistent<B>(c, scales, stream, &launched);
-    if (launched || rc != LMKV_OK) return rc;
     if (c.chunk_size <= kQuantCluster * lmkv::kQuantMaxRows) {
         const int64_t h = quant_hybrid_smem_bytes(c, kQuantCluster);
         if (h <= kQuantSmemMax) return launch_hybrid<B, kQuantCluster>(c, scales, stream, h);

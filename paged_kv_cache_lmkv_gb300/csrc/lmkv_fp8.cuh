@@ -752,253 +752,3 @@ dequant_scatter_kernel(const __grid_constant__ B p, int64_t num_items) {
 }
 
 }  // namespace lmkv
-
-namespace lmkv {
-
-// ---------------------------------------------------------------------------
-// Persistent quantising gather.  A cluster of kCluster CTAs (one CTA per SM,
-// kThreads threads) walks the tiles t = cluster, cluster + clusters, ...; CTA
-// `rank` owns rows [rank*R, rank*R + R) of each tile (R = ceil(n_g /
-// kCluster)).  Per tile every thread holds kPairs 32-byte pairs of its slice
-// in registers and kPairs more in shared memory (16-byte cp.async copies that
-// the thread itself reads back, so no CTA barrier orders them), and the slice
-// is read from HBM once.  Two buffers of each: the next tile's loads are
-// issued before the current tile is reduced, its maxima exchanged across the
-// cluster through distributed shared memory, and its codes written, so the
-// loads of one tile are in flight while the SM works on the other.  Copies
-// complete through cp.async.wait_group (a hardware wait: no spin loop, and
-// no CTA can leave with copies in flight).
-__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* gsrc) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(saddr), "l"(gsrc) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_prev() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
-// 32-byte load of a pair of 16-byte vectors (streaming, no L1 allocation);
-// volatile so that the compiler keeps it where the next tile's loads are
-// issued rather than sinking it towards its use.
-__device__ __forceinline__ void ld_pair(const uint8_t* src, uint4& a, uint4& b) {
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w) : "l"(src));
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w) : "l"(src + 16));
-}
-
-// One tile as one CTA of its cluster sees it.
-struct QTile {
-    const uint8_t* kv_base;     // pool layer l, K or V half (null: bad pointer)
-    const int32_t* bt;          // the chunk's block-table entries
-    uint8_t* codes;             // the CTA's first code byte (null: bad pointer)
-    uint32_t r0, nrows, h;      // first row, rows, rows held in registers
-    int32_t gl, kv, l;
-};
-
-template <int kCluster, class B>
-__device__ __forceinline__ QTile make_qtile(const B& p, uint32_t tile, uint32_t rank, uint32_t reg_rows) {
-    QTile t;
-    const uint32_t ll = tile % (uint32_t)p.layer_n;
-    t.kv = (int32_t)((tile / (uint32_t)p.layer_n) & 1u);
-    t.gl = (int32_t)(tile / (uint32_t)p.layer_n / 2u);
-    t.l = p.layer_lo + (int32_t)ll;
-    const ChunkRef c = resolve_chunk(p, t.gl);
-    const uint32_t rows_per = (uint32_t)(c.ntok + kCluster - 1) / kCluster;
-    t.r0 = rank * rows_per;
-    t.nrows = (uint32_t)max(0, min(c.ntok, (int)(t.r0 + rows_per)) - (int)t.r0);
-    t.h = min(t.nrows, reg_rows);
-    uint8_t* codes = p.chunk_ptrs[p.chunk_base + t.gl];
-    const uint8_t* lb = p.layer_base[t.l];
-    const bool ok = codes != nullptr && lb != nullptr &&
-                    ((reinterpret_cast<uintptr_t>(codes) | reinterpret_cast<uintptr_t>(lb)) & 15) == 0;
-    t.kv_base = ok ? lb + (int64_t)t.kv * p.num_blocks * p.block_size * p.row_bytes : nullptr;
-    t.codes = ok ? codes + (((int64_t)t.kv * p.num_layers + t.l) * c.ntok + t.r0) * (p.row_bytes >> 1) : nullptr;
-    t.bt = p.block_table + (int64_t)c.req_row * p.bt_stride + c.col0;
-    return t;
-}
-
-template <class B, int kThreads, int kPairs, int kCluster>
-__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
-quant_gather_persistent_kernel(const __grid_constant__ B p) {
-    namespace cg = cooperative_groups;
-    cg::cluster_group cluster = cg::this_cluster();
-    extern __shared__ __align__(128) uint8_t stage_mem[];     // [2][kPairs][kThreads] pairs of 32 bytes
-    constexpr int kWarps = kThreads / 32;
-    constexpr int kSlots = kCluster * kWarps;
-    __shared__ uint32_t warp_max[2][2][kWarps];               // [tile parity][exchange round][warp]
-    pdl_launch_dependents();
-    pdl_wait();
-
-    const uint32_t rank = cluster.block_rank();
-    const uint32_t clusters = gridDim.x / kCluster;
-    const uint32_t ntiles = (uint32_t)p.num_chunks * 2u * (uint32_t)p.layer_n;
-    const uint32_t row_bytes = (uint32_t)p.row_bytes;
-    const uint32_t ppr = row_bytes >> 5;                      // 32-byte pairs per row (row_bytes % 32 == 0)
-    const UDiv pdiv(ppr), bdiv((uint32_t)p.block_size);
-    const uint32_t reg_rows = (uint32_t)(kThreads * kPairs) / ppr;
-    const uint32_t bs = (uint32_t)p.block_size, nblk = (uint32_t)p.num_blocks;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const uint32_t stage_base = smem_addr(stage_mem);
-    constexpr uint32_t kStageBytes = (uint32_t)kPairs * kThreads * 32u;
-
-    uint4 regs[2][kPairs][2];
-    uint32_t rvalid[2] = {0, 0}, svalid[2] = {0, 0};
-
-    // Source of pair j of the slice (row j / ppr), or null for a bad block.
-    auto pair_src = [&](const QTile& t, uint32_t j) -> const uint8_t* {
-        const uint32_t row = pdiv.div(j);
-        const uint32_t tr = t.r0 + row;
-        const uint32_t jb = bdiv.div(tr);
-        const int32_t blk = t.bt[jb];
-        if ((uint32_t)blk >= nblk) return nullptr;
-        return t.kv_base + ((int64_t)blk * bs + (tr - jb * bs)) * row_bytes + (j - row * ppr) * 32u;
-    };
-
-    // Issue tile `tile`'s loads into buffer kB: registers and shared memory.
-    auto issue = [&](auto kb, uint32_t tile) {
-        constexpr int kB = decltype(kb)::value;
-        rvalid[kB] = svalid[kB] = 0;
-        bool bad = false;
-        if (tile < ntiles) {
-            const QTile t = make_qtile<kCluster>(p, tile, rank, reg_rows);
-            const uint32_t nreg = t.h * ppr, nall = t.nrows * ppr;
-#pragma unroll
-            for (int u = 0; u < kPairs; ++u) {
-                const uint32_t j = threadIdx.x + u * kThreads;
-                if (t.kv_base != nullptr && j < nreg) {
-                    const uint8_t* src = pair_src(t, j);
-                    if (src == nullptr) bad = true;
-                    else { ld_pair(src, regs[kB][u][0], regs[kB][u][1]); rvalid[kB] |= 1u << u; }
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < kPairs; ++u) {
-                const uint32_t j = nreg + threadIdx.x + u * kThreads;
-                if (t.kv_base != nullptr && j < nall) {
-                    const uint8_t* src = pair_src(t, j);
-                    if (src == nullptr) {
-                        bad = true;
-                    } else {
-                        const uint32_t dst = stage_base + kB * kStageBytes + (threadIdx.x + u * kThreads) * 32u;
-                        cp_async16(dst, src);
-                        cp_async16(dst + 16, src + 16);
-                        svalid[kB] |= 1u << u;
-                    }
-                }
-            }
-        }
-        cp_async_commit();
-        if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) report(p, kStatusBadBlock);
-    };
-
-    auto smem_pair = [&](int kB, int u, uint4& a, uint4& b) {
-        const uint8_t* s = stage_mem + kB * kStageBytes + (threadIdx.x + u * kThreads) * 32u;
-        a = *reinterpret_cast<const uint4*>(s);
-        b = *reinterpret_cast<const uint4*>(s + 16);
-    };
-
-    // CTA-slice absmax of buffer kB into warp_max[par][round].
-    auto slice_absmax = [&](auto kb, auto nan_prop, uint32_t par, int round) {
-        constexpr int kB = decltype(kb)::value;
-        constexpr bool kNP = decltype(nan_prop)::value;
-        uint32_t acc = 0;
-#pragma unroll
-        for (int u = 0; u < kPairs; ++u) {
-            if ((rvalid[kB] >> u) & 1u) {
-                acc = absmax_bf16x8<kNP>(acc, regs[kB][u][0]);
-                acc = absmax_bf16x8<kNP>(acc, regs[kB][u][1]);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kPairs; ++u) {
-            if ((svalid[kB] >> u) & 1u) {
-                uint4 a, b;
-                smem_pair(kB, u, a, b);
-                acc = absmax_bf16x8<kNP>(acc, a);
-                acc = absmax_bf16x8<kNP>(acc, b);
-            }
-        }
-        const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, absmax_halves(acc));
-        if (lane == 0) warp_max[par][round][warp] = m;
-    };
-    auto exchange = [&](uint32_t par, int round) {
-        cluster_arrive_release();
-        cluster_wait_acquire();
-        uint32_t x = 0;
-#pragma unroll
-        for (int i = lane; i < kSlots; i += 32)
-            x = max(x, *cluster.map_shared_rank(&warp_max[par][round][i % kWarps], (unsigned)(i / kWarps)));
-        return __reduce_max_sync(0xFFFFFFFFu, x);
-    };
-
-    // Tile `tile` from buffer kB: absmax, exchange, scale, codes.
-    auto process = [&](auto kb, uint32_t tile, uint32_t par) {
-        constexpr int kB = decltype(kb)::value;
-        const QTile t = make_qtile<kCluster>(p, tile, rank, reg_rows);
-        slice_absmax(kb, std::true_type{}, par, 0);
-        uint32_t w = exchange(par, 0);
-        // A NaN in the tile (the same w in every CTA of the cluster): the
-        // scale comes from a second round with NaNs ignored, and the tile
-        // takes the IEEE division.
-        const bool nan_tile = w > kBf16InfBits;
-        if (nan_tile) {
-            slice_absmax(kb, std::false_type{}, par, 1);
-            w = exchange(par, 1);
-        }
-        const float scale = __fdiv_rn(__uint_as_float(w << 16), 448.0f);
-        if (rank == 0 && threadIdx.x == 0 && p.scales != nullptr)
-            p.scales[((int64_t)(p.chunk_base + t.gl) * 2 + t.kv) * p.num_layers + t.l] = scale;
-        if (t.codes == nullptr) {
-            if (rank == 0 && threadIdx.x == 0) report(p, kStatusBadPointer);
-            return;
-        }
-        const bool fast = fast_div_ok(scale, nan_tile);
-        const QuantK k = make_quant(scale, fast);
-        auto quant_pair = [&](const uint4& a, const uint4& b) -> uint4 {
-            if (scale == 0.0f) return make_uint4(0, 0, 0, 0);
-            const uint2 qa = fast ? quant_bf16x8<true>(a, k) : quant_bf16x8<false>(a, k);
-            const uint2 qb = fast ? quant_bf16x8<true>(b, k) : quant_bf16x8<false>(b, k);
-            return make_uint4(qa.x, qa.y, qb.x, qb.y);
-        };
-        const uint32_t nreg = t.h * ppr;
-#pragma unroll
-        for (int u = 0; u < kPairs; ++u) {
-            if ((rvalid[kB] >> u) & 1u) {
-                const uint32_t j = threadIdx.x + u * kThreads;
-                *reinterpret_cast<uint4*>(t.codes + (size_t)j * 16) = quant_pair(regs[kB][u][0], regs[kB][u][1]);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kPairs; ++u) {
-            if ((svalid[kB] >> u) & 1u) {
-                uint4 a, b;
-                smem_pair(kB, u, a, b);
-                const uint32_t j = nreg + threadIdx.x + u * kThreads;
-                *reinterpret_cast<uint4*>(t.codes + (size_t)j * 16) = quant_pair(a, b);
-            }
-        }
-    };
-
-    const std::integral_constant<int, 0> b0;
-    const std::integral_constant<int, 1> b1;
-    uint32_t tile = blockIdx.x / kCluster;
-    issue(b0, tile);
-    for (uint32_t par = 0; tile < ntiles; par ^= 1) {
-        // buffer 0 holds `tile`; buffer 1 gets the next one
-        issue(b1, tile + clusters);
-        cp_async_wait_prev();
-        process(b0, tile, par);
-        tile += clusters;
-        if (tile >= ntiles) break;
-        par ^= 1;
-        issue(b0, tile + clusters);
-        cp_async_wait_prev();
-        process(b1, tile, par);
-        tile += clusters;
-    }
-    cp_async_wait_all();
-    // no CTA leaves while a peer may still read its shared memory
-    cluster_arrive_release();
-    cluster_wait_acquire();
-}
-
-}  // namespace lmkv

@@ -179,15 +179,15 @@ def bf16_nan_mask(a: np.ndarray) -> np.ndarray:
 
 
 @pytest.mark.parametrize("shape", [
-    # L, H, D, B, nb, ends, C, rows per CTA.  The bench's launch shape (persistent
-    # clusters of 4: rows 0-31 of each CTA's 64 in registers, 32-63 in shared
-    # memory); 512-token chunks (one tile per cluster of 8: rows 0-7 of 64 in
-    # registers, 8-63 staged by bulk copies); 2048-token chunks (register-staged
-    # kernel, 256 rows per CTA, re-reading what does not fit)
+    # L, H, D, B, nb, ends, C, rows per CTA.  The bench's launch shape (clusters
+    # of 4: rows 0-7 of each CTA's 64 in registers, 8-63 staged in shared memory
+    # by bulk copies); 512-token chunks (clusters of 8, the same split of 64
+    # rows); 2048-token chunks (register-staged kernel, 256 rows per CTA,
+    # re-reading what does not fit)
     (4, 8, 128, 16, 64, (512,), 256, 64),
     (4, 8, 128, 16, 96, (1024,), 512, 64),
     (2, 8, 128, 16, 256, (2048 + 700,), 2048, 256),
-], ids=["persistent", "staged", "register"])
+], ids=["cluster4", "cluster8", "register"])
 def test_non_finite_values_vs_oracle(shape):
     """NaN and infinity in register-held and shared-memory-held rows: codes and
     scales bit for bit against the oracle (a NaN is left out of the absmax and
