@@ -269,3 +269,98 @@ def test_llama8b_fp8_bench_launch_sampled():
     assert oracle.scatter_fp8(oracle.HostPool(h2, 16), tab2, s2, e2, 256, True, rc, rs) == 0
     for a, b in zip(hq.layers, h2):
         np.testing.assert_array_equal(a.view(np.uint16), b)
+
+
+def fp8_gather_call(pool, bt, w, flag, cptrs, scales, st):
+    return pkg.gather_chunks_fp8e4m3(pool, bt, w.starts, w.ends, w.chunk_size, flag, cptrs, scales, st)
+
+
+def test_bad_block_ids_vs_oracle():
+    """Out-of-range block ids: those rows take no part in the absmax and get
+    no codes (the buffers keep their fill), the status says LMKV_ERR_BAD_BLOCK,
+    and everything else equals the oracle's codes and scales."""
+    w = wl.Workload("bad8", 2, 2, 64, 4, 64, (90, 40), req_start=(0, 0), chunk_size=32)
+    table = wl.block_table(w, 1)
+    table[0, 2] = 64
+    table[0, 9] = -7
+    table[1, 0] = 1 << 30
+    pool = device_pool(w, 0)
+    bt = torch.from_numpy(table).to(DEV)
+    chunks = pkg.enumerate_chunks(w.starts, w.ends, w.chunk_size, True)
+    codes, cptrs = alloc_chunks(chunks, w, dtype=torch.uint8, fill=0xEE)
+    scales = torch.full((len(chunks), 2, w.num_layers), -1.0, dtype=torch.float32, device=DEV)
+    st = new_status()
+    pkg.check(fp8_gather_call(pool, bt, w, True, cptrs, scales, st))
+    torch.cuda.synchronize()
+    assert st.item() == pkg.lmkv.ERR_BAD_BLOCK
+    host = [host_u16(t) for t in pool.layers]
+    rc = [np.full((2, w.num_layers, n, w.row_elems), 0xEE, np.uint8) for _, _, n in chunks]
+    rs = np.full((len(chunks), 2, w.num_layers), -1.0, np.float32)
+    assert oracle.gather_fp8(oracle.HostPool(host, 4), table, w.starts, w.ends, w.chunk_size, True,
+                             rc, rs) == oracle.BAD_BLOCK
+    np.testing.assert_array_equal(scales.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+    for g, (a, b) in enumerate(zip(codes, rc)):
+        np.testing.assert_array_equal(a.cpu().numpy(), b, err_msg=f"codes chunk {g}")
+
+
+def test_null_code_pointer_reported():
+    """A null code pointer: LMKV_ERR_BAD_POINTER; that chunk gets no codes and
+    its tiles' scales are 0 (nothing of the tile is read); the other chunk
+    equals the oracle."""
+    w = wl.TINY
+    pool = device_pool(w, 0)
+    table = wl.block_table(w, 0)
+    bt = torch.from_numpy(table).to(DEV)
+    chunks = pkg.enumerate_chunks(w.starts, w.ends, 256, True)
+    codes, cptrs = alloc_chunks(chunks, w, dtype=torch.uint8, fill=0xEE)
+    cptrs[1] = 0
+    scales = torch.full((len(chunks), 2, w.num_layers), -1.0, dtype=torch.float32, device=DEV)
+    st = new_status()
+    pkg.check(fp8_gather_call(pool, bt, w, True, cptrs, scales, st))
+    torch.cuda.synchronize()
+    assert st.item() == pkg.lmkv.ERR_BAD_POINTER
+    assert (codes[1] == 0xEE).all()
+    assert (scales[1] == 0).all()
+    host = [host_u16(t) for t in pool.layers]
+    rc = [np.zeros((2, w.num_layers, 256, w.row_elems), np.uint8)]
+    rs = np.zeros((1, 2, w.num_layers), np.float32)
+    assert oracle.gather_fp8(oracle.HostPool(host, w.block_size), table, [0], [256], 256, True, rc, rs) == 0
+    np.testing.assert_array_equal(scales[0].cpu().numpy().view(np.uint32), rs[0].view(np.uint32))
+    np.testing.assert_array_equal(codes[0].cpu().numpy(), rc[0])
+
+
+def test_many_requests_split_over_launches():
+    """300 requests: more than one launch's parameter block holds (256), so
+    the quantising gather and the dequantising scatter each take two
+    launches; codes, scales and the dequantised pool equal the oracle's."""
+    rng = np.random.default_rng(9)
+    ends = tuple(int(x) for x in rng.integers(0, 70, 300))
+    w = wl.Workload("many8", 2, 1, 16, 4, 6000, ends, chunk_size=16, outliers=True)
+    table, table2 = wl.block_table(w, 5), wl.block_table(w, 6)
+    pool = device_pool(w, 0)
+    bt = torch.from_numpy(table).to(DEV)
+    chunks = pkg.enumerate_chunks(w.starts, w.ends, 16, True)
+    codes, cptrs = alloc_chunks(chunks, w, dtype=torch.uint8, fill=0xEE)
+    scales = torch.full((len(chunks), 2, w.num_layers), -1.0, dtype=torch.float32, device=DEV)
+    st = new_status()
+    before = pkg.lmkv.launch_count()
+    pkg.check(fp8_gather_call(pool, bt, w, True, cptrs, scales, st))
+    assert pkg.lmkv.launch_count() - before == 2
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    host = [host_u16(t) for t in pool.layers]
+    rc = [np.full((2, w.num_layers, n, w.row_elems), 0xEE, np.uint8) for _, _, n in chunks]
+    rs = np.full((len(chunks), 2, w.num_layers), -1.0, np.float32)
+    assert oracle.gather_fp8(oracle.HostPool(host, 4), table, w.starts, w.ends, 16, True, rc, rs) == 0
+    np.testing.assert_array_equal(scales.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+    for g, (a, b) in enumerate(zip(codes, rc)):
+        np.testing.assert_array_equal(a.cpu().numpy(), b, err_msg=f"codes chunk {g}")
+    pool2 = device_pool(w, None, fill="sentinel")
+    pkg.check(pkg.scatter_chunks_fp8e4m3(pool2, torch.from_numpy(table2).to(DEV), w.starts, w.ends, 16, True,
+                                         cptrs, scales, st))
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    h2 = [np.full_like(a, wl.SENTINEL_BF16) for a in host]
+    assert oracle.scatter_fp8(oracle.HostPool(h2, 4), table2, w.starts, w.ends, 16, True, rc, rs) == 0
+    for l, (t, h) in enumerate(zip(pool2.layers, h2)):
+        np.testing.assert_array_equal(host_u16(t), h, err_msg=f"dequant layer {l}")
